@@ -1,0 +1,227 @@
+/*
+ * polyact.h -- C ABI of libpolyact: packed-polynomial activation programs for
+ * GB300 (sm_103a).
+ *
+ * Method: "Fast Polynomial Transcendentals for LLMs" (arXiv 2610.00049).
+ * Sigmoid, tanh, SiLU and exact GELU (and the derivatives used in backward)
+ * are replaced by short range-reduced polynomial programs evaluated with
+ * packed two-lane FP16 / BF16 FMAs (§3.1 analytic reduction, §3.4 packed
+ * CUDA programs), standalone or fused into a SwiGLU gate (§3.4, §5.2.4
+ * eq. 15).  A host-side constrained fitter builds the programs (§3.2).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Status: every function returns an int; POLY_OK (0) on success, a
+ *   negative POLY_E* code otherwise (poly_status_str names it).  No function
+ *   throws, aborts or prints.
+ * - Ownership: the caller owns every buffer.  The library never allocates,
+ *   frees or synchronises device memory.
+ * - Device calls (poly_act_*, poly_swiglu_*, poly_ctrl_*) take device
+ *   pointers and a CUDA stream (poly_stream_t is layout-compatible with
+ *   cudaStream_t; NULL = the legacy default stream).  They validate the
+ *   arguments on the host, enqueue one kernel and return without waiting.
+ *   A launch failure is reported as POLY_ECUDA (the CUDA error is consumed
+ *   and available through poly_last_cuda_error).
+ * - Tensors hold 16-bit elements (FP16 or BF16 bit patterns), contiguous
+ *   unless leading dimensions are given.  Any 2-byte alignment is accepted:
+ *   16-byte-aligned data takes the 128-bit vector path, a scalar head and
+ *   tail cover the rest.  Odd addresses -> POLY_EINVAL.
+ * - n == 0 (or rows == 0 / cols == 0) is a valid no-op: POLY_OK, no launch.
+ * - Aliasing: an output may be exactly the same buffer as an input (in
+ *   place).  Partial overlap of an output with any other tensor ->
+ *   POLY_EINVAL.
+ * - Arithmetic: every packed FMA / multiply rounds once to the target format,
+ *   to nearest-even, with subnormals kept; a NaN result is 0x7FFF.  Outputs
+ *   are bit-exact functions of the inputs and the installed program.
+ */
+#ifndef POLYACT_H
+#define POLYACT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *poly_stream_t;
+
+/* Target formats (§3.4: FP16 for the isolated sweep, BF16 in integrations). */
+enum { POLY_F16 = 0, POLY_BF16 = 1 };
+
+/* Functions.  Forward evaluates the function, backward its derivative. */
+enum { POLY_SIGMOID = 0, POLY_TANH = 1, POLY_SILU = 2, POLY_GELU = 3 };
+enum { POLY_FWD = 0, POLY_BWD = 1 };
+
+/* Reduction forms (§3.1 eq. 2-6, §3.3 eq. 9), with t = min(|x|, Lc):
+ *   POLY_FORM_CO  centred odd  y = 1/2 + sign(x) t (c1 + c2 t + ... + cD t^(D-1))
+ *                 sigmoid forward; SiLU' and GELU' backward
+ *   POLY_FORM_O   odd          y = sign(x) t (c1 + ... + cD t^(D-1))      tanh forward
+ *   POLY_FORM_E   even         y = c0 + c1 t + ... + cD t^D          sigmoid', tanh'
+ *   POLY_FORM_HX  x/2 + even   y = x/2 + t (c1 + ... + cD t^(D-1)) for |x| <= Lc,
+ *                              y = max(x, +0) for |x| > Lc           SiLU, GELU forward
+ * The form is fixed by (fn, dir). */
+enum { POLY_FORM_CO = 0, POLY_FORM_O = 1, POLY_FORM_E = 2, POLY_FORM_HX = 3 };
+
+enum {
+  POLY_OK = 0,
+  POLY_EINVAL = -1,   /* bad enum, null pointer with work to do, bad size,
+                         misaligned (odd) address, partial aliasing          */
+  POLY_ENOPROG = -2,  /* program descriptor inconsistent (form/degree/dtype) */
+  POLY_ECUDA = -3,    /* a CUDA call or kernel launch failed                 */
+  POLY_ENOFIT = -4    /* the fitter found no candidate passing its gates     */
+};
+
+#define POLY_MIN_DEGREE 3
+#define POLY_MAX_DEGREE 6
+#define POLY_PROGRAM_VERSION 1u
+
+/* One accepted program (§3.2).  Plain data; copy freely. */
+typedef struct poly_program {
+  int32_t fn, dir, dtype, form, degree;
+  uint16_t coef[POLY_MAX_DEGREE + 1]; /* c_0..c_D, target-format bit patterns;
+                                         c_0 = f(0) (0 for CO/O/HX forms)    */
+  uint16_t lc_bits;                   /* runtime clamp Lc in the target format */
+  double li;                          /* fit interval [0, Li] of eq. 7-8       */
+  double lc;                          /* Lc as a number                        */
+  double search_score;                /* split-rounding max abs error, §3.2 step 6 */
+  double deployed_score;              /* same grid, deployed (fused) order     */
+  double stated_max_abs_err;          /* max over every finite input of
+                                         |program - FP64 function|            */
+  double table2;                      /* Table 2 metric: real arithmetic on
+                                         20,001 points over [-Lc, Lc]          */
+  int32_t rank;                       /* split-score rank of the accepted one  */
+  uint32_t version;                   /* POLY_PROGRAM_VERSION                  */
+} poly_program;
+
+/* Search options of the fitter (§3.2 steps 1-7).  poly_fit_defaults fills:
+ * Li in {1, 1.25, ..., 12}; Lc in {1, 1.25, ..., Li + 1}; 2,000 Chebyshev
+ * nodes; 8,000 score points over [0, 12]; 8 finalists re-scored in deployed
+ * order. */
+typedef struct poly_fit_opts {
+  double li_min, li_max, li_step;
+  double lc_min, lc_step;
+  int32_t n_nodes;
+  int32_t n_score;
+  double score_hi;
+  int32_t top_k;
+} poly_fit_opts;
+
+/* ---- status / metadata ------------------------------------------------ */
+
+/* Static string naming a status code (never NULL). */
+const char *poly_status_str(int status);
+/* The CUDA error code behind the last POLY_ECUDA on this thread (0 if none). */
+int poly_last_cuda_error(void);
+/* Library ABI version (bumped when a signature or struct changes). */
+int poly_abi_version(void);
+/* Form of (fn, dir) or POLY_EINVAL. */
+int poly_form_of(int fn, int dir);
+/* Degree of the default program of (fn, dir): sigmoid D3, tanh D4, SiLU D3,
+ * GELU D5 forward; D4 for every derivative.  POLY_EINVAL on bad enums. */
+int poly_default_degree(int fn, int dir);
+
+/* ---- fitter (host only, no CUDA) ---------------------------------------- */
+
+/* Fill *opts with the defaults listed above.  POLY_EINVAL if opts is NULL. */
+int poly_fit_defaults(poly_fit_opts *opts);
+
+/* Run the constrained fit and search of §3.2 for (fn, dir, dtype, degree):
+ * eq. 8 endpoint-constrained least squares in FP64 for every Li, coefficients
+ * rounded to the target format, every Lc <= Li + 1 replayed with one rounding
+ * per multiply and per add, scored as max abs error over the score grid and
+ * gated (finite; exact P(0) = f(0); range for sigmoid/tanh/sigma'/tanh';
+ * monotone real-arithmetic replay for functions monotone on t >= 0); the
+ * top_k candidates are re-scored in the deployed fused order and the best is
+ * written to *out.  opts NULL = defaults.  Deterministic.  Host memory only.
+ * Returns POLY_EINVAL (bad enum, degree outside [3, 6], bad opts, out NULL)
+ * or POLY_ENOFIT (no candidate passed). */
+int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
+             poly_program *out);
+
+/* ---- program registry ---------------------------------------------------- */
+
+/* Install *p as the program used for (p->fn, p->dir, p->dtype) by later
+ * calls.  Validates enums, form, degree, version and that c_0 matches the
+ * form.  POLY_ENOPROG if inconsistent.  Thread-safe. */
+int poly_set_program(const poly_program *p);
+
+/* Copy the installed program for (fn, dir, dtype) into *out.  If none is
+ * installed yet, the default-degree program is fitted (poly_fit with default
+ * options, tens to hundreds of milliseconds of host time) and installed
+ * first.  Thread-safe. */
+int poly_get_program(int fn, int dir, int dtype, poly_program *out);
+
+/* Forget every installed program (defaults are re-fitted on next use). */
+int poly_reset_programs(void);
+
+/* ---- elementwise programs (§5.1.1, Table 3) ------------------------------ */
+
+/* y[i] = program_fwd(fn, dtype)(x[i]) for i < n.  x, y: device, n elements.
+ * y == x allowed.  Uses the installed (or default) forward program. */
+int poly_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n,
+                 poly_stream_t stream);
+
+/* dx[i] = dy[i] * program_bwd(fn, dtype)(x[i]) (one rounding) -- the direct
+ * derivative fit evaluated from x (§4.2).  dx may equal x or dy. */
+int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx,
+                 int64_t n, poly_stream_t stream);
+
+/* ---- SwiGLU gate (§3.4, §5.2.4 eq. 15) ------------------------------------
+ * s = installed SiLU forward program (HX form), s' = installed SiLU backward
+ * program (CO form, the centred SiLU derivative of eq. 9).
+ * Forward:   y  = s(g) * u
+ * Backward:  dg = (dy * u) * s'(g),   du = dy * s(g)      (each product rounded once)
+ * Dense: row-major [rows, cols] with leading dimensions (elements, >= cols).
+ */
+int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y,
+                    int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
+                    int64_t ldy, poly_stream_t stream);
+int poly_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy,
+                    void *dg, void *du, int64_t rows, int64_t cols, int64_t ldg,
+                    int64_t ldu, int64_t lddy, int64_t lddg, int64_t lddu,
+                    poly_stream_t stream);
+
+/* Ragged routed-expert SwiGLU: the rows of all experts are packed without
+ * padding into [cap_rows, cols] tensors (leading dimension cols); expert e
+ * owns rows [seg_off[e], seg_off[e+1]).  seg_off is a DEVICE int32 array of
+ * num_segments + 1 entries, read by the kernel (no host synchronisation):
+ * rows [max(seg_off[0], 0), min(seg_off[num_segments], cap_rows)) are
+ * processed, nothing else is touched.  status: optional device int32; when
+ * non-NULL the kernel writes 0 if seg_off is valid (seg_off[0] == 0,
+ * non-decreasing, seg_off[num_segments] <= cap_rows) and 1 otherwise. */
+int poly_swiglu_fwd_ragged(int dtype, const void *g, const void *u, void *y,
+                           const int32_t *seg_off, int num_segments,
+                           int64_t cap_rows, int64_t cols, int32_t *status,
+                           poly_stream_t stream);
+int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u,
+                           const void *dy, void *dg, void *du,
+                           const int32_t *seg_off, int num_segments,
+                           int64_t cap_rows, int64_t cols, int32_t *status,
+                           poly_stream_t stream);
+
+/* ---- MUFU-native controls (same signatures and memory schedule) ----------
+ * FP32 math on the special-function unit: sigmoid = rcp.approx(1 +
+ * ex2.approx(-x log2 e)); tanh = tanh.approx; SiLU = the overflow-safe form
+ * e = 2^(-|x| log2 e), y = (x >= 0 ? x : x e) * rcp.approx(1 + e); exact GELU
+ * = x/2 (1 + erff(x / sqrt 2)) (no special-function erf exists; erff is a
+ * CUDA-core polynomial).  Backward: sigma (1 - sigma), 1 - tanh^2,
+ * sigma (1 + x (1 - sigma)), Phi + x phi, all recomputed from x.  Results
+ * are rounded once to the target format; they are approximations of the
+ * true function, not of the polynomial programs. */
+int poly_ctrl_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n,
+                      poly_stream_t stream);
+int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy,
+                      void *dx, int64_t n, poly_stream_t stream);
+int poly_ctrl_swiglu_fwd(int dtype, const void *g, const void *u, void *y,
+                         int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
+                         int64_t ldy, poly_stream_t stream);
+int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u,
+                         const void *dy, void *dg, void *du, int64_t rows,
+                         int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,
+                         int64_t lddg, int64_t lddu, poly_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POLYACT_H */

@@ -1,0 +1,172 @@
+"""Endpoint-constrained least-squares fitter and (Li, Lc) search.
+
+TEST INFRASTRUCTURE ONLY -- see ``oracle/__init__.py``.
+
+Follows "Fast Polynomial Transcendentals for LLMs" (arXiv 2610.00049), §3.2,
+in its order:
+
+1. for each degree D and fit interval Li, solve eq. 8 in FP64: the polynomial
+   P(x) = f(0) + x (f(Li) - f(0)) / Li + sum_{j=2..D} a_j (x^j - x Li^(j-1))
+   meets both endpoint conditions of eq. 7 by construction; the a_j are the
+   least-squares solution on 2,000 Chebyshev nodes of [0, Li];
+2. convert to monomial coefficients and round every one to the target format;
+3. for each runtime clamp Lc with Lc <= Li + 1, replay the program with one
+   rounding per multiply and per add (step 4), with the same reduction, clamp,
+   sign restoration and offset as the kernel (step 5);
+4. score the maximum absolute error on 8,000 points over [0, 12] and reject
+   shape or boundary violations (step 6) and non-monotone outputs (step 7);
+5. replay the best candidates in the deployed packed-FMA order (one rounding
+   per FMA) and keep the best of those ("final acceptance", §3.2 closing
+   paragraph).
+
+Readings where the paper is silent (each also listed in the design notes):
+* Chebyshev nodes of the first kind, x_k = Li/2 (1 + cos((2k+1) pi / 4000)).
+* Li in {1, 1.25, ..., 12}, Lc in {1, 1.25, ..., Li + 1}.
+* The 8,000 points are linspace(0, 12, 8000) rounded to the target format.
+* Gates: finite outputs; exact P(0) = f(0) after rounding; outputs inside the
+  true range where its bounds are exact (sigmoid, tanh, sigma', tanh'); for
+  functions monotone on t >= 0, a monotone real-arithmetic replay along the
+  grid (rounded coefficients, clamp applied, no intermediate rounding).
+* Ties in score go to the smaller Li, then the smaller Lc.
+* The 8 best split-order candidates are re-scored in deployed order.
+* The stated error bound is the maximum over every finite target-format input
+  of |deployed output - FP64 function|.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import reference as ref
+from . import tformat as tf
+from .replay import Program, evaluate, evaluate_real
+
+N_NODES = 2000
+N_SCORE = 8000
+SCORE_HI = 12.0
+TOP_K = 8
+
+
+def chebyshev_nodes(li: float, n: int = N_NODES) -> np.ndarray:
+    """First-kind Chebyshev nodes mapped to [0, Li]."""
+    k = np.arange(n, dtype=np.float64)
+    return 0.5 * li * (1.0 + np.cos((2.0 * k + 1.0) * math.pi / (2.0 * n)))
+
+
+def fit_coefficients(fn: int, direction: int, degree: int, li: float) -> np.ndarray:
+    """FP64 monomial coefficients c_0..c_D of the eq. 8 least-squares fit."""
+    f = ref.residual(fn, direction)
+    f0 = ref.residual_at_zero(fn, direction)
+    fl = float(f(li))
+    x = chebyshev_nodes(li)
+    slope = (fl - f0) / li
+    base = f0 + x * slope
+    cols = [x ** j - x * li ** (j - 1) for j in range(2, degree + 1)]
+    A = np.stack(cols, axis=1)
+    a, *_ = np.linalg.lstsq(A, f(x) - base, rcond=None)
+    c = np.zeros(degree + 1)
+    c[0] = f0
+    c[1] = slope - sum(a[j - 2] * li ** (j - 1) for j in range(2, degree + 1))
+    for j in range(2, degree + 1):
+        c[j] = a[j - 2]
+    return c
+
+
+def score_grid(fmt: str) -> np.ndarray:
+    return tf.from_f64(np.linspace(0.0, SCORE_HI, N_SCORE), fmt)
+
+
+def _gates(fn, direction, y_bits, fmt, coef_bits, lc, x_bits):
+    """Per-row pass/fail of the shape and boundary gates (§3.2 steps 6-7).
+
+    Boundary: finite outputs, exact P(0) = f(0) after rounding, outputs inside
+    the true range where its bounds are exact.  Shape: for functions monotone
+    on t >= 0, the polynomial with its rounded coefficients, evaluated in real
+    arithmetic with the clamp, is monotone along the grid.  (Monotonicity is
+    judged before intermediate rounding: one-ulp rounding steps make the
+    rounded outputs of every candidate wiggle.)
+    """
+    y = tf.decode(y_bits, fmt)
+    ok = np.all(np.isfinite(y), axis=-1)
+    f0 = ref.residual_at_zero(fn, direction)
+    ok &= int(coef_bits[0]) == int(tf.from_f64(f0, fmt))
+    rng = ref.value_range(fn, direction)
+    if rng is not None:
+        ok &= np.all((y >= rng[0]) & (y <= rng[1]), axis=-1)
+    mono = ref.monotone_on_half(fn, direction)
+    if mono != 0:
+        form = ref.form_of(fn, direction)
+        yr = evaluate_real(form, tf.decode(np.asarray(coef_bits), fmt), lc,
+                           tf.decode(x_bits, fmt))
+        ok &= np.all(np.diff(yr, axis=-1) * mono >= 0, axis=-1)
+    return ok
+
+
+def make_program(fn, direction, fmt, degree, li, lc, coef_bits) -> Program:
+    return Program(fn=fn, direction=direction, fmt=fmt, degree=degree,
+                   li=float(li), lc=float(lc),
+                   coef=tuple(int(b) for b in coef_bits),
+                   lc_bits=int(tf.from_f64(lc, fmt)))
+
+
+def table2_metric(prog: Program) -> float:
+    """Max abs error of the rounded coefficients in real arithmetic on 20,001
+    uniform points over [-Lc, Lc] (Table 2, §4.1)."""
+    x = np.linspace(-prog.lc, prog.lc, 20001)
+    y = evaluate_real(prog.form, prog.coef_values(), prog.lc, x)
+    return float(np.max(np.abs(y - ref.function(prog.fn, prog.direction)(x))))
+
+
+def exhaustive_error(prog: Program):
+    """(max abs error, argmax bits) of the deployed program over every finite
+    target-format input."""
+    x = tf.all_patterns()
+    x = x[tf.finite_mask(x, prog.fmt)]
+    y = tf.decode(evaluate(prog.form, prog.coef, prog.lc_bits, x, prog.fmt), prog.fmt)
+    err = np.abs(y - ref.function(prog.fn, prog.direction)(tf.decode(x, prog.fmt)))
+    i = int(np.argmax(err))
+    return float(err[i]), int(x[i])
+
+
+def search(fn: int, direction: int, fmt: str, degree: int,
+           li_grid=None, lc_step: float = 0.25, top_k: int = TOP_K) -> Program:
+    """The §3.2 search; returns the accepted program (None if none passes)."""
+    if li_grid is None:
+        li_grid = [1.0 + 0.25 * i for i in range(45)]
+    x = score_grid(fmt)
+    truth = ref.function(fn, direction)(tf.decode(x, fmt))
+    form = ref.form_of(fn, direction)
+    cands = []
+    for li in li_grid:
+        cb = tf.from_f64(fit_coefficients(fn, direction, degree, li), fmt)
+        n_lc = int(round(li / lc_step)) + 1           # 1, 1+step, ..., Li+1
+        lcs = np.array([1.0 + lc_step * k for k in range(n_lc)])
+        lcb = tf.from_f64(lcs, fmt)[:, None]
+        y = evaluate(form, tuple(cb), lcb, x, fmt, fused=False)
+        ok = _gates(fn, direction, y, fmt, cb, lcs[:, None], x)
+        err = np.max(np.abs(tf.decode(y, fmt) - truth), axis=-1)
+        for k in range(n_lc):
+            if ok[k]:
+                cands.append((float(err[k]), li, float(lcs[k]), cb))
+    if not cands:
+        return None
+    cands.sort(key=lambda c: (c[0], c[1], c[2]))
+    best = None
+    for rank, (split_err, li, lc, cb) in enumerate(cands[:top_k]):
+        lcb = tf.from_f64(lc, fmt)
+        y = evaluate(form, tuple(cb), lcb, x, fmt, fused=True)
+        if not _gates(fn, direction, y[None, :], fmt, cb, lc, x)[0]:
+            continue
+        err = float(np.max(np.abs(tf.decode(y, fmt) - truth)))
+        if best is None or err < best[0]:
+            best = (err, rank, split_err, li, lc, cb)
+    if best is None:
+        return None
+    err, rank, split_err, li, lc, cb = best
+    prog = make_program(fn, direction, fmt, degree, li, lc, cb)
+    bound, at = exhaustive_error(prog)
+    prog.info = {"search_score": split_err, "deployed_score": err, "rank": rank,
+                 "stated_max_abs_err": bound, "argmax_bits": at,
+                 "table2": table2_metric(prog)}
+    return prog

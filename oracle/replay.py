@@ -1,0 +1,143 @@
+"""Replay of the polynomial programs, element by element, in three orders.
+
+TEST INFRASTRUCTURE ONLY -- see ``oracle/__init__.py``.
+
+Citations are to "Fast Polynomial Transcendentals for LLMs" (arXiv 2610.00049).
+
+A program is the reduction form (§3.1, §3.3), the coefficients c_0..c_D rounded
+to the target format T (§3.2 step 3), and the runtime clamp Lc (§3.2, eq. 2).
+With t = min(|x|, Lc) (eq. 2) and the Horner value v of the polynomial in t:
+
+  CO  centred-odd  y = 1/2 + sign(x) * t * (c_1 + c_2 t + ... + c_D t^(D-1))  (eq. 3)
+  O   odd          y =       sign(x) * t * (c_1 + ...          + c_D t^(D-1))
+  E   even         y = c_0 + c_1 t + ... + c_D t^D
+  HX  x/2 + even   y = x/2 + t * (c_1 + ... + c_D t^(D-1))  for |x| <= Lc   (eq. 6)
+                   y = max(x, +0)                           for |x| >  Lc
+
+Deployed order ("fused"): every Horner stage is one packed FMA with one
+rounding; the sign is transferred bitwise onto v; the final stage is one more
+FMA that folds in 1/2 (CO) or x/2 (HX), or a multiply by t (O).  The fitter's
+search emulator ("split", §3.2 step 4) rounds each multiply and each add
+separately in the same order.  The Table 2 metric ("real") evaluates the
+rounded coefficients without any intermediate rounding (§4.1).
+
+The backward product of a derivative program is dx = dy * y rounded once; the
+SwiGLU gate (eq. 15) is y = s(g) * u and its backward dg = (dy * u) * s'(g),
+du = dy * s(g), each product rounded once.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import tformat as tf
+from .reference import CO, E, HX, O, form_of
+
+
+@dataclass
+class Program:
+    fn: int
+    direction: int
+    fmt: str
+    degree: int
+    li: float
+    lc: float
+    coef: tuple          # c_0 .. c_D as target-format bit patterns
+    lc_bits: int
+    info: dict = field(default_factory=dict)
+
+    @property
+    def form(self) -> str:
+        return form_of(self.fn, self.direction)
+
+    def coef_values(self) -> np.ndarray:
+        return tf.decode(np.array(self.coef, dtype=np.uint16), self.fmt)
+
+
+def _half(fmt):
+    return tf.from_f64(0.5, fmt)
+
+
+def _horner(coef, t, last, fmt, fused):
+    """v = c_D; v = v*t + c_j for j = D-1 .. last."""
+    D = len(coef) - 1
+    v = np.broadcast_to(np.uint16(coef[D]), np.shape(t)).astype(np.uint16)
+    for j in range(D - 1, last - 1, -1):
+        cj = np.uint16(coef[j])
+        if fused:
+            v = tf.fma(v, t, cj, fmt)
+        else:
+            v = tf.add(tf.mul(v, t, fmt), cj, fmt)
+    return v
+
+
+def evaluate(form, coef, lc_bits, x, fmt, fused=True):
+    """Replay a program on target-format inputs ``x`` (bit patterns).
+
+    ``lc_bits`` may be an array that broadcasts against ``x`` (the fitter
+    replays many clamps at once).
+    """
+    x = np.asarray(x, dtype=np.uint16)
+    a = tf.absval(x)
+    t = tf.min_nan(a, np.asarray(lc_bits, dtype=np.uint16), fmt)       # eq. 2
+    x = np.broadcast_to(x, t.shape)
+    if form == E:
+        return _horner(coef, t, 0, fmt, fused)
+    v = _horner(coef, t, 1, fmt, fused)
+    half = _half(fmt)
+    if form == CO:
+        s = tf.xorsign(v, x)
+        return tf.fma(s, t, half, fmt) if fused else tf.add(tf.mul(s, t, fmt), half, fmt)
+    if form == O:
+        return tf.mul(tf.xorsign(v, x), t, fmt)
+    if form == HX:
+        h = tf.mul(x, half, fmt)
+        y = tf.fma(v, t, h, fmt) if fused else tf.add(tf.mul(v, t, fmt), h, fmt)
+        tail = tf.greater(a, np.asarray(lc_bits, dtype=np.uint16), fmt)
+        relu = np.where(tf.greater(x, np.uint16(0), fmt), x, np.uint16(0))
+        return np.where(tail, relu, y).astype(np.uint16)
+    raise ValueError(form)
+
+
+def forward(prog: Program, x, fused=True):
+    return evaluate(prog.form, prog.coef, prog.lc_bits, x, prog.fmt, fused)
+
+
+def backward(prog: Program, x, dy):
+    """dx = dy * y(x) for a derivative program (one rounding)."""
+    return tf.mul(dy, forward(prog, x), prog.fmt)
+
+
+def swiglu_forward(silu_prog: Program, g, u):
+    """y = s(g) * u (§5.2.4 eq. 15), one rounding for the gate product."""
+    return tf.mul(forward(silu_prog, g), u, silu_prog.fmt)
+
+
+def swiglu_backward(silu_prog: Program, dsilu_prog: Program, g, u, dy):
+    """(dg, du) = ((dy*u) * s'(g), dy * s(g)), each product rounded once."""
+    fmt = silu_prog.fmt
+    dg = tf.mul(tf.mul(dy, u, fmt), forward(dsilu_prog, g), fmt)
+    du = tf.mul(dy, forward(silu_prog, g), fmt)
+    return dg, du
+
+
+def evaluate_real(form, coef_values, lc, x):
+    """Real-arithmetic replay (FP64, no intermediate rounding): the Table 2
+    metric evaluates the rounded coefficients this way (§4.1)."""
+    x = np.asarray(x, dtype=np.float64)
+    t = np.minimum(np.abs(x), lc)
+    D = len(coef_values) - 1
+    last = 0 if form == E else 1
+    v = np.full_like(t, coef_values[D])
+    for j in range(D - 1, last - 1, -1):
+        v = v * t + coef_values[j]
+    if form == E:
+        return v
+    sv = np.where(np.signbit(x), -v, v)
+    if form == CO:
+        return 0.5 + sv * t
+    if form == O:
+        return sv * t
+    y = 0.5 * x + v * t
+    return np.where(np.abs(x) > lc, np.maximum(x, 0.0), y)

@@ -1,0 +1,169 @@
+"""Pins of the oracle fitter (oracle/fit.py).
+
+Against: the endpoint conditions of eq. 7 (exact at 0, to rounding at Li);
+the normal equations of least squares; an independent 40-digit solve of the
+same constrained problem (Lagrange multipliers, mpmath); the roots of the
+Chebyshev polynomial; the printed Table 2 values and Figure 2 configuration
+(tests/golden/); the qualitative claim of Figures 4 and 5; and the golden
+programs file being what the oracle produces today.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+from numpy.polynomial import chebyshev as cheb
+
+import golden_programs as gp
+from oracle import fit, reference as ref, tformat as tf
+from oracle.replay import evaluate
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+CASES = [(ref.SIGMOID, ref.FWD, 3, 5.0), (ref.TANH, ref.FWD, 4, 3.0),
+         (ref.SILU, ref.FWD, 3, 4.75), (ref.GELU, ref.FWD, 5, 2.25),
+         (ref.SIGMOID, ref.BWD, 4, 4.75), (ref.TANH, ref.BWD, 4, 2.25),
+         (ref.SILU, ref.BWD, 4, 7.25), (ref.SIGMOID, ref.FWD, 6, 12.0)]
+
+
+@pytest.mark.parametrize("fn,d,D,li", CASES)
+def test_endpoint_constraints_eq7(fn, d, D, li):
+    c = fit.fit_coefficients(fn, d, D, li)
+    f = ref.residual(fn, d)
+    assert c[0] == ref.residual_at_zero(fn, d)                        # P(0) = f(0)
+    pl = np.polyval(c[::-1], li)
+    assert abs(pl - float(f(li))) <= 1e-12 * max(1.0, abs(float(f(li))))   # P(Li) = f(Li)
+
+
+@pytest.mark.parametrize("fn,d,D,li", CASES)
+def test_least_squares_normal_equations(fn, d, D, li):
+    """The residual is orthogonal to every free basis term x^j - x Li^(j-1)."""
+    c = fit.fit_coefficients(fn, d, D, li)
+    x = fit.chebyshev_nodes(li)
+    r = ref.residual(fn, d)(x) - np.polyval(c[::-1], x)
+    for j in range(2, D + 1):
+        col = x ** j - x * li ** (j - 1)
+        assert abs(col @ r) <= 1e-9 * np.linalg.norm(col) * max(np.linalg.norm(r), 1e-12)
+
+
+def test_chebyshev_nodes_are_roots():
+    li = 3.7
+    x = fit.chebyshev_nodes(li, 64)
+    tn = cheb.chebval(2 * x / li - 1, [0] * 64 + [1])
+    assert np.max(np.abs(tn)) < 1e-12
+    assert np.all((x > 0) & (x < li))
+
+
+@pytest.mark.parametrize("fn,d,D,li", [(ref.SIGMOID, ref.FWD, 3, 5.0),
+                                       (ref.SIGMOID, ref.BWD, 4, 4.75)])
+def test_constrained_ls_vs_mpmath_lagrange(fn, d, D, li):
+    """Same problem solved independently: minimise ||V c - f||^2 over the full
+    monomial basis subject to P(0) = f(0), P(Li) = f(Li), via the KKT system
+    in 40-digit arithmetic."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    x = fit.chebyshev_nodes(li)[::10]          # a subsample: same problem shape
+    # the oracle on the same subsample
+    f = ref.residual(fn, d)
+    f0, fl = ref.residual_at_zero(fn, d), float(f(li))
+    base = f0 + x * (fl - f0) / li
+    A = np.stack([x ** j - x * li ** (j - 1) for j in range(2, D + 1)], 1)
+    a = np.linalg.lstsq(A, f(x) - base, rcond=None)[0]
+    c_or = np.zeros(D + 1)
+    c_or[0], c_or[1] = f0, (fl - f0) / li - sum(a[j - 2] * li ** (j - 1) for j in range(2, D + 1))
+    c_or[2:] = a
+    n = D + 1
+    V = mp.matrix([[mp.mpf(float(xi)) ** j for j in range(n)] for xi in x])
+    y = mp.matrix([mp.mpf(float(v)) for v in f(x)])
+    C = mp.matrix([[1] + [0] * D, [mp.mpf(li) ** j for j in range(n)]])
+    K = mp.zeros(n + 2, n + 2)
+    VtV = V.T * V
+    for i in range(n):
+        for j in range(n):
+            K[i, j] = 2 * VtV[i, j]
+        K[i, n], K[i, n + 1] = C[0, i], C[1, i]
+        K[n, i], K[n + 1, i] = C[0, i], C[1, i]
+    rhs = mp.matrix([2 * v for v in (V.T * y)] + [mp.mpf(f0), mp.mpf(fl)])
+    sol = mp.lu_solve(K, rhs)
+    for j in range(n):
+        assert abs(c_or[j] - float(sol[j])) <= 1e-9 * max(1.0, abs(float(sol[j])))
+
+
+def _table2_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "table2_bf16.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                d, name, D, form, v = line.split()
+                rows.append((d, name, int(D), form, float(v) * 1e-3))
+    return rows
+
+
+# How close the accepted program's Table 2 metric must come to the printed
+# value.  sigma' D4 lands on the paper's value; the others are order-of-
+# magnitude checks, because the paper's exact (Li, Lc) choice is not
+# reproducible from its text (its Lc values are off the stated 0.25 grid).
+T2_FACTOR = {("bwd", "sigmoid"): 1.02, ("fwd", "sigmoid"): 1.25, ("fwd", "tanh"): 1.5,
+             ("fwd", "silu"): 2.0, ("fwd", "gelu"): 5.0}
+
+
+@pytest.mark.parametrize("row", _table2_rows())
+def test_table2_magnitudes(row):
+    d, name, D, form, printed = row
+    fn = gp.NAMES[name]
+    direction = ref.FWD if d == "fwd" else ref.BWD
+    assert ref.form_of(fn, direction) == form
+    p = gp.get(fn, direction, "bf16", D)
+    m = fit.table2_metric(p)
+    k = T2_FACTOR[(d, name)]
+    assert printed / k <= m <= printed * k, (name, m, printed)
+
+
+def test_figure2_configuration_is_competitive():
+    """The D4 centred sigmoid at the paper's selected (Li, Lc) = (5.0,
+    5.28125) (Fig. 2b) scores at least as well, in deployed order, as the
+    program our 0.25-grid search accepts -- its Lc is one BF16 ulp above the
+    grid value 5.25."""
+    with open(os.path.join(GOLDEN, "figure2_selected.txt")) as f:
+        name, d, D, li, lc = [l for l in f if not l.startswith("#")][0].split()
+    li, lc, D = float(li), float(lc), int(D)
+    assert int(tf.from_f64(lc, "bf16")) == int(tf.from_f64(5.25, "bf16")) + 1
+    cb = tf.from_f64(fit.fit_coefficients(ref.SIGMOID, ref.FWD, D, li), "bf16")
+    p = fit.make_program(ref.SIGMOID, ref.FWD, "bf16", D, li, lc, cb)
+    err_fig2 = fit.exhaustive_error(p)[0]
+    ours = fit.search(ref.SIGMOID, ref.FWD, "bf16", D)
+    assert err_fig2 <= ours.info["stated_max_abs_err"]
+    assert err_fig2 < 6e-3
+
+
+@pytest.mark.slow
+def test_higher_degree_can_be_worse_figs_4_5():
+    """In each of the six BF16 sweeps (sigmoid, tanh, SiLU forward; their
+    derivatives backward), at least one higher-degree program has a larger
+    maximum error than a lower-degree one after replay (§5.1, Figs. 4-5)."""
+    for fn in (ref.SIGMOID, ref.TANH, ref.SILU):
+        for d in (ref.FWD, ref.BWD):
+            errs = [fit.search(fn, d, "bf16", D).info["stated_max_abs_err"] for D in (3, 4, 5, 6)]
+            assert any(errs[j] > errs[i] for i in range(4) for j in range(i + 1, 4)), (fn, d, errs)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("k", ["sigmoid.fwd.bf16.D3", "silu.bwd.f16.D4", "gelu.fwd.bf16.D5"])
+def test_golden_programs_are_current(k):
+    """tests/golden/programs.json is exactly what the oracle fitter produces."""
+    with open(gp.PATH) as f:
+        g = json.load(f)[k]
+    p = fit.search(g["fn"], g["direction"], g["fmt"], g["degree"])
+    assert (p.li, p.lc, list(p.coef), p.lc_bits) == (g["li"], g["lc"], g["coef"], g["lc_bits"])
+    assert p.info["stated_max_abs_err"] == g["stated_max_abs_err"]
+
+
+def test_search_gates_hold_on_golden_programs():
+    """Every accepted program respects the gates it was selected under."""
+    for k, p in gp.load().items():
+        x = fit.score_grid(p.fmt)
+        y = tf.decode(evaluate(p.form, p.coef, p.lc_bits, x, p.fmt), p.fmt)
+        assert np.all(np.isfinite(y))
+        rng = ref.value_range(p.fn, p.direction)
+        if rng:
+            assert y.min() >= rng[0] and y.max() <= rng[1], k
+        assert p.lc <= p.li + 1
