@@ -1,0 +1,483 @@
+"""Benchmark of the packed-polynomial activation kernels on GB300.
+
+Workload (one step): the HBM-resident isolated sweep of "Fast Polynomial
+Transcendentals for LLMs" (§4.2, Table 3) -- 268,435,456-element FP16
+tensors (512 MiB each), x ~ N(0, 3^2) with 1 % uniform in [-40, 40],
+dy ~ N(0, 1) -- through the six programs: sigmoid D3, tanh D4, SiLU D3,
+GELU D5 forward and the direct sigma' D4, tanh' D4 backward.  The inputs are
+four times larger than L2, so no L2 flush is needed between steps.
+
+Reported (one JSON line, rank 0): whole-job Gelem/s of the step (all ranks),
+the roofline of the dominant kernel against the measured HBM bandwidth, the
+same six programs through the MUFU-native control kernels, torch's native
+ops, the SwiGLU kernels (dense [8192 x 14336] and ragged 131,072 x 2048 BF16)
+and the L2-resident 4,194,304-element sweep as extras, an end-to-end figure
+through the public API with host buffers, SM clocks sampled during the timed
+region, and the CPU replay oracle's throughput on a bounded sample.
+
+``--impl reference`` times the CPU replay oracle itself as the reference arm.
+Multi-GPU: one process per GPU (torchrun); every rank runs the same
+per-GPU workload with no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "Gelem/s and achieved HBM GB/s (% of roofline) per program fwd/bwd vs MUFU control"
+UNIT = "Gelem/s"
+WORKLOAD = "HBM-resident isolated sweep: 268,435,456-element FP16 tensors, six programs"
+SIX = [("sigmoid", 0, 3), ("tanh", 0, 4), ("silu", 0, 3), ("gelu", 0, 5),
+       ("sigmoid", 1, 4), ("tanh", 1, 4)]
+FN = {"sigmoid": 0, "tanh": 1, "silu": 2, "gelu": 3}
+BYTES = {0: 4, 1: 6}            # algorithmic bytes per element: fwd x + y, bwd x + dy + dx
+KERNEL_SOURCES = ["stream_kernel.cuh", "poly_ops.cuh", "packed.cuh", "kern_act.cu",
+                  "kern_swiglu.cu", "kern_common.cu"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "polynomial_activation_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key:
+                if parts[2] == src:
+                    return int(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            v = [s.strip() for s in line.split(",")]
+            if len(v) < 7:
+                continue
+            try:
+                sm.append(float(v[0]))
+                smax.append(float(v[1]))
+            except ValueError:
+                continue
+            for nm, flag in zip(names, v[3:7]):
+                if flag.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample_time(n_sample):
+    """Time the CPU replay oracle on the first n_sample elements of the
+    workload for each of the six programs; returns (seconds, elements)."""
+    from oracle import fit
+    from oracle.replay import backward, forward
+    x, dy = workloads.isolated_hbm("f16", n=n_sample)
+    progs = [fit.search(FN[name], d, "f16", D) for name, d, D in SIX]
+    t0 = time.perf_counter()
+    for p, (name, d, D) in zip(progs, SIX):
+        if d == 0:
+            forward(p, x)
+        else:
+            backward(p, x, dy)
+    return time.perf_counter() - t0, 6 * n_sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = int(np.clip(2 ** 23 // max(1, args.steps + args.warmup), 2 ** 12, 2 ** 20))
+    from oracle import fit
+    from oracle.replay import backward, forward
+    x, dy = workloads.isolated_hbm("f16", n=per_step)
+    progs = [fit.search(FN[name], d, "f16", D) for name, d, D in SIX]
+
+    def step():
+        for p, (name, d, D) in zip(progs, SIX):
+            forward(p, x) if d == 0 else backward(p, x, dy)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = 6 * per_step * args.steps / dt / 1e9
+    sample = f"first {per_step} elements of x and dy per program per step (CPU replay oracle, numpy)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "elements_per_program": per_step,
+                       "note": "bounded sample of the workload; the oracle is a deliberately "
+                               "plain CPU replay"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="only the timed step")
+    ap.add_argument("--cpu-sample", type=int, default=1 << 20)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from polynomial_activation_gb300 import binding as B
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = peaks()
+
+    # ---- inputs (host generation once, then resident in HBM)
+    xh, dyh = workloads.isolated_hbm("f16")
+    n = xh.size
+    x = torch.from_numpy(xh.view(np.int16)).to(dev).view(torch.float16)
+    dy = torch.from_numpy(dyh.view(np.int16)).to(dev).view(torch.float16)
+    outs = [torch.empty_like(x) for _ in SIX]
+    for name, d, D in SIX:                      # fit / install programs outside timing
+        assert B.poly_get_program(FN[name], d, B.POLY_F16).degree == D
+
+    def launch(i, ctrl=False):
+        name, d, D = SIX[i]
+        if d == 0:
+            (B.poly_ctrl_act_fwd if ctrl else B.poly_act_fwd)(FN[name], B.POLY_F16, x, outs[i], n)
+        else:
+            (B.poly_ctrl_act_bwd if ctrl else B.poly_act_bwd)(FN[name], B.POLY_F16, x, dy, outs[i], n)
+
+    def timed_steps(ctrl, steps, per_kernel=True):
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in SIX] for _ in range(steps)] if per_kernel else None
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(steps):
+            for i in range(len(SIX)):
+                if per_kernel:
+                    ev[s][i][0].record(stream)
+                launch(i, ctrl)
+                if per_kernel:
+                    ev[s][i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        total_ms = t_start.elapsed_time(t_end)
+        per = None
+        if per_kernel:
+            per = [sum(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)) / steps
+                   for i in range(len(SIX))]
+        return total_ms, per
+
+    for _ in range(args.warmup):
+        for i in range(len(SIX)):
+            launch(i)
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_ms, per_ms = timed_steps(False, args.steps)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    elems_per_step = 6 * n * world
+    value = elems_per_step / (ms_per_step * 1e-3) / 1e9
+
+    result = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+              "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "f16", "data": "synthetic",
+              "config": {"workload": WORKLOAD, "elements": n, "programs": [f"{a}.{'bwd' if d else 'fwd'}.D{D}" for a, d, D in SIX],
+                         "l2": "inputs (512 MiB per tensor) larger than L2; no flush",
+                         "parallelism": f"replicas x{world}, no collective"},
+              "gpu_launches": len(SIX) * args.steps,
+              "clocks": clk}
+
+    # ---- per program: poly vs MUFU control vs torch native
+    for _ in range(args.warmup):
+        for i in range(len(SIX)):
+            launch(i, ctrl=True)
+    ctrl_total, ctrl_ms = timed_steps(True, max(20, args.steps // 4))
+    programs = {}
+    torch_fns = {"sigmoid": torch.sigmoid, "tanh": torch.tanh,
+                 "silu": torch.nn.functional.silu, "gelu": torch.nn.functional.gelu}
+    for i, (name, d, D) in enumerate(SIX):
+        key = f"{name}.{'bwd' if d else 'fwd'}.D{D}"
+        gb = BYTES[d] * n / 1e9
+        entry = {"poly_ms": per_ms[i], "poly_gelem_s": n / per_ms[i] / 1e6,
+                 "poly_gbs": gb / per_ms[i] * 1e3, "poly_frac": gb / per_ms[i] * 1e3 / peak,
+                 "ctrl_ms": ctrl_ms[i], "ctrl_gbs": gb / ctrl_ms[i] * 1e3,
+                 "speedup_vs_ctrl": ctrl_ms[i] / per_ms[i]}
+        if not args.no_extras:
+            if d == 0:
+                fnat = lambda: torch_fns[name](x)
+            elif name == "sigmoid":
+                ysav = torch.sigmoid(x)
+                fnat = lambda: dy * ysav * (1 - ysav)
+            else:
+                ysav = torch.tanh(x)
+                fnat = lambda: dy * (1 - ysav * ysav)
+            for _ in range(3):
+                fnat()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 10
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                fnat()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            entry["torch_native_ms"] = e0.elapsed_time(e1) / reps
+            entry["speedup_vs_torch"] = entry["torch_native_ms"] / per_ms[i]
+        programs[key] = entry
+    result["programs"] = programs
+
+    # ---- roofline of the dominant kernel
+    dom = max(range(len(SIX)), key=lambda i: per_ms[i])
+    name, d, D = SIX[dom]
+    kkey = f"{name}.{'bwd' if d else 'fwd'}.D{D}"
+    ach = BYTES[d] * n / (per_ms[dom] * 1e-3) / 1e9
+    result["roofline"] = {"kernel": f"stream_kernel<OpBwd|OpFwd> {kkey}", "bound": "hbm",
+                          "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                          "algorithmic_bytes_per_launch": BYTES[d] * n,
+                          "traffic": recorded_traffic(kkey),
+                          "share_of_step": per_ms[dom] / sum(per_ms)}
+
+    # ---- extras: SwiGLU and the L2-resident sweep
+    if not args.no_extras:
+        result["swiglu"] = swiglu_extras(args, dev, stream, peak)
+        result["l2_resident"] = l2_extras(dev, stream)
+
+    # ---- end to end through the public API with host buffers
+    result["e2e"] = e2e(args, dev, stream, xh, dyh)
+
+    # ---- CPU oracle on a bounded sample
+    if rank == 0:
+        secs, elems = oracle_sample_time(args.cpu_sample)
+        result["cpu_baseline"] = {"value": elems / secs / 1e9, "unit": UNIT, "cores": 1,
+                                  "kind": "oracle",
+                                  "sample": f"first {args.cpu_sample} elements of the workload "
+                                            f"through each of the six programs (numpy replay, "
+                                            f"{secs:.1f} s)"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _time(fn, stream, reps, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def swiglu_extras(args, dev, stream, peak):
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    out = {}
+    bf = B.POLY_BF16
+    g, u, dy = workloads.dense_swiglu("bf16")
+    t = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    gd, ud, dyd = t(g), t(u), t(dy)
+    del g, u, dy
+    y, dg, du = torch.empty_like(gd), torch.empty_like(gd), torch.empty_like(gd)
+    n = gd.numel()
+    reps = 20
+    for label, fn, nbytes in [
+        ("dense_fwd", lambda: B.poly_swiglu_fwd(bf, gd, ud, y), 6),
+        ("dense_fwd_ctrl", lambda: B.poly_ctrl_swiglu_fwd(bf, gd, ud, y), 6),
+        ("dense_bwd", lambda: B.poly_swiglu_bwd(bf, gd, ud, dyd, dg, du), 10),
+        ("dense_bwd_ctrl", lambda: B.poly_ctrl_swiglu_bwd(bf, gd, ud, dyd, dg, du), 10),
+        ("dense_fwd_torch", lambda: torch.nn.functional.silu(gd) * ud, 6),
+    ]:
+        ms = _time(fn, stream, reps)
+        out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
+                      "frac": nbytes * n / ms / 1e6 / peak}
+    del gd, ud, dyd, y, dg, du
+    g, u, dy, seg = workloads.ragged_swiglu("bf16")
+    gd, ud, dyd = t(g), t(u), t(dy)
+    del g, u, dy
+    segd = torch.from_numpy(seg).to(dev)
+    y, dg, du = torch.empty_like(gd), torch.empty_like(gd), torch.empty_like(gd)
+    n = gd.numel()
+    for label, fn, nbytes in [
+        ("ragged_fwd", lambda: B.poly_swiglu_fwd_ragged(bf, gd, ud, y, segd), 6),
+        ("ragged_bwd", lambda: B.poly_swiglu_bwd_ragged(bf, gd, ud, dyd, dg, du, segd), 10),
+    ]:
+        ms = _time(fn, stream, reps)
+        out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
+                      "frac": nbytes * n / ms / 1e6 / peak}
+    out["config"] = {"dense": "BF16 [8192 x 14336], gate/up 2 N(0,1), dy N(0,1)",
+                     "ragged": "BF16 131,072 x 2048 rows from 64 Zipf(1.1) segments, N(0,1.5^2)"}
+    return out
+
+
+def l2_extras(dev, stream):
+    """4,194,304-element FP16 sweep, deliberately L2-resident (no flush): the
+    regime where arithmetic, not HBM, can show (Table 3, first column)."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    xh, dyh = workloads.isolated_l2("f16")
+    x = torch.from_numpy(xh.view(np.int16)).to(dev).view(torch.float16)
+    dy = torch.from_numpy(dyh.view(np.int16)).to(dev).view(torch.float16)
+    y = torch.empty_like(x)
+    n = x.numel()
+    res = {}
+    for name, d, D in SIX:
+        key = f"{name}.{'bwd' if d else 'fwd'}.D{D}"
+        if d == 0:
+            fp = lambda: B.poly_act_fwd(FN[name], B.POLY_F16, x, y, n)
+            fc = lambda: B.poly_ctrl_act_fwd(FN[name], B.POLY_F16, x, y, n)
+        else:
+            fp = lambda: B.poly_act_bwd(FN[name], B.POLY_F16, x, dy, y, n)
+            fc = lambda: B.poly_ctrl_act_bwd(FN[name], B.POLY_F16, x, dy, y, n)
+        tp, tc = _time(fp, stream, 200, 20), _time(fc, stream, 200, 20)
+        res[key] = {"poly_us": tp * 1e3, "ctrl_us": tc * 1e3, "speedup_vs_ctrl": tc / tp,
+                    "poly_gbs": BYTES[d] * n / tp / 1e6}
+    res["config"] = "4,194,304 FP16 elements, x ~ N(0, 3^2), dy ~ N(0, 1); L2-resident by design"
+    return res
+
+
+def e2e(args, dev, stream, xh, dyh):
+    """Same step through the public API with host buffers: per step the
+    inputs are copied from pinned host memory, the six programs run, and all
+    six outputs are read back to pinned host memory."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    n = xh.size
+    xp = torch.from_numpy(xh.view(np.int16)).pin_memory()
+    dyp = torch.from_numpy(dyh.view(np.int16)).pin_memory()
+    outs_h = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in SIX]
+    x = torch.empty(n, dtype=torch.float16, device=dev)
+    dy = torch.empty(n, dtype=torch.float16, device=dev)
+    outs = [torch.empty_like(x) for _ in SIX]
+
+    def step():
+        x.view(torch.int16).copy_(xp, non_blocking=True)
+        dy.view(torch.int16).copy_(dyp, non_blocking=True)
+        for i, (name, d, D) in enumerate(SIX):
+            if d == 0:
+                B.poly_act_fwd(FN[name], B.POLY_F16, x, outs[i], n)
+            else:
+                B.poly_act_bwd(FN[name], B.POLY_F16, x, dy, outs[i], n)
+        for i in range(len(SIX)):
+            outs_h[i].copy_(outs[i].view(torch.int16), non_blocking=True)
+
+    steps = max(3, min(20, args.steps // 20))
+    ms = _time(step, stream, steps, 2)
+    return {"value": 6 * n / ms / 1e6, "unit": UNIT, "h2d_bytes_per_step": 2 * 2 * n,
+            "d2h_bytes_per_step": 6 * 2 * n, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

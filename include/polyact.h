@@ -220,6 +220,23 @@ int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u,
                          int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,
                          int64_t lddg, int64_t lddu, poly_stream_t stream);
 
+/* ---- arithmetic diagnostic ------------------------------------------------
+ * Runs one raw packed instruction over n element triples so that the
+ * target-format arithmetic the programs rely on (one rounding per FMA or
+ * multiply, nearest-even, subnormals kept, NaN results 0x7FFF, §3.2 Fig. 2c
+ * and §3.4) can be checked against an independent model, element by element:
+ *   POLY_DIAG_FMA     out = a * b + c        (fma.rn.{f16x2,bf16x2})
+ *   POLY_DIAG_MUL     out = a * b            (mul.rn)
+ *   POLY_DIAG_MIN_NAN out = min(a, b), NaN if either is NaN
+ *   POLY_DIAG_MAX     out = max(a, b)
+ *   POLY_DIAG_GT      out = 0xFFFF if a > b (ordered) else 0
+ * a, b, c, out: device arrays of n 16-bit elements (c unused except by FMA,
+ * may be NULL otherwise).  Same validation and status codes as above. */
+enum { POLY_DIAG_FMA = 0, POLY_DIAG_MUL = 1, POLY_DIAG_MIN_NAN = 2, POLY_DIAG_MAX = 3,
+       POLY_DIAG_GT = 4 };
+int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c,
+                     void *out, int64_t n, poly_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -46,10 +46,10 @@ def _u16(bits) -> np.ndarray:
 def decode(bits, fmt: str) -> np.ndarray:
     """Target-format bit patterns -> exact FP64 values."""
     b = _u16(bits)
-    if fmt == F16:
-        return b.view(np.float16).astype(np.float64)
-    if fmt == BF16:
-        with np.errstate(invalid="ignore"):    # signalling-NaN payloads
+    with np.errstate(invalid="ignore"):        # signalling-NaN payloads
+        if fmt == F16:
+            return b.view(np.float16).astype(np.float64)
+        if fmt == BF16:
             return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     raise ValueError(fmt)
 

@@ -1,0 +1,275 @@
+"""Thin ctypes binding of libpolyact (include/polyact.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, turns tensors into device pointers and sizes, passes the
+current torch CUDA stream unless one is given, and raises ``PolyError`` on a
+non-zero status.  All computation happens in the library's CUDA kernels (and,
+for ``poly_fit``, in its host fitter); there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpolyact.so")
+
+POLY_F16, POLY_BF16 = 0, 1
+POLY_SIGMOID, POLY_TANH, POLY_SILU, POLY_GELU = 0, 1, 2, 3
+POLY_FWD, POLY_BWD = 0, 1
+POLY_FORM_CO, POLY_FORM_O, POLY_FORM_E, POLY_FORM_HX = 0, 1, 2, 3
+POLY_OK, POLY_EINVAL, POLY_ENOPROG, POLY_ECUDA, POLY_ENOFIT = 0, -1, -2, -3, -4
+POLY_MAX_DEGREE = 6
+POLY_PROGRAM_VERSION = 1
+FN = {"sigmoid": POLY_SIGMOID, "tanh": POLY_TANH, "silu": POLY_SILU, "gelu": POLY_GELU}
+
+# every function declared in include/polyact.h
+EXPORTS = [
+    "poly_status_str", "poly_last_cuda_error", "poly_abi_version", "poly_form_of",
+    "poly_default_degree", "poly_fit_defaults", "poly_fit", "poly_set_program",
+    "poly_get_program", "poly_reset_programs", "poly_act_fwd", "poly_act_bwd",
+    "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
+    "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
+    "poly_diag_packed",
+]
+POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
+
+
+class PolyProgram(ctypes.Structure):
+    _fields_ = [
+        ("fn", ctypes.c_int32), ("dir", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("form", ctypes.c_int32), ("degree", ctypes.c_int32),
+        ("coef", ctypes.c_uint16 * (POLY_MAX_DEGREE + 1)), ("lc_bits", ctypes.c_uint16),
+        ("li", ctypes.c_double), ("lc", ctypes.c_double),
+        ("search_score", ctypes.c_double), ("deployed_score", ctypes.c_double),
+        ("stated_max_abs_err", ctypes.c_double), ("table2", ctypes.c_double),
+        ("rank", ctypes.c_int32), ("version", ctypes.c_uint32),
+    ]
+
+    def coefficients(self):
+        return [int(self.coef[j]) for j in range(self.degree + 1)]
+
+
+class PolyFitOpts(ctypes.Structure):
+    _fields_ = [
+        ("li_min", ctypes.c_double), ("li_max", ctypes.c_double), ("li_step", ctypes.c_double),
+        ("lc_min", ctypes.c_double), ("lc_step", ctypes.c_double),
+        ("n_nodes", ctypes.c_int32), ("n_score", ctypes.c_int32),
+        ("score_hi", ctypes.c_double), ("top_k", ctypes.c_int32),
+    ]
+
+
+class PolyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().poly_status_str(status).decode()
+        if status == POLY_ECUDA:
+            msg += f" (cudaError {lib().poly_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+_LIB = None
+
+_i, _i64, _p = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+
+
+def lib():
+    """Load libpolyact.so (built by ``__graft_entry__.build()``); fails loudly
+    if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    L.poly_status_str.restype = ctypes.c_char_p
+    L.poly_status_str.argtypes = [_i]
+    for name in ("poly_last_cuda_error", "poly_abi_version", "poly_reset_programs"):
+        getattr(L, name).restype = _i
+        getattr(L, name).argtypes = []
+    L.poly_form_of.argtypes = [_i, _i]
+    L.poly_default_degree.argtypes = [_i, _i]
+    L.poly_fit_defaults.argtypes = [ctypes.POINTER(PolyFitOpts)]
+    L.poly_fit.argtypes = [_i, _i, _i, _i, ctypes.POINTER(PolyFitOpts), ctypes.POINTER(PolyProgram)]
+    L.poly_set_program.argtypes = [ctypes.POINTER(PolyProgram)]
+    L.poly_get_program.argtypes = [_i, _i, _i, ctypes.POINTER(PolyProgram)]
+    for name in ("poly_act_fwd", "poly_ctrl_act_fwd"):
+        getattr(L, name).argtypes = [_i, _i, _p, _p, _i64, _p]
+    for name in ("poly_act_bwd", "poly_ctrl_act_bwd"):
+        getattr(L, name).argtypes = [_i, _i, _p, _p, _p, _i64, _p]
+    for name in ("poly_swiglu_fwd", "poly_ctrl_swiglu_fwd"):
+        getattr(L, name).argtypes = [_i, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p]
+    for name in ("poly_swiglu_bwd", "poly_ctrl_swiglu_bwd"):
+        getattr(L, name).argtypes = [_i, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64,
+                                     _i64, _i64, _p]
+    L.poly_swiglu_fwd_ragged.argtypes = [_i, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
+    L.poly_swiglu_bwd_ragged.argtypes = [_i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
+    L.poly_diag_packed.argtypes = [_i, _i, _p, _p, _p, _p, _i64, _p]
+    for name in EXPORTS:
+        if name not in ("poly_status_str",):
+            getattr(L, name).restype = _i
+    _LIB = L
+    return L
+
+
+# ---- marshalling helpers ----------------------------------------------------
+
+def _ptr(t):
+    """Device (or host) address of a tensor, an int address, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_of(t):
+    import torch
+    return {torch.float16: POLY_F16, torch.bfloat16: POLY_BF16}[t.dtype]
+
+
+def _check(status, where):
+    if status != POLY_OK:
+        raise PolyError(status, where)
+
+
+def _ld(t, cols):
+    """Leading dimension (elements) of a 2-D row-major view."""
+    if t is None or isinstance(t, int):
+        return cols
+    if t.dim() == 2 and t.stride(1) == 1:
+        return t.stride(0)
+    if t.is_contiguous():
+        return cols
+    raise ValueError("tensor must be row-major with unit column stride")
+
+
+# ---- entry points (same names as the C ABI) ----------------------------------
+
+def poly_fit_defaults():
+    o = PolyFitOpts()
+    _check(lib().poly_fit_defaults(ctypes.byref(o)), "poly_fit_defaults")
+    return o
+
+
+def poly_fit(fn, direction, dtype, degree, opts=None):
+    p = PolyProgram()
+    st = lib().poly_fit(fn, direction, dtype, degree,
+                        ctypes.byref(opts) if opts is not None else None, ctypes.byref(p))
+    _check(st, "poly_fit")
+    return p
+
+
+def poly_set_program(p: PolyProgram):
+    _check(lib().poly_set_program(ctypes.byref(p)), "poly_set_program")
+
+
+def poly_get_program(fn, direction, dtype):
+    p = PolyProgram()
+    _check(lib().poly_get_program(fn, direction, dtype, ctypes.byref(p)), "poly_get_program")
+    return p
+
+
+def poly_reset_programs():
+    _check(lib().poly_reset_programs(), "poly_reset_programs")
+
+
+def poly_act_fwd(fn, dtype, x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_act_fwd(fn, dtype, _ptr(x), _ptr(y), n, _stream(stream)), "poly_act_fwd")
+
+
+def poly_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_act_bwd(fn, dtype, _ptr(x), _ptr(dy), _ptr(dx), n, _stream(stream)),
+           "poly_act_bwd")
+
+
+def poly_ctrl_act_fwd(fn, dtype, x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_ctrl_act_fwd(fn, dtype, _ptr(x), _ptr(y), n, _stream(stream)),
+           "poly_ctrl_act_fwd")
+
+
+def poly_ctrl_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_ctrl_act_bwd(fn, dtype, _ptr(x), _ptr(dy), _ptr(dx), n, _stream(stream)),
+           "poly_ctrl_act_bwd")
+
+
+def _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, name):
+    rows = g.shape[0] if rows is None else rows
+    cols = g.shape[-1] if cols is None else cols
+    ldg = _ld(g, cols) if ldg is None else ldg
+    ldu = _ld(u, cols) if ldu is None else ldu
+    ldy = _ld(y, cols) if ldy is None else ldy
+    _check(cfn(dtype, _ptr(g), _ptr(u), _ptr(y), rows, cols, ldg, ldu, ldy, _stream(stream)),
+           name)
+
+
+def poly_swiglu_fwd(dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=None, ldy=None,
+                    stream=None):
+    _swiglu_fwd(lib().poly_swiglu_fwd, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream,
+                "poly_swiglu_fwd")
+
+
+def poly_ctrl_swiglu_fwd(dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=None, ldy=None,
+                         stream=None):
+    _swiglu_fwd(lib().poly_ctrl_swiglu_fwd, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream,
+                "poly_ctrl_swiglu_fwd")
+
+
+def _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, lds, stream, name):
+    rows = g.shape[0] if rows is None else rows
+    cols = g.shape[-1] if cols is None else cols
+    ts = (g, u, dy, dg, du)
+    lds = [(_ld(t, cols) if l is None else l) for t, l in zip(ts, lds)]
+    _check(cfn(dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg), _ptr(du), rows, cols, *lds,
+               _stream(stream)), name)
+
+
+def poly_swiglu_bwd(dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None, ldu=None,
+                    lddy=None, lddg=None, lddu=None, stream=None):
+    _swiglu_bwd(lib().poly_swiglu_bwd, dtype, g, u, dy, dg, du, rows, cols,
+                (ldg, ldu, lddy, lddg, lddu), stream, "poly_swiglu_bwd")
+
+
+def poly_ctrl_swiglu_bwd(dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None, ldu=None,
+                         lddy=None, lddg=None, lddu=None, stream=None):
+    _swiglu_bwd(lib().poly_ctrl_swiglu_bwd, dtype, g, u, dy, dg, du, rows, cols,
+                (ldg, ldu, lddy, lddg, lddu), stream, "poly_ctrl_swiglu_bwd")
+
+
+def poly_swiglu_fwd_ragged(dtype, g, u, y, seg_off, num_segments=None, cap_rows=None,
+                           cols=None, status=None, stream=None):
+    num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
+    cap_rows = g.shape[0] if cap_rows is None else cap_rows
+    cols = g.shape[-1] if cols is None else cols
+    _check(lib().poly_swiglu_fwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(y), _ptr(seg_off),
+                                        num_segments, cap_rows, cols, _ptr(status),
+                                        _stream(stream)), "poly_swiglu_fwd_ragged")
+
+
+def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, cap_rows=None,
+                           cols=None, status=None, stream=None):
+    num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
+    cap_rows = g.shape[0] if cap_rows is None else cap_rows
+    cols = g.shape[-1] if cols is None else cols
+    _check(lib().poly_swiglu_bwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg), _ptr(du),
+                                        _ptr(seg_off), num_segments, cap_rows, cols,
+                                        _ptr(status), _stream(stream)),
+           "poly_swiglu_bwd_ragged")
+
+
+def poly_diag_packed(op, dtype, a, b, c, out, n=None, stream=None):
+    n = a.numel() if n is None else n
+    _check(lib().poly_diag_packed(op, dtype, _ptr(a), _ptr(b), _ptr(c), _ptr(out), n,
+                                  _stream(stream)), "poly_diag_packed")

@@ -1,0 +1,64 @@
+"""Build libpolyact.so in-tree with nvcc for sm_103a (no CMake, no torch
+extension machinery): every translation unit is compiled in parallel, then
+linked into ``polynomial_activation_gb300/libpolyact.so``."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libpolyact.so")
+SOURCES = ["kern_act.cu", "kern_swiglu.cu", "kern_ctrl.cu", "kern_common.cu", "capi.cpp",
+           "fit.cpp"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# host code: no floating-point contraction, so the fitter's FP64 arithmetic is
+# the same on x86-64 and aarch64
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-ffp-contract=off",
+          "-I", os.path.join(os.path.dirname(PKG), "include")]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def cuda_lib_dir(nv: str) -> str:
+    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nv))), "lib64")
+
+
+def _compile(nv: str, src: str, extra) -> str:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+    cmd = [nv, *ARCH, *COMMON, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    return obj
+
+
+def build(verbose: bool = False, extra=()) -> str:
+    """Compile and link; returns the library path."""
+    nv = nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(lambda s: _compile(nv, s, list(extra)), SOURCES))
+    tmp = LIB + ".tmp"
+    cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+           "-Xlinker", "-rpath," + cuda_lib_dir(nv)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    if verbose:
+        print("built", LIB, file=sys.stderr)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(verbose=True)

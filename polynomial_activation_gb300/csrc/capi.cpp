@@ -1,0 +1,440 @@
+// capi.cpp -- the extern "C" boundary of libpolyact (declared in
+// include/polyact.h): argument validation, the program registry and the
+// dispatch to the CUDA launchers.  Every check happens on the host before any
+// CUDA call, so invalid arguments never reach the GPU.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/polyact.h"
+#include "fit_internal.h"
+#include "launch.h"
+
+using namespace polyact;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+std::mutex g_reg_mu;
+bool g_have[4][2][2];
+poly_program g_prog[4][2][2];
+
+bool valid_fn(int fn) { return fn >= POLY_SIGMOID && fn <= POLY_GELU; }
+bool valid_dir(int d) { return d == POLY_FWD || d == POLY_BWD; }
+bool valid_dtype(int dt) { return dt == POLY_F16 || dt == POLY_BF16; }
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return POLY_OK;
+  t_last_cuda_error = (int)e;
+  return POLY_ECUDA;
+}
+
+DevProg dev_prog(const poly_program &p) {
+  DevProg d;
+  std::memset(&d, 0, sizeof(d));
+  for (int j = 0; j <= p.degree; ++j) d.c[j] = (uint32_t)p.coef[j] * 0x00010001u;
+  d.lc = (uint32_t)p.lc_bits * 0x00010001u;
+  return d;
+}
+
+int check_program(const poly_program &p) {
+  if (!valid_fn(p.fn) || !valid_dir(p.dir) || !valid_dtype(p.dtype)) return POLY_ENOPROG;
+  if (p.degree < POLY_MIN_DEGREE || p.degree > POLY_MAX_DEGREE) return POLY_ENOPROG;
+  if (p.form != form_of_fn(p.fn, p.dir)) return POLY_ENOPROG;
+  if (p.version != POLY_PROGRAM_VERSION) return POLY_ENOPROG;
+  const bool even = p.form == POLY_FORM_E;
+  if (!even && (p.coef[0] & 0x7FFF) != 0) return POLY_ENOPROG;   // c_0 = f(0) = 0
+  return POLY_OK;
+}
+
+// Byte span [lo, hi) of a tensor.
+struct Span {
+  uintptr_t lo, hi;
+};
+
+Span span_flat(const void *p, int64_t n) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + (uintptr_t)n * 2};
+}
+
+Span span_2d(const void *p, int64_t rows, int64_t cols, int64_t ld) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + (uintptr_t)(((rows - 1) * ld + cols) * 2)};
+}
+
+bool overlaps(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Outputs may coincide exactly with an input (in place), never partially
+// overlap anything, and never overlap each other.
+bool aliasing_ok(const Span *in, int nin, const Span *out, int nout) {
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < nin; ++i) {
+      if (!overlaps(out[o], in[i])) continue;
+      if (out[o].lo == in[i].lo && out[o].hi == in[i].hi) continue;
+      return false;
+    }
+    for (int o2 = o + 1; o2 < nout; ++o2)
+      if (overlaps(out[o], out[o2])) return false;
+  }
+  return true;
+}
+
+bool even_address(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+// Flat layout: the vector path needs every stream at the same offset mod 16.
+Layout flat_layout(const void *const *ptrs, int np, int64_t n) {
+  Layout l;
+  std::memset(&l, 0, sizeof(l));
+  l.mode = kFlat;
+  l.n = n;
+  const uintptr_t m = reinterpret_cast<uintptr_t>(ptrs[0]) & 15u;
+  l.vec = 1;
+  for (int i = 1; i < np; ++i)
+    if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != m) l.vec = 0;
+  if (l.vec) {
+    int64_t head = (int64_t)(((16u - m) & 15u) >> 1);
+    l.head = head < n ? head : n;
+  } else {
+    l.head = n;
+  }
+  return l;
+}
+
+int registry_get(int fn, int dir, int dtype, poly_program *out) {
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    if (g_have[fn][dir][dtype]) {
+      *out = g_prog[fn][dir][dtype];
+      return POLY_OK;
+    }
+  }
+  poly_program p;
+  int st = poly_fit(fn, dir, dtype, poly_default_degree(fn, dir), nullptr, &p);
+  if (st != POLY_OK) return st;
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  if (!g_have[fn][dir][dtype]) {
+    g_prog[fn][dir][dtype] = p;
+    g_have[fn][dir][dtype] = true;
+  }
+  *out = g_prog[fn][dir][dtype];
+  return POLY_OK;
+}
+
+// Shared validation + layout for the dense 2-D SwiGLU calls.
+int swiglu_layout(const void *const *in, const int64_t *ld_in, int nin, void *const *out,
+                  const int64_t *ld_out, int nout, int64_t rows, int64_t cols, Layout *l) {
+  if (rows < 0 || cols < 0) return POLY_EINVAL;
+  for (int i = 0; i < nin; ++i)
+    if (ld_in[i] < cols) return POLY_EINVAL;
+  for (int i = 0; i < nout; ++i)
+    if (ld_out[i] < cols) return POLY_EINVAL;
+  if (rows == 0 || cols == 0) return 1;   // nothing to do
+  const void *all[5];
+  Span si[3], so[2];
+  for (int i = 0; i < nin; ++i) {
+    if (in[i] == nullptr || !even_address(in[i])) return POLY_EINVAL;
+    si[i] = span_2d(in[i], rows, cols, ld_in[i]);
+    all[i] = in[i];
+  }
+  for (int i = 0; i < nout; ++i) {
+    if (out[i] == nullptr || !even_address(out[i])) return POLY_EINVAL;
+    so[i] = span_2d(out[i], rows, cols, ld_out[i]);
+    all[nin + i] = out[i];
+  }
+  if (!aliasing_ok(si, nin, so, nout)) return POLY_EINVAL;
+  bool contiguous = true;
+  for (int i = 0; i < nin; ++i) contiguous &= (ld_in[i] == cols) || rows == 1;
+  for (int i = 0; i < nout; ++i) contiguous &= (ld_out[i] == cols) || rows == 1;
+  if (contiguous) {
+    *l = flat_layout(all, nin + nout, rows * cols);
+    return POLY_OK;
+  }
+  std::memset(l, 0, sizeof(*l));
+  l->mode = kStrided;
+  l->rows = rows;
+  l->cols = cols;
+  bool vec = (cols % 8) == 0;
+  for (int i = 0; i < nin; ++i) {
+    l->ld_in[i] = ld_in[i];
+    vec &= (reinterpret_cast<uintptr_t>(in[i]) & 15u) == 0 && (ld_in[i] % 8) == 0;
+  }
+  for (int i = 0; i < nout; ++i) {
+    l->ld_out[i] = ld_out[i];
+    vec &= (reinterpret_cast<uintptr_t>(out[i]) & 15u) == 0 && (ld_out[i] % 8) == 0;
+  }
+  l->vec = vec ? 1 : 0;
+  return POLY_OK;
+}
+
+int ragged_layout(const void *const *in, int nin, void *const *out, int nout,
+                  const int32_t *seg_off, int num_segments, int64_t cap_rows, int64_t cols,
+                  int32_t *status, Layout *l) {
+  if (cap_rows < 0 || cols < 0 || num_segments < 0 || seg_off == nullptr) return POLY_EINVAL;
+  if (cap_rows == 0 || cols == 0) return 1;
+  const void *all[5];
+  Span si[3], so[2];
+  const int64_t n = cap_rows * cols;
+  for (int i = 0; i < nin; ++i) {
+    if (in[i] == nullptr || !even_address(in[i])) return POLY_EINVAL;
+    si[i] = span_flat(in[i], n);
+    all[i] = in[i];
+  }
+  for (int i = 0; i < nout; ++i) {
+    if (out[i] == nullptr || !even_address(out[i])) return POLY_EINVAL;
+    so[i] = span_flat(out[i], n);
+    all[nin + i] = out[i];
+  }
+  if (!aliasing_ok(si, nin, so, nout)) return POLY_EINVAL;
+  *l = flat_layout(all, nin + nout, n);
+  l->mode = kRagged;
+  l->seg = seg_off;
+  l->nseg = num_segments;
+  l->cap_rows = cap_rows;
+  l->cols = cols;
+  l->status = status;
+  return POLY_OK;
+}
+
+int swiglu_programs(int dtype, bool need_bwd, poly_program *s, poly_program *sd) {
+  int st = registry_get(POLY_SILU, POLY_FWD, dtype, s);
+  if (st != POLY_OK) return st;
+  if (need_bwd) return registry_get(POLY_SILU, POLY_BWD, dtype, sd);
+  *sd = *s;
+  return POLY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *poly_status_str(int status) {
+  switch (status) {
+    case POLY_OK: return "POLY_OK";
+    case POLY_EINVAL: return "POLY_EINVAL: invalid argument";
+    case POLY_ENOPROG: return "POLY_ENOPROG: inconsistent program descriptor";
+    case POLY_ECUDA: return "POLY_ECUDA: CUDA call or kernel launch failed";
+    case POLY_ENOFIT: return "POLY_ENOFIT: no candidate passed the fitter's gates";
+  }
+  return "unknown status";
+}
+
+int poly_last_cuda_error(void) { return t_last_cuda_error; }
+
+int poly_abi_version(void) { return 1; }
+
+int poly_form_of(int fn, int dir) {
+  if (!valid_fn(fn) || !valid_dir(dir)) return POLY_EINVAL;
+  return form_of_fn(fn, dir);
+}
+
+int poly_default_degree(int fn, int dir) {
+  if (!valid_fn(fn) || !valid_dir(dir)) return POLY_EINVAL;
+  if (dir == POLY_BWD) return 4;
+  static const int fwd[4] = {3, 4, 3, 5};
+  return fwd[fn];
+}
+
+int poly_fit_defaults(poly_fit_opts *o) {
+  if (o == nullptr) return POLY_EINVAL;
+  o->li_min = 1.0;
+  o->li_max = 12.0;
+  o->li_step = 0.25;
+  o->lc_min = 1.0;
+  o->lc_step = 0.25;
+  o->n_nodes = 2000;
+  o->n_score = 8000;
+  o->score_hi = 12.0;
+  o->top_k = 8;
+  return POLY_OK;
+}
+
+int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
+             poly_program *out) {
+  if (!valid_fn(fn) || !valid_dir(dir) || !valid_dtype(dtype) || out == nullptr)
+    return POLY_EINVAL;
+  if (degree < POLY_MIN_DEGREE || degree > POLY_MAX_DEGREE) return POLY_EINVAL;
+  poly_fit_opts o;
+  if (opts == nullptr)
+    poly_fit_defaults(&o);
+  else
+    o = *opts;
+  if (!(o.li_min > 0) || !(o.li_step > 0) || !(o.li_max >= o.li_min) || !(o.lc_min > 0) ||
+      !(o.lc_step > 0) || o.n_nodes < degree || o.n_score < 2 || !(o.score_hi > 0) ||
+      o.top_k < 1 || o.li_max > 1e4 || (o.li_max - o.li_min) / o.li_step > 1e5)
+    return POLY_EINVAL;
+  return fit_program(fn, dir, dtype, degree, o, out);
+}
+
+int poly_set_program(const poly_program *p) {
+  if (p == nullptr) return POLY_EINVAL;
+  int st = check_program(*p);
+  if (st != POLY_OK) return st;
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  g_prog[p->fn][p->dir][p->dtype] = *p;
+  g_have[p->fn][p->dir][p->dtype] = true;
+  return POLY_OK;
+}
+
+int poly_get_program(int fn, int dir, int dtype, poly_program *out) {
+  if (!valid_fn(fn) || !valid_dir(dir) || !valid_dtype(dtype) || out == nullptr)
+    return POLY_EINVAL;
+  return registry_get(fn, dir, dtype, out);
+}
+
+int poly_reset_programs(void) {
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  std::memset(g_have, 0, sizeof(g_have));
+  return POLY_OK;
+}
+
+static int act_call(bool ctrl, int kind, int fn, int dtype, const void *x, const void *dy,
+                    void *y, int64_t n, poly_stream_t stream) {
+  if (!valid_fn(fn) || !valid_dtype(dtype) || n < 0) return POLY_EINVAL;
+  if (n == 0) return POLY_OK;
+  const bool bwd = kind == kActBwd;
+  if (x == nullptr || y == nullptr || (bwd && dy == nullptr)) return POLY_EINVAL;
+  if (!even_address(x) || !even_address(y) || (bwd && !even_address(dy))) return POLY_EINVAL;
+  Span si[2] = {span_flat(x, n), span_flat(bwd ? dy : x, n)};
+  Span so[1] = {span_flat(y, n)};
+  if (!aliasing_ok(si, bwd ? 2 : 1, so, 1)) return POLY_EINVAL;
+  const void *ptrs[3] = {x, bwd ? dy : x, y};
+  Layout l = flat_layout(ptrs, 3, n);
+  Streams s{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dy), nullptr,
+            static_cast<uint16_t *>(y), nullptr};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (ctrl) return cuda_status(launch_ctrl(kind, dtype, fn, s, l, cs));
+  poly_program p;
+  int st = registry_get(fn, bwd ? POLY_BWD : POLY_FWD, dtype, &p);
+  if (st != POLY_OK) return st;
+  DevProg d = dev_prog(p);
+  return cuda_status(launch_poly(kind, dtype, p.form, p.degree, 0, s, l, d, d, cs));
+}
+
+int poly_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n, poly_stream_t stream) {
+  return act_call(false, kActFwd, fn, dtype, x, nullptr, y, n, stream);
+}
+
+int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx, int64_t n,
+                 poly_stream_t stream) {
+  return act_call(false, kActBwd, fn, dtype, x, dy, dx, n, stream);
+}
+
+int poly_ctrl_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n,
+                      poly_stream_t stream) {
+  return act_call(true, kActFwd, fn, dtype, x, nullptr, y, n, stream);
+}
+
+int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx, int64_t n,
+                      poly_stream_t stream) {
+  return act_call(true, kActBwd, fn, dtype, x, dy, dx, n, stream);
+}
+
+static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void *u,
+                       const void *dy, void *o0, void *o1, int64_t rows, int64_t cols,
+                       const int64_t *ld_in, const int64_t *ld_out, poly_stream_t stream) {
+  if (!valid_dtype(dtype)) return POLY_EINVAL;
+  const void *in[3] = {g, u, dy};
+  void *out[2] = {o0, o1};
+  Layout l;
+  int st = swiglu_layout(in, ld_in, bwd ? 3 : 2, out, ld_out, bwd ? 2 : 1, rows, cols, &l);
+  if (st == 1) return POLY_OK;
+  if (st != POLY_OK) return st;
+  Streams s{static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(u),
+            static_cast<const uint16_t *>(dy), static_cast<uint16_t *>(o0),
+            static_cast<uint16_t *>(o1)};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int kind = bwd ? kSwigluBwd : kSwigluFwd;
+  if (ctrl) return cuda_status(launch_ctrl(kind, dtype, POLY_SILU, s, l, cs));
+  poly_program ps, pd;
+  st = swiglu_programs(dtype, bwd, &ps, &pd);
+  if (st != POLY_OK) return st;
+  return cuda_status(launch_poly(kind, dtype, ps.form, ps.degree, pd.degree, s, l,
+                                 dev_prog(ps), dev_prog(pd), cs));
+}
+
+int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
+                    int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy, poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
+  return swiglu_call(false, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo, stream);
+}
+
+int poly_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy, void *dg, void *du,
+                    int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,
+                    int64_t lddg, int64_t lddu, poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, lddy}, lo[2] = {lddg, lddu};
+  return swiglu_call(false, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
+}
+
+int poly_ctrl_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
+                         int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
+                         poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
+  return swiglu_call(true, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo, stream);
+}
+
+int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy, void *dg,
+                         void *du, int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
+                         int64_t lddy, int64_t lddg, int64_t lddu, poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, lddy}, lo[2] = {lddg, lddu};
+  return swiglu_call(true, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
+}
+
+static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const void *dy,
+                       void *o0, void *o1, const int32_t *seg_off, int num_segments,
+                       int64_t cap_rows, int64_t cols, int32_t *status, poly_stream_t stream) {
+  if (!valid_dtype(dtype)) return POLY_EINVAL;
+  const void *in[3] = {g, u, dy};
+  void *out[2] = {o0, o1};
+  Layout l;
+  int st = ragged_layout(in, bwd ? 3 : 2, out, bwd ? 2 : 1, seg_off, num_segments, cap_rows,
+                         cols, status, &l);
+  if (st == 1) return POLY_OK;
+  if (st != POLY_OK) return st;
+  poly_program ps, pd;
+  st = swiglu_programs(dtype, bwd, &ps, &pd);
+  if (st != POLY_OK) return st;
+  Streams s{static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(u),
+            static_cast<const uint16_t *>(dy), static_cast<uint16_t *>(o0),
+            static_cast<uint16_t *>(o1)};
+  return cuda_status(launch_poly(bwd ? kSwigluBwd : kSwigluFwd, dtype, ps.form, ps.degree,
+                                 pd.degree, s, l, dev_prog(ps), dev_prog(pd),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int poly_swiglu_fwd_ragged(int dtype, const void *g, const void *u, void *y,
+                           const int32_t *seg_off, int num_segments, int64_t cap_rows,
+                           int64_t cols, int32_t *status, poly_stream_t stream) {
+  return ragged_call(false, dtype, g, u, nullptr, y, nullptr, seg_off, num_segments, cap_rows,
+                     cols, status, stream);
+}
+
+int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u, const void *dy, void *dg,
+                           void *du, const int32_t *seg_off, int num_segments, int64_t cap_rows,
+                           int64_t cols, int32_t *status, poly_stream_t stream) {
+  return ragged_call(true, dtype, g, u, dy, dg, du, seg_off, num_segments, cap_rows, cols,
+                     status, stream);
+}
+
+int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c, void *out,
+                     int64_t n, poly_stream_t stream) {
+  if (op < POLY_DIAG_FMA || op > POLY_DIAG_GT || !valid_dtype(dtype) || n < 0)
+    return POLY_EINVAL;
+  if (n == 0) return POLY_OK;
+  if (op == POLY_DIAG_FMA && c == nullptr) return POLY_EINVAL;
+  if (c == nullptr) c = a;   // only FMA reads c
+  if (a == nullptr || b == nullptr || out == nullptr) return POLY_EINVAL;
+  if (!even_address(a) || !even_address(b) || !even_address(c) || !even_address(out))
+    return POLY_EINVAL;
+  Span si[3] = {span_flat(a, n), span_flat(b, n), span_flat(c, n)};
+  Span so[1] = {span_flat(out, n)};
+  if (!aliasing_ok(si, 3, so, 1)) return POLY_EINVAL;
+  const void *ptrs[4] = {a, b, c, out};
+  Layout l = flat_layout(ptrs, 4, n);
+  Streams s{static_cast<const uint16_t *>(a), static_cast<const uint16_t *>(b),
+            static_cast<const uint16_t *>(c), static_cast<uint16_t *>(out), nullptr};
+  return cuda_status(launch_diag(op, dtype, s, l, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// kern_common.cu -- launch sizing and the dispatch from the C ABI layer to
+// the per-family translation units.
+#include <mutex>
+#include <unordered_map>
+
+#include "poly_ops.cuh"
+
+namespace polyact {
+namespace dev {
+
+cudaError_t launch_act(int kind, int dtype, int form, int deg, const Streams &s,
+                       const Layout &l, const ProgPair &p, cudaStream_t st);
+cudaError_t launch_swiglu(int kind, int dtype, int ds, int dd, const Streams &s,
+                          const Layout &l, const ProgPair &p, cudaStream_t st);
+
+namespace {
+std::mutex g_mu;
+std::unordered_map<int, int> g_sms;                       // device -> SM count
+std::unordered_map<const void *, int> g_occ;              // kernel -> resident blocks / SM
+}  // namespace
+
+int64_t grid_for(const void *kernel, const Layout &l) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int sms = 0, occ = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(dev);
+    if (it == g_sms.end()) {
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      g_sms[dev] = sms;
+    } else {
+      sms = it->second;
+    }
+    auto jt = g_occ.find(kernel);
+    if (jt == g_occ.end()) {
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+      g_occ[kernel] = occ;
+    } else {
+      occ = jt->second;
+    }
+  }
+  if (sms <= 0) sms = 1;
+  if (occ <= 0) occ = 1;
+  // elements of work per block in one pass
+  int64_t work;
+  if (l.mode == kStrided)
+    work = l.vec ? l.rows * (l.cols / 8) * 8 : l.rows * l.cols;
+  else if (l.mode == kRagged)
+    work = l.cap_rows * l.cols;
+  else
+    work = l.n;
+  const int64_t per_block = (int64_t)kThreads * kUnroll * 8;
+  int64_t blocks = (work + per_block - 1) / per_block;
+  const int64_t cap = (int64_t)sms * occ;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return blocks;
+}
+
+template <int DT, int OP>
+struct OpDiag {
+  static constexpr int NIN = 3, NOUT = 1;
+  struct Params {};
+  __device__ __forceinline__ static void pair(const uint32_t (&a)[3], uint32_t (&b)[1],
+                                              const Params &) {
+    if constexpr (OP == POLY_DIAG_FMA) b[0] = pfma<DT>(a[0], a[1], a[2]);
+    else if constexpr (OP == POLY_DIAG_MUL) b[0] = pmul<DT>(a[0], a[1]);
+    else if constexpr (OP == POLY_DIAG_MIN_NAN) b[0] = pmin_nan<DT>(a[0], a[1]);
+    else if constexpr (OP == POLY_DIAG_MAX) b[0] = pmax<DT>(a[0], a[1]);
+    else b[0] = pgt_mask<DT>(a[0], a[1]);
+  }
+};
+
+template <int DT>
+static cudaError_t diag_dt(int op, const Streams &s, const Layout &l, cudaStream_t st) {
+  switch (op) {
+    case POLY_DIAG_FMA: return launch_op<OpDiag<DT, POLY_DIAG_FMA>>(s, l, {}, st);
+    case POLY_DIAG_MUL: return launch_op<OpDiag<DT, POLY_DIAG_MUL>>(s, l, {}, st);
+    case POLY_DIAG_MIN_NAN: return launch_op<OpDiag<DT, POLY_DIAG_MIN_NAN>>(s, l, {}, st);
+    case POLY_DIAG_MAX: return launch_op<OpDiag<DT, POLY_DIAG_MAX>>(s, l, {}, st);
+    case POLY_DIAG_GT: return launch_op<OpDiag<DT, POLY_DIAG_GT>>(s, l, {}, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dev
+
+cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
+                        cudaStream_t stream) {
+  return dtype == dev::kF16 ? dev::diag_dt<dev::kF16>(op, s, l, stream)
+                            : dev::diag_dt<dev::kBF16>(op, s, l, stream);
+}
+
+cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, const Streams &s,
+                        const Layout &l, const DevProg &p1, const DevProg &p2,
+                        cudaStream_t stream) {
+  dev::ProgPair pp{p1, p2};
+  if (kind == kActFwd || kind == kActBwd)
+    return dev::launch_act(kind, dtype, form1, deg1, s, l, pp, stream);
+  return dev::launch_swiglu(kind, dtype, deg1, deg2, s, l, pp, stream);
+}
+
+}  // namespace polyact

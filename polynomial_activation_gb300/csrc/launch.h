@@ -1,0 +1,61 @@
+// launch.h -- host-side launch interface between the C ABI layer and the
+// CUDA translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/polyact.h"
+
+namespace polyact {
+
+// A program as the kernels see it: every coefficient duplicated into both
+// lanes of a 32-bit register.
+struct DevProg {
+  uint32_t c[POLY_MAX_DEGREE + 1];
+  uint32_t lc;
+};
+
+// Up to three input and two output streams of 16-bit elements.
+struct Streams {
+  const uint16_t *in0, *in1, *in2;
+  uint16_t *out0, *out1;
+};
+
+enum LayoutMode { kFlat = 0, kRagged = 1, kStrided = 2 };
+
+// Where the elements are.
+//  kFlat:    n contiguous elements; `head` leading elements run scalar and the
+//            rest, if `vec`, as 16-byte chunks (all streams share alignment).
+//  kRagged:  rows [seg[0], seg[nseg]) of a [cap_rows, cols] matrix, bounds
+//            read on the device; `vec` as above for the whole allocation.
+//  kStrided: rows x cols with per-stream leading dimensions; `vec` when every
+//            row start is 16-byte aligned and cols % 8 == 0.
+struct Layout {
+  int mode;
+  int vec;
+  int64_t n, head;
+  const int32_t *seg;
+  int32_t nseg;
+  int64_t cap_rows, cols, rows;
+  int32_t *status;
+  int64_t ld_in[3], ld_out[2];
+};
+
+enum Kind { kActFwd = 0, kActBwd = 1, kSwigluFwd = 2, kSwigluBwd = 3 };
+
+// Polynomial programs.  p2 is used by kSwigluBwd only (the SiLU derivative).
+cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, const Streams &s,
+                        const Layout &l, const DevProg &p1, const DevProg &p2,
+                        cudaStream_t stream);
+
+// MUFU controls (fn used by kActFwd / kActBwd).
+cudaError_t launch_ctrl(int kind, int dtype, int fn, const Streams &s, const Layout &l,
+                        cudaStream_t stream);
+
+// Raw packed instruction over element triples (arithmetic diagnostic).
+cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
+                        cudaStream_t stream);
+
+}  // namespace polyact

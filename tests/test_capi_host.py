@@ -1,0 +1,163 @@
+"""Host-side tests of libpolyact: symbol exports, argument validation and the
+C++ fitter.  No compute call reaches the GPU: every device entry point is
+called only with arguments that fail validation (or with n == 0), which the
+library rejects on the host before any CUDA call."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import golden_programs as gp
+from polynomial_activation_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "polyact.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    return B.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(poly_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = header_functions()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(B.EXPORTS) == declared
+
+
+def test_status_strings(L):
+    for st in (B.POLY_OK, B.POLY_EINVAL, B.POLY_ENOPROG, B.POLY_ECUDA, B.POLY_ENOFIT):
+        assert L.poly_status_str(st).startswith(b"POLY_")
+    assert L.poly_status_str(12345) == b"unknown status"
+
+
+def test_forms_and_default_degrees(L):
+    assert [L.poly_form_of(f, 0) for f in range(4)] == [B.POLY_FORM_CO, B.POLY_FORM_O,
+                                                        B.POLY_FORM_HX, B.POLY_FORM_HX]
+    assert [L.poly_form_of(f, 1) for f in range(4)] == [B.POLY_FORM_E, B.POLY_FORM_E,
+                                                        B.POLY_FORM_CO, B.POLY_FORM_CO]
+    assert [L.poly_default_degree(f, 0) for f in range(4)] == [3, 4, 3, 5]
+    assert [L.poly_default_degree(f, 1) for f in range(4)] == [4, 4, 4, 4]
+    assert L.poly_form_of(7, 0) == B.POLY_EINVAL
+    assert L.poly_default_degree(0, 2) == B.POLY_EINVAL
+
+
+@pytest.mark.parametrize("k", sorted(json.load(open(gp.PATH))))
+def test_cpp_fitter_reproduces_oracle_programs(k):
+    """The library's C++ fitter (independent code: integer soft-float,
+    Householder QR) accepts exactly the program the oracle fitter accepts."""
+    g = json.load(open(gp.PATH))[k]
+    dt = B.POLY_F16 if g["fmt"] == "f16" else B.POLY_BF16
+    p = B.poly_fit(g["fn"], g["direction"], dt, g["degree"])
+    assert p.coefficients() == g["coef"]
+    assert p.lc_bits == g["lc_bits"] and p.li == g["li"] and p.lc == g["lc"]
+    assert p.form == B.lib().poly_form_of(g["fn"], g["direction"])
+    assert p.rank == g["rank"]
+    assert p.stated_max_abs_err == pytest.approx(g["stated_max_abs_err"], rel=1e-12)
+    assert p.search_score == pytest.approx(g["search_score"], rel=1e-12)
+    assert p.table2 == pytest.approx(g["table2"], rel=1e-9)
+
+
+def test_fit_is_deterministic_and_registry_roundtrip():
+    a = B.poly_fit(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16, 4)
+    b = B.poly_fit(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16, 4)
+    assert bytes(a) == bytes(b)
+    B.poly_reset_programs()
+    got = B.poly_get_program(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16)
+    assert bytes(got) == bytes(a)
+    # install a different-degree program and read it back
+    c = B.poly_fit(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16, 6)
+    B.poly_set_program(c)
+    assert B.poly_get_program(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16).degree == 6
+    B.poly_reset_programs()
+    assert B.poly_get_program(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16).degree == 4
+
+
+def test_fit_argument_errors(L):
+    p = B.PolyProgram()
+    assert L.poly_fit(9, 0, 0, 3, None, ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit(0, 2, 0, 3, None, ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit(0, 0, 5, 3, None, ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit(0, 0, 0, 2, None, ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit(0, 0, 0, 7, None, ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit(0, 0, 0, 3, None, None) == B.POLY_EINVAL
+    o = B.poly_fit_defaults()
+    o.li_step = 0.0
+    assert L.poly_fit(0, 0, 0, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_fit_defaults(None) == B.POLY_EINVAL
+    # no admissible clamp at all: Lc starts above Li + 1
+    o = B.poly_fit_defaults()
+    o.li_max, o.lc_min = 2.0, 5.0
+    assert L.poly_fit(0, 0, 1, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_ENOFIT
+
+
+def test_set_program_rejects_inconsistent_descriptors(L):
+    good = B.poly_fit(B.POLY_SIGMOID, B.POLY_FWD, B.POLY_BF16, 3)
+    for field, value in (("form", B.POLY_FORM_E), ("degree", 2), ("degree", 7),
+                         ("version", 99), ("fn", 8), ("dtype", 4)):
+        bad = B.PolyProgram.from_buffer_copy(bytes(good))
+        setattr(bad, field, value)
+        assert L.poly_set_program(ctypes.byref(bad)) == B.POLY_ENOPROG, field
+    bad = B.PolyProgram.from_buffer_copy(bytes(good))
+    bad.coef[0] = 0x3F80                                # c_0 must be 0 for the CO form
+    assert L.poly_set_program(ctypes.byref(bad)) == B.POLY_ENOPROG
+    assert L.poly_set_program(None) == B.POLY_EINVAL
+    B.poly_reset_programs()
+
+
+FAKE = 0x7F0000001000          # never dereferenced: every call below fails validation
+
+
+def test_device_calls_reject_bad_arguments_on_host(L):
+    s = None
+    # bad enums
+    assert L.poly_act_fwd(9, 0, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    assert L.poly_act_fwd(0, 3, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    # negative size, null pointers
+    assert L.poly_act_fwd(0, 0, FAKE, FAKE + 4096, -1, s) == B.POLY_EINVAL
+    assert L.poly_act_fwd(0, 0, None, FAKE, 8, s) == B.POLY_EINVAL
+    assert L.poly_act_bwd(0, 0, FAKE, None, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    # odd (misaligned for 16-bit elements) addresses
+    assert L.poly_act_fwd(0, 0, FAKE + 1, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    # partial overlap of output and input
+    assert L.poly_act_fwd(0, 0, FAKE, FAKE + 2, 8, s) == B.POLY_EINVAL
+    assert L.poly_act_bwd(0, 0, FAKE, FAKE + 4096, FAKE + 4098, 8, s) == B.POLY_EINVAL
+    # SwiGLU: ld < cols, overlapping outputs, negative rows
+    assert L.poly_swiglu_fwd(1, FAKE, FAKE + 8192, FAKE + 16384, 4, 16, 8, 16, 16, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd(1, FAKE, FAKE + 8192, FAKE + 16384, -1, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_bwd(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576, FAKE + 24578,
+                             4, 16, 16, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd(7, FAKE, FAKE + 8192, FAKE + 16384, 4, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    # ragged: null offsets, negative segments
+    assert L.poly_swiglu_fwd_ragged(1, FAKE, FAKE + 8192, FAKE + 16384, None, 4, 4, 16, None, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd_ragged(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 30000, -1, 4, 16, None, s) == B.POLY_EINVAL
+    # controls share the validation
+    assert L.poly_ctrl_act_fwd(0, 0, FAKE + 1, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    assert L.poly_ctrl_swiglu_bwd(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576, FAKE + 24578,
+                                  4, 16, 16, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    # diagnostic: FMA needs c, bad op
+    assert L.poly_diag_packed(0, 0, FAKE, FAKE + 4096, None, FAKE + 8192, 8, s) == B.POLY_EINVAL
+    assert L.poly_diag_packed(9, 0, FAKE, FAKE + 4096, FAKE, FAKE + 8192, 8, s) == B.POLY_EINVAL
+
+
+def test_empty_calls_are_no_ops(L):
+    """n == 0 / rows == 0 return POLY_OK without touching CUDA (no GPU here)."""
+    s = None
+    assert L.poly_act_fwd(0, 0, None, None, 0, s) == B.POLY_OK
+    assert L.poly_act_bwd(1, 1, None, None, None, 0, s) == B.POLY_OK
+    assert L.poly_ctrl_act_fwd(3, 1, None, None, 0, s) == B.POLY_OK
+    assert L.poly_swiglu_fwd(1, None, None, None, 0, 16, 16, 16, 16, s) == B.POLY_OK
+    assert L.poly_swiglu_bwd(1, None, None, None, None, None, 5, 0, 0, 0, 0, 0, 0, s) == B.POLY_OK
+    assert L.poly_swiglu_fwd_ragged(1, None, None, None, FAKE, 4, 0, 16, None, s) == B.POLY_OK
+    assert L.poly_diag_packed(0, 0, None, None, None, None, 0, s) == B.POLY_OK
+    assert L.poly_last_cuda_error() == 0

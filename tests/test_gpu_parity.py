@@ -1,0 +1,399 @@
+"""GPU parity: every kernel of libpolyact, called through the C ABI, against
+the CPU replay oracle, bit for bit.
+
+Cases: the raw packed instructions against the oracle's arithmetic; every
+program over all 65,536 input patterns (±0, subnormals, ±inf, NaN); sizes
+1..67 at element offsets 0..7 with guard bands; in-place calls; the
+L2-resident (4,194,304) and HBM-resident (268,435,456) FP16 sweeps at full
+size (forward: every element through the oracle's exhaustive table;
+backward: sampled elements); dense SwiGLU [8192 x 14336] BF16 (sampled) and
+small contiguous and strided cases (every element); ragged routed-expert
+SwiGLU with Zipf segments (sampled, plus untouched rows past the last
+offset and the offset-validation status).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import DEV, FMT, TDT, from_dev, guards_intact, oracle_program, sentinel_buffer, to_dev
+from oracle import reference as ref
+from oracle import tformat as tf
+from oracle.replay import backward, forward, swiglu_backward, swiglu_forward
+from polynomial_activation_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+
+DTS = [B.POLY_BF16, B.POLY_F16]
+FNS = [B.POLY_SIGMOID, B.POLY_TANH, B.POLY_SILU, B.POLY_GELU]
+PROGRAMS = [(fn, d) for fn in FNS for d in (B.POLY_FWD, B.POLY_BWD)]
+X_ALL = tf.all_patterns()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(DEV)
+    B.poly_reset_programs()
+    yield
+    torch.cuda.synchronize()
+
+
+def _rand_bits(rng, n, fmt):
+    b = rng.integers(0, 65536, n, dtype=np.uint32).astype(np.uint16)
+    k = n // 2
+    b[:k] = tf.from_f64(rng.normal(0, 4, k), fmt)
+    return b
+
+
+# ---------------------------------------------------------------- arithmetic
+
+@pytest.mark.parametrize("dt", DTS)
+def test_silicon_matches_oracle_arithmetic(dt):
+    """fma.rn / mul.rn / min.NaN / max / set.gt on random and special operands
+    equal the oracle's one-rounding model (the programs rely on nothing else)."""
+    fmt = FMT[dt]
+    rng = np.random.default_rng(100 + dt)
+    n = 1 << 20
+    a, b, c = (_rand_bits(rng, n, fmt) for _ in range(3))
+    sp = np.array([0, 0x8000, 1, 0x8001, 0x7FFF, 0xFFFF, 0x7C00 if dt == 0 else 0x7F80,
+                   0xFC00 if dt == 0 else 0xFF80, 0x3C00 if dt == 0 else 0x3F80], dtype=np.uint16)
+    for arr in (a, b, c):
+        idx = rng.random(n) < 0.03
+        arr[idx] = sp[rng.integers(0, len(sp), int(idx.sum()))]
+    da, db, dc = to_dev(a, dt), to_dev(b, dt), to_dev(c, dt)
+    out = torch.empty_like(da)
+
+    def run(op):
+        B.poly_diag_packed(op, dt, da, db, dc, out)
+        return from_dev(out)
+
+    assert np.array_equal(run(B.POLY_DIAG_FMA), tf.fma(a, b, c, fmt))
+    assert np.array_equal(run(B.POLY_DIAG_MUL), tf.mul(a, b, fmt))
+    # the clamp only ever sees min(|x|, Lc) with Lc > 0
+    da2 = to_dev(tf.absval(a), dt)
+    lc = np.full(n, int(tf.from_f64(4.75, fmt)), dtype=np.uint16)
+    B.poly_diag_packed(B.POLY_DIAG_MIN_NAN, dt, da2, to_dev(lc, dt), dc, out)
+    assert np.array_equal(from_dev(out), tf.min_nan(tf.absval(a), lc, fmt))
+    gt = run(B.POLY_DIAG_GT)
+    want_gt = np.where(tf.greater(a, b, fmt), np.uint16(0xFFFF), np.uint16(0))
+    assert np.array_equal(gt, want_gt)
+    # max(x, +0) as used by the exact tail: x away from zero and not NaN
+    zero = np.zeros(n, dtype=np.uint16)
+    ok = ~tf.is_nan(a, fmt) & (tf.decode(a, fmt) != 0)
+    B.poly_diag_packed(B.POLY_DIAG_MAX, dt, da, to_dev(zero, dt), dc, out)
+    mx = from_dev(out)
+    want = np.where(tf.decode(a, fmt) > 0, a, np.uint16(0))
+    assert np.array_equal(mx[ok], want[ok])
+
+
+# ------------------------------------------------------------- exhaustive
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("fn,d", PROGRAMS)
+def test_exhaustive_patterns(fn, d, dt):
+    """All 65,536 input patterns through every program, forward and backward."""
+    op = oracle_program(fn, d, dt)
+    x = X_ALL
+    xd = to_dev(x, dt)
+    out = torch.empty_like(xd)
+    if d == B.POLY_FWD:
+        B.poly_act_fwd(fn, dt, xd, out)
+        want = forward(op, x)
+    else:
+        dy = _rand_bits(np.random.default_rng(5), x.size, FMT[dt])
+        B.poly_act_bwd(fn, dt, xd, to_dev(dy, dt), out)
+        want = backward(op, x, dy)
+    got = from_dev(out)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(x[i]), hex(got[i]), hex(want[i])) for i in bad[:8]]
+
+
+# ------------------------------------------------------- sizes and offsets
+
+@pytest.mark.parametrize("dt", DTS)
+def test_small_sizes_offsets_and_guards(dt):
+    """n = 1..67 at element offsets 0..7 (scalar head, vector body, scalar
+    tail, unaligned fallback); nothing outside [0, n) is written."""
+    fmt = FMT[dt]
+    rng = np.random.default_rng(9)
+    ops = {(fn, d): oracle_program(fn, d, dt) for fn, d in PROGRAMS}
+    G = 64
+    for n in list(range(1, 68)) + [255, 1031]:
+        for off_x in range(8):
+            off_y = off_x if n % 3 else (off_x + 3) % 8      # sometimes mismatched alignment
+            fn, d = PROGRAMS[(n + off_x) % len(PROGRAMS)]
+            x = _rand_bits(rng, n, fmt)
+            dy = _rand_bits(rng, n, fmt)
+            xb = to_dev(np.concatenate([np.zeros(off_x, np.uint16), x]), dt)[off_x:]
+            dyb = to_dev(np.concatenate([np.zeros(off_x, np.uint16), dy]), dt)[off_x:]
+            buf, y = sentinel_buffer(n, G, dt, off_y)
+            if d == B.POLY_FWD:
+                B.poly_act_fwd(fn, dt, xb, y, n)
+                want = forward(ops[(fn, d)], x)
+            else:
+                B.poly_act_bwd(fn, dt, xb, dyb, y, n)
+                want = backward(ops[(fn, d)], x, dy)
+            assert np.array_equal(from_dev(y), want), (n, off_x, off_y, fn, d)
+            assert guards_intact(buf, n, G, off_y), (n, off_x, off_y)
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_in_place(dt):
+    fmt = FMT[dt]
+    x = _rand_bits(np.random.default_rng(3), 100_003, fmt)
+    for fn in FNS:
+        op = oracle_program(fn, B.POLY_FWD, dt)
+        t = to_dev(x, dt)
+        B.poly_act_fwd(fn, dt, t, t)
+        assert np.array_equal(from_dev(t), forward(op, x))
+        dop = oracle_program(fn, B.POLY_BWD, dt)
+        t = to_dev(x, dt)
+        dy = to_dev(x[::-1].copy(), dt)
+        B.poly_act_bwd(fn, dt, t, dy, dy)                   # dx written over dy
+        assert np.array_equal(from_dev(dy), backward(dop, x, x[::-1].copy()))
+
+
+# ------------------------------------------------------------ full configs
+
+SIX = [(B.POLY_SIGMOID, B.POLY_FWD), (B.POLY_TANH, B.POLY_FWD), (B.POLY_SILU, B.POLY_FWD),
+       (B.POLY_GELU, B.POLY_FWD), (B.POLY_SIGMOID, B.POLY_BWD), (B.POLY_TANH, B.POLY_BWD)]
+
+
+def test_l2_resident_sweep_every_element():
+    """4,194,304 FP16 elements, x ~ N(0, 3^2), dy ~ N(0, 1): all six programs,
+    every element compared."""
+    dt = B.POLY_F16
+    x, dy = workloads.isolated_l2("f16")
+    xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+    out = torch.empty_like(xd)
+    for fn, d in SIX:
+        op = oracle_program(fn, d, dt)
+        if d == B.POLY_FWD:
+            B.poly_act_fwd(fn, dt, xd, out)
+            want = forward(op, x)
+        else:
+            B.poly_act_bwd(fn, dt, xd, dyd, out)
+            want = backward(op, x, dy)
+        assert np.array_equal(from_dev(out), want), (fn, d)
+
+
+def _lut(op):
+    return torch.from_numpy(forward(op, X_ALL).view(np.int16)).to(DEV)
+
+
+def test_hbm_resident_sweep_full_size():
+    """268,435,456 FP16 elements (512 MiB per tensor), 1 % outliers in
+    [-40, 40].  Forward: every element equals the oracle's exhaustive table
+    at its input.  Backward: 2^21 sampled elements plus both ends."""
+    dt = B.POLY_F16
+    x, dy = workloads.isolated_hbm("f16")
+    n = x.size
+    xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+    out = torch.empty_like(xd)
+    idx_x = xd.view(torch.int16).to(torch.int32) & 0xFFFF
+    rng = np.random.default_rng(77)
+    sample = np.unique(np.concatenate([rng.integers(0, n, 1 << 21), np.arange(4096),
+                                       np.arange(n - 4096, n)]))
+    for fn, d in SIX:
+        op = oracle_program(fn, d, dt)
+        if d == B.POLY_FWD:
+            B.poly_act_fwd(fn, dt, xd, out)
+            want = _lut(op)[idx_x.long()]
+            assert torch.equal(out.view(torch.int16), want), fn
+        else:
+            B.poly_act_bwd(fn, dt, xd, dyd, out)
+            got = from_dev(out[torch.from_numpy(sample).to(DEV)])
+            assert np.array_equal(got, backward(op, x[sample], dy[sample])), fn
+    del idx_x
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ SwiGLU
+
+def _swiglu_ops(dt):
+    return (oracle_program(B.POLY_SILU, B.POLY_FWD, dt),
+            oracle_program(B.POLY_SILU, B.POLY_BWD, dt))
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_swiglu_small_every_element(dt):
+    fmt = FMT[dt]
+    s_op, d_op = _swiglu_ops(dt)
+    rng = np.random.default_rng(21)
+    for rows, cols in [(1, 1), (3, 7), (17, 1000), (64, 2048), (5, 8)]:
+        g = _rand_bits(rng, rows * cols, fmt).reshape(rows, cols)
+        u = _rand_bits(rng, rows * cols, fmt).reshape(rows, cols)
+        dy = _rand_bits(rng, rows * cols, fmt).reshape(rows, cols)
+        gd, ud, dyd = to_dev(g, dt), to_dev(u, dt), to_dev(dy, dt)
+        y = torch.empty_like(gd)
+        B.poly_swiglu_fwd(dt, gd, ud, y)
+        assert np.array_equal(from_dev(y).reshape(rows, cols), swiglu_forward(s_op, g, u))
+        dg, du = torch.empty_like(gd), torch.empty_like(gd)
+        B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+        wdg, wdu = swiglu_backward(s_op, d_op, g, u, dy)
+        assert np.array_equal(from_dev(dg).reshape(rows, cols), wdg)
+        assert np.array_equal(from_dev(du).reshape(rows, cols), wdu)
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("cols,pad", [(2048, 8), (1000, 24), (1001, 3)])
+def test_swiglu_strided_every_element(dt, cols, pad):
+    """Gate and up as the two halves of one [rows, 2 cols + pad] buffer (a
+    fused gate/up projection output), outputs with their own pitch."""
+    fmt = FMT[dt]
+    s_op, d_op = _swiglu_ops(dt)
+    rows = 37
+    rng = np.random.default_rng(cols)
+    W = 2 * cols + pad
+    gu = _rand_bits(rng, rows * W, fmt).reshape(rows, W)
+    dy = _rand_bits(rng, rows * cols, fmt).reshape(rows, cols)
+    gud = to_dev(gu, dt)
+    g, u = gud[:, :cols], gud[:, cols:2 * cols]
+    yb = torch.full((rows, cols + pad), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    y = yb[:, :cols]
+    B.poly_swiglu_fwd(dt, g, u, y)
+    gg, uu = gu[:, :cols], gu[:, cols:2 * cols]
+    assert np.array_equal(from_dev(y).reshape(rows, cols), swiglu_forward(s_op, gg, uu))
+    assert bool((yb.view(torch.int16)[:, cols:] == 0x5A5A).all())
+    dgb = torch.full((rows, cols + pad), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    du = torch.empty(rows, cols, dtype=TDT[dt], device=DEV)
+    B.poly_swiglu_bwd(dt, g, u, to_dev(dy, dt), dgb[:, :cols], du)
+    wdg, wdu = swiglu_backward(s_op, d_op, gg, uu, dy)
+    assert np.array_equal(from_dev(dgb[:, :cols]).reshape(rows, cols), wdg)
+    assert np.array_equal(from_dev(du).reshape(rows, cols), wdu)
+    assert bool((dgb.view(torch.int16)[:, cols:] == 0x5A5A).all())
+
+
+def test_dense_swiglu_full_size_sampled():
+    """[8192 x 14336] BF16, gate and up ~ 2 N(0, 1), dy ~ N(0, 1)."""
+    dt = B.POLY_BF16
+    s_op, d_op = _swiglu_ops(dt)
+    g, u, dy = workloads.dense_swiglu("bf16")
+    gd, ud, dyd = to_dev(g, dt), to_dev(u, dt), to_dev(dy, dt)
+    y = torch.empty_like(gd)
+    dg, du = torch.empty_like(gd), torch.empty_like(gd)
+    B.poly_swiglu_fwd(dt, gd, ud, y)
+    B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+    n = g.size
+    rng = np.random.default_rng(31)
+    s = np.unique(np.concatenate([rng.integers(0, n, 1 << 20), np.arange(2048),
+                                  np.arange(n - 2048, n)]))
+    sd = torch.from_numpy(s).to(DEV)
+    gf, uf, dyf = g.reshape(-1), u.reshape(-1), dy.reshape(-1)
+    assert np.array_equal(from_dev(y.view(-1)[sd]), swiglu_forward(s_op, gf[s], uf[s]))
+    wdg, wdu = swiglu_backward(s_op, d_op, gf[s], uf[s], dyf[s])
+    assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
+    assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+
+
+def test_ragged_swiglu_full_size_sampled():
+    """16,384 tokens x top-8 over 64 experts: Zipf(1.1) segments summing to
+    131,072 rows of 2048; the offsets stay on the device.  Rows past the last
+    offset (a larger capacity) must stay untouched."""
+    dt = B.POLY_BF16
+    s_op, d_op = _swiglu_ops(dt)
+    g, u, dy, seg = workloads.ragged_swiglu("bf16")
+    rows, cols = g.shape
+    cap = rows + 3000
+    pad = np.zeros((cap - rows, cols), np.uint16)
+    gd = to_dev(np.concatenate([g, pad]), dt).view(cap, cols)
+    ud = to_dev(np.concatenate([u, pad]), dt).view(cap, cols)
+    dyd = to_dev(np.concatenate([dy, pad]), dt).view(cap, cols)
+    segd = torch.from_numpy(seg).to(DEV)
+    status = torch.full((1,), -7, dtype=torch.int32, device=DEV)
+    fill = lambda: torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    y, dg, du = fill(), fill(), fill()
+    B.poly_swiglu_fwd_ragged(dt, gd, ud, y, segd, status=status)
+    assert int(status.item()) == 0
+    B.poly_swiglu_bwd_ragged(dt, gd, ud, dyd, dg, du, segd, status=status)
+    assert int(status.item()) == 0
+    for t in (y, dg, du):
+        assert bool((t.view(torch.int16)[rows:] == 0x5A5A).all())
+    n = rows * cols
+    rng = np.random.default_rng(41)
+    # every segment boundary row, plus random elements
+    bnd = np.concatenate([np.arange(max(0, b - 1) * cols, min(rows, b + 1) * cols) for b in seg[1:-1]])
+    s = np.unique(np.concatenate([rng.integers(0, n, 1 << 20), bnd, np.arange(n - cols, n)]))
+    sd = torch.from_numpy(s).to(DEV)
+    gf, uf, dyf = g.reshape(-1), u.reshape(-1), dy.reshape(-1)
+    assert np.array_equal(from_dev(y.view(-1)[sd]), swiglu_forward(s_op, gf[s], uf[s]))
+    wdg, wdu = swiglu_backward(s_op, d_op, gf[s], uf[s], dyf[s])
+    assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
+    assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_ragged_small_every_element_and_status(dt):
+    fmt = FMT[dt]
+    s_op, d_op = _swiglu_ops(dt)
+    rng = np.random.default_rng(51)
+    cols, cap = 24, 50
+    seg = np.array([0, 3, 3, 10, 31, 40], dtype=np.int32)
+    g = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
+    u = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
+    gd, ud = to_dev(g, dt), to_dev(u, dt)
+    y = torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.poly_swiglu_fwd_ragged(dt, gd, ud, y, torch.from_numpy(seg).to(DEV), status=status)
+    got = from_dev(y).reshape(cap, cols)
+    assert np.array_equal(got[:40], swiglu_forward(s_op, g[:40], u[:40]))
+    assert np.all(got[40:] == 0x5A5A) and int(status.item()) == 0
+    # non-monotone offsets (still inside the capacity): status 1
+    bad = torch.from_numpy(np.array([0, 5, 2, 10, 31, 40], dtype=np.int32)).to(DEV)
+    B.poly_swiglu_fwd_ragged(dt, gd, ud, y, bad, status=status)
+    assert int(status.item()) == 1
+    # last offset beyond the capacity: clamped to it, status 1
+    over = torch.from_numpy(np.array([0, 3, 3, 10, 31, 60], dtype=np.int32)).to(DEV)
+    y2 = torch.empty_like(y)
+    B.poly_swiglu_fwd_ragged(dt, gd, ud, y2, over, status=status)
+    assert int(status.item()) == 1
+    assert np.array_equal(from_dev(y2).reshape(cap, cols), swiglu_forward(s_op, g, u))
+
+
+# ---------------------------------------------------------------- controls
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("fn,d", PROGRAMS)
+def test_mufu_controls_accuracy(fn, d, dt):
+    """The special-function-unit controls approximate the true function to
+    within two target-format ulps (plus the FP32 approximation error)."""
+    fmt = FMT[dt]
+    x = _rand_bits(np.random.default_rng(2), 1 << 16, fmt)
+    x = x[tf.finite_mask(x, fmt)]
+    x = x[np.abs(tf.decode(x, fmt)) < 60]
+    xd = to_dev(x, dt)
+    out = torch.empty_like(xd)
+    f = ref.function(fn, d)(tf.decode(x, fmt))
+    if d == B.POLY_FWD:
+        B.poly_ctrl_act_fwd(fn, dt, xd, out)
+    else:
+        ones = to_dev(tf.from_f64(np.ones(x.size), fmt), dt)
+        B.poly_ctrl_act_bwd(fn, dt, xd, ones, out)
+    y = tf.decode(from_dev(out), fmt)
+    ulp = np.spacing(np.abs(f).astype(np.float16 if fmt == "f16" else np.float32))
+    ulp = ulp.astype(np.float64) * (1 if fmt == "f16" else 2.0 ** 16)
+    tol = 2 * ulp + 1e-3 * (1.0 + np.abs(f))
+    assert np.all(np.abs(y - f) <= tol), (fn, d, np.max(np.abs(y - f)))
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_mufu_swiglu_controls(dt):
+    fmt = FMT[dt]
+    rng = np.random.default_rng(8)
+    g = _rand_bits(rng, 64 * 256, fmt)
+    g = np.where(tf.finite_mask(g, fmt) & (np.abs(tf.decode(g, fmt)) < 30), g, np.uint16(0)).reshape(64, 256)
+    u = tf.from_f64(rng.normal(0, 1, g.size), fmt).reshape(64, 256)
+    gd, ud = to_dev(g, dt), to_dev(u, dt)
+    y = torch.empty_like(gd)
+    B.poly_ctrl_swiglu_fwd(dt, gd, ud, y)
+    gv, uv = tf.decode(g, fmt), tf.decode(u, fmt)
+    want = ref.silu(gv) * uv
+    got = tf.decode(from_dev(y).reshape(64, 256), fmt)
+    assert np.max(np.abs(got - want) / np.maximum(np.abs(want), 1)) < 2e-2
+    dg, du = torch.empty_like(gd), torch.empty_like(gd)
+    B.poly_ctrl_swiglu_bwd(dt, gd, ud, ud, dg, du)
+    wdg = uv * uv * ref.dsilu(gv)
+    wdu = uv * ref.silu(gv)
+    assert np.max(np.abs(tf.decode(from_dev(dg).reshape(64, 256), fmt) - wdg) / np.maximum(np.abs(wdg), 1)) < 2e-2
+    assert np.max(np.abs(tf.decode(from_dev(du).reshape(64, 256), fmt) - wdu) / np.maximum(np.abs(wdu), 1)) < 2e-2
