@@ -153,13 +153,26 @@ def max_over_ranks(x, world, device):
 
 # --------------------------------------------------------------- CPU oracle
 
+def oracle_programs():
+    """The oracle fitter's programs for the six (written to
+    tests/golden/programs.json by a script that calls only the oracle)."""
+    from oracle.replay import Program
+    with open(os.path.join(ROOT, "tests", "golden", "programs.json")) as f:
+        g = json.load(f)
+    out = []
+    for name, d, D in SIX:
+        v = g[f"{name}.{'bwd' if d else 'fwd'}.f16.D{D}"]
+        out.append(Program(fn=v["fn"], direction=v["direction"], fmt="f16", degree=D,
+                           li=v["li"], lc=v["lc"], coef=tuple(v["coef"]), lc_bits=v["lc_bits"]))
+    return out
+
+
 def oracle_sample_time(n_sample):
     """Time the CPU replay oracle on the first n_sample elements of the
     workload for each of the six programs; returns (seconds, elements)."""
-    from oracle import fit
     from oracle.replay import backward, forward
     x, dy = workloads.isolated_hbm("f16", n=n_sample)
-    progs = [fit.search(FN[name], d, "f16", D) for name, d, D in SIX]
+    progs = oracle_programs()
     t0 = time.perf_counter()
     for p, (name, d, D) in zip(progs, SIX):
         if d == 0:
@@ -174,10 +187,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     per_step = int(np.clip(2 ** 23 // max(1, args.steps + args.warmup), 2 ** 12, 2 ** 20))
-    from oracle import fit
     from oracle.replay import backward, forward
     x, dy = workloads.isolated_hbm("f16", n=per_step)
-    progs = [fit.search(FN[name], d, "f16", D) for name, d, D in SIX]
+    progs = oracle_programs()
 
     def step():
         for p, (name, d, D) in zip(progs, SIX):
@@ -215,7 +227,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="only the timed step")
-    ap.add_argument("--cpu-sample", type=int, default=1 << 20)
+    ap.add_argument("--cpu-sample", type=int, default=1 << 20,
+                    help="elements per program for the CPU oracle baseline (0 = skip)")
+    ap.add_argument("--elements", type=int, default=workloads.N_HBM,
+                    help="tensor size (a smaller case for profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -232,7 +248,7 @@ def main():
     peak, peak_kind = peaks()
 
     # ---- inputs (host generation once, then resident in HBM)
-    xh, dyh = workloads.isolated_hbm("f16")
+    xh, dyh = workloads.isolated_hbm("f16", n=args.elements)
     n = xh.size
     x = torch.from_numpy(xh.view(np.int16)).to(dev).view(torch.float16)
     dy = torch.from_numpy(dyh.view(np.int16)).to(dev).view(torch.float16)
@@ -350,16 +366,20 @@ def main():
         result["l2_resident"] = l2_extras(dev, stream)
 
     # ---- end to end through the public API with host buffers
-    result["e2e"] = e2e(args, dev, stream, xh, dyh)
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, dev, stream, xh, dyh)
 
     # ---- CPU oracle on a bounded sample
-    if rank == 0:
+    if rank == 0 and args.cpu_sample > 0:
         secs, elems = oracle_sample_time(args.cpu_sample)
         result["cpu_baseline"] = {"value": elems / secs / 1e9, "unit": UNIT, "cores": 1,
                                   "kind": "oracle",
                                   "sample": f"first {args.cpu_sample} elements of the workload "
                                             f"through each of the six programs (numpy replay, "
                                             f"{secs:.1f} s)"}
+    if rank == 0:
+        if args.elements != workloads.N_HBM:
+            result["config"]["workload"] = f"profiling case: {args.elements} elements"
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
