@@ -16,9 +16,12 @@
  *   throws, aborts or prints.
  * - Ownership: the caller owns every buffer.  The library never allocates,
  *   frees or synchronises device memory.
- * - Device calls (poly_act_*, poly_swiglu_*, poly_ctrl_*) take device
- *   pointers and a CUDA stream (poly_stream_t is layout-compatible with
- *   cudaStream_t; NULL = the legacy default stream).  They validate the
+ * - Device calls (poly_act_*, poly_swiglu_*, poly_ctrl_*) take addresses
+ *   the GPU can reach -- device memory, or, on systems with coherent host
+ *   access such as GB300's NVLink-C2C, pinned host memory (the kernels then
+ *   stream it over the link with no staging copy) -- and a CUDA stream
+ *   (poly_stream_t is layout-compatible with cudaStream_t; NULL = the legacy
+ *   default stream).  Kernels run on the calling thread's current device.  They validate the
  *   arguments on the host, enqueue one kernel and return without waiting.
  *   A launch failure is reported as POLY_ECUDA (the CUDA error is consumed
  *   and available through poly_last_cuda_error).

@@ -83,7 +83,8 @@ bool aliasing_ok(const Span *in, int nin, const Span *out, int nout) {
 
 bool even_address(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 
-// Flat layout: the vector path needs every stream at the same offset mod 16.
+// Flat layout of n contiguous elements: the 16-byte path needs every stream
+// at the same address modulo 16 (the kernel derives the scalar head).
 Layout flat_layout(const void *const *ptrs, int np, int64_t n) {
   Layout l;
   std::memset(&l, 0, sizeof(l));
@@ -93,12 +94,6 @@ Layout flat_layout(const void *const *ptrs, int np, int64_t n) {
   l.vec = 1;
   for (int i = 1; i < np; ++i)
     if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != m) l.vec = 0;
-  if (l.vec) {
-    int64_t head = (int64_t)(((16u - m) & 15u) >> 1);
-    l.head = head < n ? head : n;
-  } else {
-    l.head = n;
-  }
   return l;
 }
 

@@ -9,10 +9,18 @@ namespace dev {
 template <int DT, int FORM>
 static cudaError_t act_deg(int kind, int deg, const Streams &s, const Layout &l,
                            const ProgPair &p, cudaStream_t st) {
-#define POLYACT_CASE(D)                                                  \
-  case D:                                                                \
-    return kind == kActFwd ? launch_op<OpFwd<DT, FORM, D>>(s, l, p, st)  \
-                           : launch_op<OpBwd<DT, FORM, D>>(s, l, p, st);
+  // forward forms: CO, O, HX; backward forms: E, CO
+  constexpr bool fwd_ok = FORM != POLY_FORM_E;
+  constexpr bool bwd_ok = FORM == POLY_FORM_E || FORM == POLY_FORM_CO;
+#define POLYACT_CASE(D)                                                          \
+  case D:                                                                        \
+    if constexpr (fwd_ok) {                                                      \
+      if (kind == kActFwd) return launch_op<OpFwd<DT, FORM, D>>(s, l, p, st);    \
+    }                                                                            \
+    if constexpr (bwd_ok) {                                                      \
+      if (kind == kActBwd) return launch_op<OpBwd<DT, FORM, D>>(s, l, p, st);    \
+    }                                                                            \
+    return cudaErrorInvalidValue;
   switch (deg) {
     POLYACT_CASE(3)
     POLYACT_CASE(4)

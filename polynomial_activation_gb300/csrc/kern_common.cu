@@ -1,8 +1,5 @@
 // kern_common.cu -- launch sizing and the dispatch from the C ABI layer to
 // the per-family translation units.
-#include <mutex>
-#include <unordered_map>
-
 #include "poly_ops.cuh"
 
 namespace polyact {
@@ -13,47 +10,18 @@ cudaError_t launch_act(int kind, int dtype, int form, int deg, const Streams &s,
 cudaError_t launch_swiglu(int kind, int dtype, int ds, int dd, const Streams &s,
                           const Layout &l, const ProgPair &p, cudaStream_t st);
 
-namespace {
-std::mutex g_mu;
-std::unordered_map<int, int> g_sms;                       // device -> SM count
-std::unordered_map<const void *, int> g_occ;              // kernel -> resident blocks / SM
-}  // namespace
-
-int64_t grid_for(const void *kernel, const Layout &l) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int sms = 0, occ = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_sms.find(dev);
-    if (it == g_sms.end()) {
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      g_sms[dev] = sms;
-    } else {
-      sms = it->second;
-    }
-    auto jt = g_occ.find(kernel);
-    if (jt == g_occ.end()) {
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
-      g_occ[kernel] = occ;
-    } else {
-      occ = jt->second;
-    }
-  }
-  if (sms <= 0) sms = 1;
-  if (occ <= 0) occ = 1;
-  // elements of work per block in one pass
+int64_t grid_for(const Layout &l, int per_thread) {
   int64_t work;
   if (l.mode == kStrided)
-    work = l.vec ? l.rows * (l.cols / 8) * 8 : l.rows * l.cols;
+    work = l.rows * l.cols;
   else if (l.mode == kRagged)
-    work = l.cap_rows * l.cols;
+    work = l.cap_rows * l.cols;   // an upper bound: the row range is on the device
   else
     work = l.n;
-  const int64_t per_block = (int64_t)kThreads * kUnroll * 8;
+  const int64_t per_block = (int64_t)kThreads * per_thread;
   int64_t blocks = (work + per_block - 1) / per_block;
-  const int64_t cap = (int64_t)sms * occ;
-  if (blocks > cap) blocks = cap;
+  const int64_t max_blocks = 0x7FFFFFFF;
+  if (blocks > max_blocks) blocks = max_blocks;   // the kernels stride past this
   if (blocks < 1) blocks = 1;
   return blocks;
 }
@@ -61,6 +29,7 @@ int64_t grid_for(const void *kernel, const Layout &l) {
 template <int DT, int OP>
 struct OpDiag {
   static constexpr int NIN = 3, NOUT = 1;
+  static constexpr bool TWO_D = false;
   struct Params {};
   __device__ __forceinline__ static void pair(const uint32_t (&a)[3], uint32_t (&b)[1],
                                               const Params &) {

@@ -98,6 +98,7 @@ struct NoParams {};
 template <int DT, int FN>
 struct CtrlFwd {
   static constexpr int NIN = 1, NOUT = 1;
+  static constexpr bool TWO_D = false;
   using Params = NoParams;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[1], uint32_t (&b)[1],
                                               const Params &) {
@@ -109,6 +110,7 @@ struct CtrlFwd {
 template <int DT, int FN>
 struct CtrlBwd {
   static constexpr int NIN = 2, NOUT = 1;
+  static constexpr bool TWO_D = false;
   using Params = NoParams;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[2], uint32_t (&b)[1],
                                               const Params &) {
@@ -120,6 +122,7 @@ struct CtrlBwd {
 template <int DT>
 struct CtrlSwigluFwd {
   static constexpr int NIN = 2, NOUT = 1;
+  static constexpr bool TWO_D = true;
   using Params = NoParams;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[2], uint32_t (&b)[1],
                                               const Params &) {
@@ -131,6 +134,7 @@ struct CtrlSwigluFwd {
 template <int DT>
 struct CtrlSwigluBwd {
   static constexpr int NIN = 3, NOUT = 2;
+  static constexpr bool TWO_D = true;
   using Params = NoParams;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[3], uint32_t (&b)[2],
                                               const Params &) {

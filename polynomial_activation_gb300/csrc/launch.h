@@ -26,16 +26,16 @@ struct Streams {
 enum LayoutMode { kFlat = 0, kRagged = 1, kStrided = 2 };
 
 // Where the elements are.
-//  kFlat:    n contiguous elements; `head` leading elements run scalar and the
-//            rest, if `vec`, as 16-byte chunks (all streams share alignment).
+//  kFlat:    n contiguous elements; `vec` when every stream sits at the same
+//            address modulo 16 (16-byte body, scalar head and tail).
 //  kRagged:  rows [seg[0], seg[nseg]) of a [cap_rows, cols] matrix, bounds
-//            read on the device; `vec` as above for the whole allocation.
+//            read on the device; `vec` as for kFlat on the base addresses.
 //  kStrided: rows x cols with per-stream leading dimensions; `vec` when every
 //            row start is 16-byte aligned and cols % 8 == 0.
 struct Layout {
   int mode;
   int vec;
-  int64_t n, head;
+  int64_t n;
   const int32_t *seg;
   int32_t nseg;
   int64_t cap_rows, cols, rows;

@@ -50,6 +50,7 @@ struct ProgPair {
 template <int DT, int FORM, int D>
 struct OpFwd {
   static constexpr int NIN = 1, NOUT = 1;
+  static constexpr bool TWO_D = false;
   using Params = ProgPair;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[1], uint32_t (&b)[1],
                                               const Params &p) {
@@ -61,6 +62,7 @@ struct OpFwd {
 template <int DT, int FORM, int D>
 struct OpBwd {
   static constexpr int NIN = 2, NOUT = 1;
+  static constexpr bool TWO_D = false;
   using Params = ProgPair;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[2], uint32_t (&b)[1],
                                               const Params &p) {
@@ -72,6 +74,7 @@ struct OpBwd {
 template <int DT, int DS>
 struct OpSwigluFwd {
   static constexpr int NIN = 2, NOUT = 1;
+  static constexpr bool TWO_D = true;
   using Params = ProgPair;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[2], uint32_t (&b)[1],
                                               const Params &p) {
@@ -83,6 +86,7 @@ struct OpSwigluFwd {
 template <int DT, int DS, int DD>
 struct OpSwigluBwd {
   static constexpr int NIN = 3, NOUT = 2;
+  static constexpr bool TWO_D = true;
   using Params = ProgPair;
   __device__ __forceinline__ static void pair(const uint32_t (&a)[3], uint32_t (&b)[2],
                                               const Params &p) {

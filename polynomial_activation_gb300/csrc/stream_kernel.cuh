@@ -4,14 +4,15 @@
 // Each element is independent, so the work is a pure memory stream: HBM (or
 // L2) bandwidth bounds it, not arithmetic.  The kernel therefore does
 //  * 16-byte loads and stores (8 FP16/BF16 elements = 4 packed pairs per
-//    access, "Fast Polynomial Transcendentals for LLMs" §3.4: "one thread
-//    loads a 16-byte int4 chunk, reinterprets it as four pairs"), with
-//    kUnroll independent chunks per stream in flight per thread;
-//  * a grid sized to the resident capacity of the GPU (a multiple of the SM
-//    count), striding over the tensor;
-//  * a scalar head (up to 7 elements, when the tensors are not 16-byte
-//    aligned) and tail (n % 8), evaluated with the same packed instructions
-//    on one lane so that every element gets bit-identical arithmetic.
+//    access, as the paper, "Fast Polynomial Transcendentals for LLMs" §3.4,
+//    loads int4 chunks and reinterprets them as four pairs), one or two
+//    chunks per stream per thread;
+//  * a one-pass grid: every thread owns its chunks, blocks retire and are
+//    replaced as fast as the memory system drains them;
+//  * a scalar head (up to the first 16-byte boundary) and tail, evaluated
+//    with the same packed instructions on one lane so that every element
+//    gets bit-identical arithmetic; streams whose addresses disagree modulo
+//    16 bytes take the scalar path throughout.
 // An operation ("Op") supplies NIN input streams, NOUT output streams and a
 // function from NIN packed pairs to NOUT packed pairs.
 #pragma once
@@ -24,9 +25,8 @@ namespace polyact {
 namespace dev {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
 
-// Streaming loads: the data is touched once, keep it out of L1.
+// Streaming loads / stores: the data is touched once, keep it out of L1.
 __device__ __forceinline__ uint4 ld_stream(const uint16_t *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -48,23 +48,25 @@ __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
   return v;
 }
 
+// Chunks of 8 elements per stream per thread: two for single-input
+// operations, one for multi-input ones (measured on GB300 with a one-pass
+// grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes).
+template <class Op>
+__host__ __device__ constexpr int chunks_per_thread() {
+  return Op::NIN == 1 ? 2 : 1;
+}
+
 template <class Op>
 __device__ __forceinline__ void apply_chunk(const uint4 (&in)[Op::NIN], uint4 (&out)[Op::NOUT],
                                             const typename Op::Params &p) {
-  const uint32_t *iw[Op::NIN];
-#pragma unroll
-  for (int k = 0; k < Op::NIN; ++k) iw[k] = reinterpret_cast<const uint32_t *>(&in[k]);
-  uint32_t *ow[Op::NOUT];
-#pragma unroll
-  for (int k = 0; k < Op::NOUT; ++k) ow[k] = reinterpret_cast<uint32_t *>(&out[k]);
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t a[Op::NIN], b[Op::NOUT];
 #pragma unroll
-    for (int k = 0; k < Op::NIN; ++k) a[k] = iw[k][w];
+    for (int k = 0; k < Op::NIN; ++k) a[k] = reinterpret_cast<const uint32_t *>(&in[k])[w];
     Op::pair(a, b, p);
 #pragma unroll
-    for (int k = 0; k < Op::NOUT; ++k) ow[k][w] = b[k];
+    for (int k = 0; k < Op::NOUT; ++k) reinterpret_cast<uint32_t *>(&out[k])[w] = b[k];
   }
 }
 
@@ -82,11 +84,15 @@ __device__ __forceinline__ void apply_one(const uint16_t *const *in, uint16_t *c
   for (int k = 0; k < Op::NOUT; ++k) out[k][e] = (uint16_t)(b[k] & 0xFFFFu);
 }
 
-// Flat / ragged: one contiguous range of elements.
+// Flat / ragged: one contiguous range of elements.  When every stream sits at
+// the same address modulo 16 (l.vec), the scalar head runs up to the first
+// 16-byte boundary and the body moves 16-byte chunks; otherwise every
+// element takes the scalar path.
 template <class Op>
-__device__ __forceinline__ void flat_body(const Streams &s, const Layout &l,
-                                          const typename Op::Params &p) {
-  int64_t n = l.n, head = l.head, off = 0;
+__global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
+                                                          typename Op::Params p) {
+  constexpr int U = chunks_per_thread<Op>();
+  int64_t n = l.n, off = 0;
   if (l.mode == kRagged) {
     int64_t lo = l.seg[0], hi = l.seg[l.nseg];
     if (lo < 0) lo = 0;
@@ -94,13 +100,6 @@ __device__ __forceinline__ void flat_body(const Streams &s, const Layout &l,
     if (hi < lo) hi = lo;
     off = lo * l.cols;
     n = (hi - lo) * l.cols;
-    if (l.vec) {
-      const uintptr_t a = reinterpret_cast<uintptr_t>(s.in0 + off);
-      head = (int64_t)(((16u - (a & 15u)) & 15u) >> 1);
-      if (head > n) head = n;
-    } else {
-      head = n;
-    }
     if (l.status != nullptr && blockIdx.x == 0) {
       int bad = 0;
       for (int e = threadIdx.x; e < l.nseg; e += blockDim.x) bad |= l.seg[e] > l.seg[e + 1];
@@ -118,32 +117,39 @@ __device__ __forceinline__ void flat_body(const Streams &s, const Layout &l,
 #pragma unroll
   for (int k = 0; k < Op::NOUT; ++k) out[k] = dst[k] + off;
 
-  const int64_t nvec = l.vec ? (n - head) / 8 : 0;
-  const int64_t body_end = head + nvec * 8;
-  const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
-  for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nvec;
-       base += step) {
-    uint4 r[kUnroll][Op::NIN];
+  int64_t head = n;
+  if (l.vec) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in[0]);
+    head = (int64_t)(((16u - (a & 15u)) & 15u) >> 1);
+    if (head > n) head = n;
+  }
+  const int64_t nvec = (n - head) >> 3;
+  const int64_t body_end = head + (nvec << 3);
+#pragma unroll 1
+  for (int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x; base < nvec;
+       base += (int64_t)gridDim.x * (kThreads * U)) {
+    uint4 r[U][Op::NIN];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t i = base + u * kThreads;
       if (i < nvec) {
 #pragma unroll
-        for (int k = 0; k < Op::NIN; ++k) r[u][k] = ld_stream(in[k] + head + i * 8);
+        for (int k = 0; k < Op::NIN; ++k) r[u][k] = ld_stream(in[k] + head + (i << 3));
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t i = base + u * kThreads;
       if (i < nvec) {
         uint4 o[Op::NOUT];
         apply_chunk<Op>(r[u], o, p);
 #pragma unroll
-        for (int k = 0; k < Op::NOUT; ++k) st_stream(out[k] + head + i * 8, o[k]);
+        for (int k = 0; k < Op::NOUT; ++k) st_stream(out[k] + head + (i << 3), o[k]);
       }
     }
   }
   const int64_t ntail = n - body_end;
+#pragma unroll 1
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < head + ntail;
        i += (int64_t)gridDim.x * kThreads) {
     const int64_t e = i < head ? i : body_end + (i - head);
@@ -151,20 +157,22 @@ __device__ __forceinline__ void flat_body(const Streams &s, const Layout &l,
   }
 }
 
-// Strided: rows x cols with a leading dimension per stream.
+// Strided: rows x cols with a leading dimension per stream (a separate
+// kernel so that its index arithmetic does not weigh on the flat path).
 template <class Op>
-__device__ __forceinline__ void strided_body(const Streams &s, const Layout &l,
-                                             const typename Op::Params &p) {
+__global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
+                                                           typename Op::Params p) {
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
   const int64_t gid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   if (l.vec) {
-    const int64_t cpr = l.cols / 8;
+    const int64_t cpr = l.cols >> 3;
     const int64_t total = l.rows * cpr;
+#pragma unroll 1
     for (int64_t c = gid; c < total; c += stride) {
       const int64_t row = c / cpr;
-      const int64_t col = (c - row * cpr) * 8;
+      const int64_t col = (c - row * cpr) << 3;
       uint4 r[Op::NIN], o[Op::NOUT];
 #pragma unroll
       for (int k = 0; k < Op::NIN; ++k) r[k] = ld_stream(src[k] + row * l.ld_in[k] + col);
@@ -174,6 +182,7 @@ __device__ __forceinline__ void strided_body(const Streams &s, const Layout &l,
     }
   } else {
     const int64_t total = l.rows * l.cols;
+#pragma unroll 1
     for (int64_t e = gid; e < total; e += stride) {
       const int64_t row = e / l.cols;
       const int64_t col = e - row * l.cols;
@@ -188,24 +197,25 @@ __device__ __forceinline__ void strided_body(const Streams &s, const Layout &l,
   }
 }
 
-template <class Op>
-__global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
-                                                          typename Op::Params p) {
-  if (l.mode == kStrided)
-    strided_body<Op>(s, l, p);
-  else
-    flat_body<Op>(s, l, p);
-}
+// Blocks for a launch: `per_thread` elements per thread, covering the work
+// in one pass (measured on GB300: a one-pass grid streams 8-10 % faster than
+// a persistent grid striding over the tensor).
+int64_t grid_for(const Layout &l, int per_thread);
 
-// Blocks for a launch: enough to cover the work once, capped at what the
-// GPU holds resident (SM count x resident blocks per SM).
-int64_t grid_for(const void *kernel, const Layout &l);
-
+// Launch an op on a flat / ragged layout (every op) or, when the op allows
+// it (TWO_D), on a strided one.
 template <class Op>
 cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Params &p,
                       cudaStream_t stream) {
-  const void *k = reinterpret_cast<const void *>(&stream_kernel<Op>);
-  const int64_t blocks = grid_for(k, l);
+  if constexpr (Op::TWO_D) {
+    if (l.mode == kStrided) {
+      const int64_t blocks = grid_for(l, l.vec ? 8 : 1);
+      strided_kernel<Op><<<(unsigned)blocks, kThreads, 0, stream>>>(s, l, p);
+      return cudaGetLastError();
+    }
+  }
+  if (l.mode == kStrided) return cudaErrorInvalidValue;
+  const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   stream_kernel<Op><<<(unsigned)blocks, kThreads, 0, stream>>>(s, l, p);
   return cudaGetLastError();
 }

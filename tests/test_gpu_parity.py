@@ -397,3 +397,22 @@ def test_mufu_swiglu_controls(dt):
     wdu = uv * ref.silu(gv)
     assert np.max(np.abs(tf.decode(from_dev(dg).reshape(64, 256), fmt) - wdg) / np.maximum(np.abs(wdg), 1)) < 2e-2
     assert np.max(np.abs(tf.decode(from_dev(du).reshape(64, 256), fmt) - wdu) / np.maximum(np.abs(wdu), 1)) < 2e-2
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_host_memory_operands(dt):
+    """On GB300 the GPU reaches pinned host memory over NVLink-C2C: inputs
+    and outputs may live there, with bit-identical results."""
+    fmt = FMT[dt]
+    x = _rand_bits(np.random.default_rng(13), 300_001, fmt)
+    op = oracle_program(B.POLY_SILU, B.POLY_FWD, dt)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory().view(TDT[dt])
+    yh = torch.full((x.size,), 0x5A5A, dtype=torch.int16).pin_memory().view(TDT[dt])
+    B.poly_act_fwd(B.POLY_SILU, dt, xh, yh, x.size)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh.view(torch.int16).numpy().view(np.uint16), forward(op, x))
+    xd = to_dev(x, dt)
+    yh2 = torch.empty(x.size, dtype=torch.int16).pin_memory().view(TDT[dt])
+    B.poly_act_fwd(B.POLY_SILU, dt, xd, yh2, x.size)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh2.view(torch.int16).numpy().view(np.uint16), forward(op, x))
