@@ -426,6 +426,18 @@ def swiglu_extras(args, dev, stream, peak):
         ms = _time(fn, stream, reps)
         out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
                       "frac": nbytes * n / ms / 1e6 / peak}
+    # the paper's deployed B1/B4 rule: sigmoid program recomputed
+    B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
+    try:
+        for label, fn, nbytes in [
+            ("dense_fwd_sigmoid_rule", lambda: B.poly_swiglu_fwd(bf, gd, ud, y), 6),
+            ("dense_bwd_sigmoid_rule", lambda: B.poly_swiglu_bwd(bf, gd, ud, dyd, dg, du), 10),
+        ]:
+            ms = _time(fn, stream, reps)
+            out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
+                          "frac": nbytes * n / ms / 1e6 / peak}
+    finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
     del gd, ud, dyd, y, dg, du
     g, u, dy, seg = workloads.ragged_swiglu("bf16")
     gd, ud, dyd = t(g), t(u), t(dy)

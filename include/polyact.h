@@ -170,12 +170,27 @@ int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx,
                  int64_t n, poly_stream_t stream);
 
 /* ---- SwiGLU gate (§3.4, §5.2.4 eq. 15) ------------------------------------
- * s = installed SiLU forward program (HX form), s' = installed SiLU backward
- * program (CO form, the centred SiLU derivative of eq. 9).
- * Forward:   y  = s(g) * u
- * Backward:  dg = (dy * u) * s'(g),   du = dy * s(g)      (each product rounded once)
+ * Two rules, chosen process-wide by poly_set_swiglu_variant:
+ * POLY_SWIGLU_DIRECT (default): s = installed SiLU forward program (HX form),
+ *   s' = installed SiLU backward program (CO form, the centred SiLU
+ *   derivative of eq. 9).
+ *   Forward:   y  = s(g) * u
+ *   Backward:  dg = (dy * u) * s'(g),   du = dy * s(g)
+ * POLY_SWIGLU_SIGMOID: the rule the paper deploys in B1/B4 (§3.3, §5.2.4):
+ *   p = installed sigmoid forward program, s = g * p,
+ *   s' = p + g p (1 - p) evaluated as q = fma(-p, p, p), s' = fma(g, q, p).
+ *   Forward:   y  = (g * p) * u
+ *   Backward:  dg = (dy * u) * s',      du = dy * (g * p)
+ * Every product and fma rounds once.
  * Dense: row-major [rows, cols] with leading dimensions (elements, >= cols).
  */
+enum { POLY_SWIGLU_DIRECT = 0, POLY_SWIGLU_SIGMOID = 1 };
+/* Select the SwiGLU rule for later calls (thread-safe, process-wide).
+ * POLY_EINVAL for an unknown variant. */
+int poly_set_swiglu_variant(int variant);
+/* The current SwiGLU rule. */
+int poly_get_swiglu_variant(void);
+
 int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y,
                     int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
                     int64_t ldy, poly_stream_t stream);

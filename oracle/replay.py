@@ -23,7 +23,9 @@ rounded coefficients without any intermediate rounding (§4.1).
 
 The backward product of a derivative program is dx = dy * y rounded once; the
 SwiGLU gate (eq. 15) is y = s(g) * u and its backward dg = (dy * u) * s'(g),
-du = dy * s(g), each product rounded once.
+du = dy * s(g), each product rounded once.  The paper's deployed B1/B4 rule
+instead recomputes the sigmoid program p and forms s = g p and
+s' = p + g p (1 - p) (§3.3 "Forward and backward programs", §5.2.4).
 """
 from __future__ import annotations
 
@@ -119,6 +121,29 @@ def swiglu_backward(silu_prog: Program, dsilu_prog: Program, g, u, dy):
     fmt = silu_prog.fmt
     dg = tf.mul(tf.mul(dy, u, fmt), forward(dsilu_prog, g), fmt)
     du = tf.mul(dy, forward(silu_prog, g), fmt)
+    return dg, du
+
+
+def swiglu_sigmoid_forward(sig_prog: Program, g, u):
+    """The deployed B1/B4 SwiGLU of §3.3 / §5.2.4: recompute the sigmoid
+    program p(g), form SiLU as s = g * p, then y = s * u (each product
+    rounded once)."""
+    fmt = sig_prog.fmt
+    p = forward(sig_prog, g)
+    return tf.mul(tf.mul(g, p, fmt), u, fmt)
+
+
+def swiglu_sigmoid_backward(sig_prog: Program, g, u, dy):
+    """Backward of the deployed B1/B4 SwiGLU: s' = p + g p (1 - p) (§3.3),
+    evaluated as q = fma(-p, p, p) = p - p^2 and s' = fma(g, q, p), each
+    rounding once; dg = (dy * u) * s', du = dy * (g * p)."""
+    fmt = sig_prog.fmt
+    p = forward(sig_prog, g)
+    q = tf.fma(tf.xorsign(p, np.uint16(0x8000)), p, p, fmt)
+    sd = tf.fma(g, q, p, fmt)
+    s = tf.mul(g, p, fmt)
+    dg = tf.mul(tf.mul(dy, u, fmt), sd, fmt)
+    du = tf.mul(dy, s, fmt)
     return dg, du
 
 

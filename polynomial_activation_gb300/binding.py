@@ -29,8 +29,9 @@ EXPORTS = [
     "poly_get_program", "poly_reset_programs", "poly_act_fwd", "poly_act_bwd",
     "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
-    "poly_diag_packed",
+    "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
 ]
+POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID = 0, 1
 POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
 
 
@@ -83,7 +84,9 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     L.poly_status_str.restype = ctypes.c_char_p
     L.poly_status_str.argtypes = [_i]
-    for name in ("poly_last_cuda_error", "poly_abi_version", "poly_reset_programs"):
+    L.poly_set_swiglu_variant.argtypes = [_i]
+    for name in ("poly_last_cuda_error", "poly_abi_version", "poly_reset_programs",
+                 "poly_get_swiglu_variant"):
         getattr(L, name).restype = _i
         getattr(L, name).argtypes = []
     L.poly_form_of.argtypes = [_i, _i]
@@ -180,6 +183,14 @@ def poly_get_program(fn, direction, dtype):
 
 def poly_reset_programs():
     _check(lib().poly_reset_programs(), "poly_reset_programs")
+
+
+def poly_set_swiglu_variant(variant):
+    _check(lib().poly_set_swiglu_variant(variant), "poly_set_swiglu_variant")
+
+
+def poly_get_swiglu_variant():
+    return lib().poly_get_swiglu_variant()
 
 
 def poly_act_fwd(fn, dtype, x, y, n=None, stream=None):

@@ -4,6 +4,7 @@
 // CUDA call, so invalid arguments never reach the GPU.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -20,6 +21,7 @@ thread_local int t_last_cuda_error = 0;
 std::mutex g_reg_mu;
 bool g_have[4][2][2];
 poly_program g_prog[4][2][2];
+std::atomic<int> g_swiglu_variant{POLY_SWIGLU_DIRECT};
 
 bool valid_fn(int fn) { return fn >= POLY_SIGMOID && fn <= POLY_GELU; }
 bool valid_dir(int d) { return d == POLY_FWD || d == POLY_BWD; }
@@ -192,7 +194,14 @@ int ragged_layout(const void *const *in, int nin, void *const *out, int nout,
   return POLY_OK;
 }
 
-int swiglu_programs(int dtype, bool need_bwd, poly_program *s, poly_program *sd) {
+// Programs of the current SwiGLU variant: the SiLU program (and, for the
+// direct backward, the centred SiLU derivative), or the sigmoid program.
+int swiglu_programs(int variant, int dtype, bool need_bwd, poly_program *s, poly_program *sd) {
+  if (variant == POLY_SWIGLU_SIGMOID) {
+    int st = registry_get(POLY_SIGMOID, POLY_FWD, dtype, s);
+    *sd = *s;
+    return st;
+  }
   int st = registry_get(POLY_SILU, POLY_FWD, dtype, s);
   if (st != POLY_OK) return st;
   if (need_bwd) return registry_get(POLY_SILU, POLY_BWD, dtype, sd);
@@ -278,6 +287,14 @@ int poly_get_program(int fn, int dir, int dtype, poly_program *out) {
   return registry_get(fn, dir, dtype, out);
 }
 
+int poly_set_swiglu_variant(int variant) {
+  if (variant != POLY_SWIGLU_DIRECT && variant != POLY_SWIGLU_SIGMOID) return POLY_EINVAL;
+  g_swiglu_variant.store(variant);
+  return POLY_OK;
+}
+
+int poly_get_swiglu_variant(void) { return g_swiglu_variant.load(); }
+
 int poly_reset_programs(void) {
   std::lock_guard<std::mutex> lk(g_reg_mu);
   std::memset(g_have, 0, sizeof(g_have));
@@ -342,11 +359,12 @@ static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int kind = bwd ? kSwigluBwd : kSwigluFwd;
   if (ctrl) return cuda_status(launch_ctrl(kind, dtype, POLY_SILU, s, l, cs));
+  const int variant = g_swiglu_variant.load();
   poly_program ps, pd;
-  st = swiglu_programs(dtype, bwd, &ps, &pd);
+  st = swiglu_programs(variant, dtype, bwd, &ps, &pd);
   if (st != POLY_OK) return st;
   return cuda_status(launch_poly(kind, dtype, ps.form, ps.degree, pd.degree, s, l,
-                                 dev_prog(ps), dev_prog(pd), cs));
+                                 dev_prog(ps), dev_prog(pd), cs, variant));
 }
 
 int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
@@ -387,15 +405,16 @@ static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const 
                          cols, status, &l);
   if (st == 1) return POLY_OK;
   if (st != POLY_OK) return st;
+  const int variant = g_swiglu_variant.load();
   poly_program ps, pd;
-  st = swiglu_programs(dtype, bwd, &ps, &pd);
+  st = swiglu_programs(variant, dtype, bwd, &ps, &pd);
   if (st != POLY_OK) return st;
   Streams s{static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(u),
             static_cast<const uint16_t *>(dy), static_cast<uint16_t *>(o0),
             static_cast<uint16_t *>(o1)};
   return cuda_status(launch_poly(bwd ? kSwigluBwd : kSwigluFwd, dtype, ps.form, ps.degree,
                                  pd.degree, s, l, dev_prog(ps), dev_prog(pd),
-                                 reinterpret_cast<cudaStream_t>(stream)));
+                                 reinterpret_cast<cudaStream_t>(stream), variant));
 }
 
 int poly_swiglu_fwd_ragged(int dtype, const void *g, const void *u, void *y,

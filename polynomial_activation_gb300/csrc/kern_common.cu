@@ -7,7 +7,7 @@ namespace dev {
 
 cudaError_t launch_act(int kind, int dtype, int form, int deg, const Streams &s,
                        const Layout &l, const ProgPair &p, cudaStream_t st);
-cudaError_t launch_swiglu(int kind, int dtype, int ds, int dd, const Streams &s,
+cudaError_t launch_swiglu(int kind, int variant, int dtype, int ds, int dd, const Streams &s,
                           const Layout &l, const ProgPair &p, cudaStream_t st);
 
 int64_t grid_for(const Layout &l, int per_thread) {
@@ -63,11 +63,11 @@ cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
 
 cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, const Streams &s,
                         const Layout &l, const DevProg &p1, const DevProg &p2,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int variant) {
   dev::ProgPair pp{p1, p2};
   if (kind == kActFwd || kind == kActBwd)
     return dev::launch_act(kind, dtype, form1, deg1, s, l, pp, stream);
-  return dev::launch_swiglu(kind, dtype, deg1, deg2, s, l, pp, stream);
+  return dev::launch_swiglu(kind, variant, dtype, deg1, deg2, s, l, pp, stream);
 }
 
 }  // namespace polyact

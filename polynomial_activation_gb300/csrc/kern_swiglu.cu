@@ -39,8 +39,31 @@ static cudaError_t sw_dt(int kind, int ds, int dd, const Streams &s, const Layou
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_swiglu(int kind, int dtype, int ds, int dd, const Streams &s,
+template <int DT>
+static cudaError_t sw_sig_dt(int kind, int dp, const Streams &s, const Layout &l,
+                             const ProgPair &p, cudaStream_t st) {
+#define POLYACT_SIG(D)                                                        \
+  case D:                                                                     \
+    return kind == kSwigluFwd ? launch_op<OpSwigluSigFwd<DT, D>>(s, l, p, st) \
+                              : launch_op<OpSwigluSigBwd<DT, D>>(s, l, p, st);
+  switch (dp) {
+    POLYACT_SIG(3)
+    POLYACT_SIG(4)
+    POLYACT_SIG(5)
+    POLYACT_SIG(6)
+  }
+#undef POLYACT_SIG
+  return cudaErrorInvalidValue;
+}
+
+// variant 0: direct SiLU program (+ centred SiLU' program in backward);
+// variant 1: sigmoid program recomputed, SiLU and SiLU' formed algebraically
+// (ds = the sigmoid program's degree, dd unused).
+cudaError_t launch_swiglu(int kind, int variant, int dtype, int ds, int dd, const Streams &s,
                           const Layout &l, const ProgPair &p, cudaStream_t st) {
+  if (variant == 1)
+    return dtype == kF16 ? sw_sig_dt<kF16>(kind, ds, s, l, p, st)
+                         : sw_sig_dt<kBF16>(kind, ds, s, l, p, st);
   return dtype == kF16 ? sw_dt<kF16>(kind, ds, dd, s, l, p, st)
                        : sw_dt<kBF16>(kind, ds, dd, s, l, p, st);
 }

@@ -45,10 +45,11 @@ struct Layout {
 
 enum Kind { kActFwd = 0, kActBwd = 1, kSwigluFwd = 2, kSwigluBwd = 3 };
 
-// Polynomial programs.  p2 is used by kSwigluBwd only (the SiLU derivative).
+// Polynomial programs.  p2 is used by kSwigluBwd of variant 0 only (the SiLU
+// derivative); SwiGLU variant 1 takes the sigmoid program in p1.
 cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, const Streams &s,
                         const Layout &l, const DevProg &p1, const DevProg &p2,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int variant = 0);
 
 // MUFU controls (fn used by kActFwd / kActBwd).
 cudaError_t launch_ctrl(int kind, int dtype, int fn, const Streams &s, const Layout &l,

@@ -97,5 +97,37 @@ struct OpSwigluBwd {
   }
 };
 
+// The paper's deployed B1/B4 rule (§3.3, §5.2.4): recompute the sigmoid
+// program p(g) and form SiLU and its derivative algebraically.
+// y = (g * p) * u; inputs (g, u)
+template <int DT, int DP>
+struct OpSwigluSigFwd {
+  static constexpr int NIN = 2, NOUT = 1;
+  static constexpr bool TWO_D = true;
+  using Params = ProgPair;
+  __device__ __forceinline__ static void pair(const uint32_t (&a)[2], uint32_t (&b)[1],
+                                              const Params &p) {
+    const uint32_t pg = eval_prog<DT, POLY_FORM_CO, DP>(a[0], p.p1);
+    b[0] = pmul<DT>(pmul<DT>(a[0], pg), a[1]);
+  }
+};
+
+// s = g p, q = fma(-p, p, p) = p (1 - p), s' = fma(g, q, p);
+// dg = (dy * u) * s', du = dy * s; inputs (g, u, dy)
+template <int DT, int DP>
+struct OpSwigluSigBwd {
+  static constexpr int NIN = 3, NOUT = 2;
+  static constexpr bool TWO_D = true;
+  using Params = ProgPair;
+  __device__ __forceinline__ static void pair(const uint32_t (&a)[3], uint32_t (&b)[2],
+                                              const Params &p) {
+    const uint32_t pg = eval_prog<DT, POLY_FORM_CO, DP>(a[0], p.p1);
+    const uint32_t q = pfma<DT>(pg ^ 0x80008000u, pg, pg);
+    const uint32_t sd = pfma<DT>(a[0], q, pg);
+    b[0] = pmul<DT>(pmul<DT>(a[2], a[1]), sd);
+    b[1] = pmul<DT>(a[2], pmul<DT>(a[0], pg));
+  }
+};
+
 }  // namespace dev
 }  // namespace polyact

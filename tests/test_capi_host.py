@@ -161,3 +161,14 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_swiglu_fwd_ragged(1, None, None, None, FAKE, 4, 0, 16, None, s) == B.POLY_OK
     assert L.poly_diag_packed(0, 0, None, None, None, None, 0, s) == B.POLY_OK
     assert L.poly_last_cuda_error() == 0
+
+
+def test_swiglu_variant_switch(L):
+    assert B.poly_get_swiglu_variant() == B.POLY_SWIGLU_DIRECT
+    try:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
+        assert B.poly_get_swiglu_variant() == B.POLY_SWIGLU_SIGMOID
+        assert L.poly_set_swiglu_variant(7) == B.POLY_EINVAL
+        assert B.poly_get_swiglu_variant() == B.POLY_SWIGLU_SIGMOID
+    finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)

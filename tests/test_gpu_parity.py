@@ -416,3 +416,70 @@ def test_host_memory_operands(dt):
     B.poly_act_fwd(B.POLY_SILU, dt, xd, yh2, x.size)
     torch.cuda.synchronize()
     assert np.array_equal(yh2.view(torch.int16).numpy().view(np.uint16), forward(op, x))
+
+
+@pytest.fixture
+def sigmoid_swiglu():
+    B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
+    try:
+        yield
+    finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_swiglu_sigmoid_rule_every_element(dt, sigmoid_swiglu):
+    """The paper's deployed B1/B4 rule, dense, strided and ragged layouts."""
+    from oracle.replay import swiglu_sigmoid_backward, swiglu_sigmoid_forward
+    fmt = FMT[dt]
+    sig = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    rng = np.random.default_rng(61)
+    for rows, cols, pad in [(1, 1, 0), (13, 1003, 0), (64, 2048, 0), (37, 2048, 8), (9, 1001, 5)]:
+        W = cols + pad
+        g = _rand_bits(rng, rows * W, fmt).reshape(rows, W)
+        u = _rand_bits(rng, rows * W, fmt).reshape(rows, W)
+        dy = _rand_bits(rng, rows * W, fmt).reshape(rows, W)
+        gd, ud, dyd = (to_dev(a, dt).view(rows, W)[:, :cols] for a in (g, u, dy))
+        gg, uu, dd = g[:, :cols], u[:, :cols], dy[:, :cols]
+        y = torch.empty(rows, cols, dtype=TDT[dt], device=DEV)
+        B.poly_swiglu_fwd(dt, gd, ud, y)
+        assert np.array_equal(from_dev(y).reshape(rows, cols), swiglu_sigmoid_forward(sig, gg, uu))
+        dg = torch.empty_like(y)
+        du = torch.empty_like(y)
+        B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+        wdg, wdu = swiglu_sigmoid_backward(sig, gg, uu, dd)
+        assert np.array_equal(from_dev(dg).reshape(rows, cols), wdg)
+        assert np.array_equal(from_dev(du).reshape(rows, cols), wdu)
+    cols, cap = 40, 30
+    seg = torch.from_numpy(np.array([0, 7, 7, 21, 26], dtype=np.int32)).to(DEV)
+    g = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
+    u = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
+    dy = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
+    dg = torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    du = torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    B.poly_swiglu_bwd_ragged(dt, to_dev(g, dt).view(cap, cols), to_dev(u, dt).view(cap, cols),
+                             to_dev(dy, dt).view(cap, cols), dg, du, seg)
+    wdg, wdu = swiglu_sigmoid_backward(sig, g[:26], u[:26], dy[:26])
+    assert np.array_equal(from_dev(dg).reshape(cap, cols)[:26], wdg)
+    assert np.array_equal(from_dev(du).reshape(cap, cols)[:26], wdu)
+    assert np.all(from_dev(dg).reshape(cap, cols)[26:] == 0x5A5A)
+
+
+def test_swiglu_sigmoid_rule_dense_full_size_sampled(sigmoid_swiglu):
+    from oracle.replay import swiglu_sigmoid_backward, swiglu_sigmoid_forward
+    dt = B.POLY_BF16
+    sig = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    g, u, dy = workloads.dense_swiglu("bf16")
+    rows, cols = g.shape
+    gd, ud, dyd = (to_dev(a, dt).view(rows, cols) for a in (g, u, dy))
+    y, dg, du = torch.empty_like(gd), torch.empty_like(gd), torch.empty_like(gd)
+    B.poly_swiglu_fwd(dt, gd, ud, y)
+    B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+    n = g.size
+    s = np.unique(np.random.default_rng(71).integers(0, n, 1 << 20))
+    sd = torch.from_numpy(s).to(DEV)
+    gf, uf, dyf = g.reshape(-1), u.reshape(-1), dy.reshape(-1)
+    assert np.array_equal(from_dev(y.view(-1)[sd]), swiglu_sigmoid_forward(sig, gf[s], uf[s]))
+    wdg, wdu = swiglu_sigmoid_backward(sig, gf[s], uf[s], dyf[s])
+    assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
+    assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)

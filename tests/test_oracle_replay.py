@@ -200,3 +200,41 @@ def test_must_fail_coarsened_program():
     y = tf.decode(evaluate(p.form, tuple(coarse), p.lc_bits, X[fin], p.fmt), p.fmt)
     err = np.max(np.abs(y - ref.sigmoid(tf.decode(X[fin], p.fmt))))
     assert err > p.info["stated_max_abs_err"]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_swiglu_sigmoid_rule_vs_exact_and_fp64(fmt):
+    """The deployed B1/B4 rule (s = g p, s' = p + g p (1 - p)) element by
+    element in exact rationals, and its error against the FP64 SiLU and SiLU'
+    within the bound the sigmoid program's own error implies."""
+    from oracle.replay import swiglu_sigmoid_backward, swiglu_sigmoid_forward
+    sig = PROGS[gp.key(ref.SIGMOID, ref.FWD, fmt, 3)]
+    rng = np.random.default_rng(17)
+    g = tf.from_f64(rng.normal(0, 3, 4000), fmt)
+    u = tf.from_f64(rng.normal(0, 1, 4000), fmt)
+    dy = tf.from_f64(rng.normal(0, 1, 4000), fmt)
+    one = int(tf.from_f64(1.0, fmt))
+    y = swiglu_sigmoid_forward(sig, g, u)
+    dg, du = swiglu_sigmoid_backward(sig, g, u, dy)
+    p = forward(sig, g)
+    for i in range(0, 4000, 9):
+        pi, gi = int(p[i]), int(g[i])
+        s = ex.mul(gi, pi, fmt)
+        assert int(y[i]) == ex.mul(s, int(u[i]), fmt)
+        q = ex.fma(pi ^ 0x8000, pi, pi, fmt)
+        sd = ex.fma(gi, q, pi, fmt)
+        assert int(du[i]) == ex.mul(int(dy[i]), s, fmt)
+        assert int(dg[i]) == ex.mul(ex.mul(int(dy[i]), int(u[i]), fmt), sd, fmt)
+    # error of s = g p and s' against FP64, with u = dy = 1
+    x = X[tf.finite_mask(X, fmt)]
+    xv = tf.decode(x, fmt)
+    x, xv = x[np.abs(xv) < 64], xv[np.abs(xv) < 64]
+    ones = np.full(x.size, one, np.uint16)
+    s = tf.decode(swiglu_sigmoid_forward(sig, x, ones), fmt)
+    sd = tf.decode(swiglu_sigmoid_backward(sig, x, ones, ones)[0], fmt)
+    e_p = sig.info["stated_max_abs_err"]
+    ulp = 2.0 ** (-10 if fmt == "f16" else -7)
+    assert np.all(np.abs(s - ref.silu(xv)) <= np.abs(xv) * (e_p + ulp) + ulp)
+    # s' = p + x p (1 - p): |d s'| <= e_p (1 + |x| |1 - 2p|) + rounding
+    bound = e_p * (1 + np.abs(xv)) + 4 * ulp * (1 + np.abs(xv))
+    assert np.all(np.abs(sd - ref.dsilu(xv)) <= bound)
