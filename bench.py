@@ -365,6 +365,7 @@ def main():
 
     # ---- extras: SwiGLU and the L2-resident sweep
     if not args.no_extras:
+        result["softcap"] = softcap_extras(x, dy, outs[0], n, stream, peak)
         result["swiglu"] = swiglu_extras(args, dev, stream, peak)
         result["l2_resident"] = l2_extras(dev, stream)
 
@@ -402,6 +403,32 @@ def _time(fn, stream, reps, warm=3):
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / reps
+
+
+def softcap_extras(x, dy, y, n, stream, peak, alpha=30.0):
+    """alpha tanh(x / alpha) forward and its backward on the step's tensors,
+    with the direct tanh' D4 program and with the differentiated D3 one."""
+    from polynomial_activation_gb300 import binding as B
+    f16 = B.POLY_F16
+    res = {"alpha": alpha}
+    for label, fn, nbytes in [
+        ("fwd", lambda: B.poly_softcap_fwd(f16, alpha, x, y, n), 4),
+        ("bwd_direct_D4", lambda: B.poly_softcap_bwd(f16, alpha, x, dy, y, n), 6),
+    ]:
+        ms = _time(fn, stream, 20)
+        res[label] = {"ms": ms, "gbs": nbytes * n / ms / 1e6, "frac": nbytes * n / ms / 1e6 / peak}
+    d = B.poly_derive_program(B.poly_get_program(B.POLY_TANH, B.POLY_FWD, f16))
+    B.poly_set_program(d)
+    try:
+        ms = _time(lambda: B.poly_softcap_bwd(f16, alpha, x, dy, y, n), stream, 20)
+        res["bwd_differentiated_D3"] = {"ms": ms, "gbs": 6 * n / ms / 1e6,
+                                        "frac": 6 * n / ms / 1e6 / peak,
+                                        "stated_max_abs_err": d.stated_max_abs_err}
+    finally:
+        B.poly_reset_programs()
+        for name, dd, D in SIX:
+            B.poly_get_program(FN[name], dd, f16)
+    return res
 
 
 def swiglu_extras(args, dev, stream, peak):

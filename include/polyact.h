@@ -157,6 +157,20 @@ int poly_get_program(int fn, int dir, int dtype, poly_program *out);
 /* Forget every installed program (defaults are re-fitted on next use). */
 int poly_reset_programs(void);
 
+/* Differentiated-polynomial backward (§3.3: B2 "differentiates its D4 tanh
+ * program and evaluates the resulting D3 program").  From an odd or
+ * centred-odd forward program y = [1/2 +] sign(x) (c_1 t + ... + c_D t^D)
+ * write to *out the even backward program of degree D - 1 with
+ * coefficients (j + 1) c_(j+1), each rounded once to the target format, the
+ * same clamp (beyond Lc it keeps its value at Lc) and its own stated bound
+ * against the true derivative.  Install it with poly_set_program to use it
+ * in poly_act_bwd / poly_softcap_bwd in place of the direct derivative fit.
+ * Host only.  POLY_EINVAL for a NULL pointer or a program that is not an odd
+ * or centred-odd forward program; POLY_ENOPROG for an inconsistent one.
+ * Direct fits are the default because they are 4-7x more accurate (the
+ * paper: "backward has its own error profile"). */
+int poly_derive_program(const poly_program *fwd, poly_program *out);
+
 /* ---- elementwise programs (§5.1.1, Table 3) ------------------------------ */
 
 /* y[i] = program_fwd(fn, dtype)(x[i]) for i < n.  x, y: device, n elements.
@@ -216,6 +230,22 @@ int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u,
                            const int32_t *seg_off, int num_segments,
                            int64_t cap_rows, int64_t cols, int32_t *status,
                            poly_stream_t stream);
+
+/* ---- tanh softcap (§2.3 eq. 1; §3.3 eq. 12) -------------------------------
+ * softcap_alpha(x) = alpha tanh(x / alpha), the attention-logit softcap.
+ * Forward:   z = x * A_inv,  y = A * tanh_program(z)
+ * Backward:  z = x * A_inv,  dx = dy * dtanh_program(z)     (alpha cancels)
+ * with A = alpha and A_inv = 1/alpha (formed in FP64) rounded once to the
+ * target format; every product rounds once.  tanh_program is the installed
+ * tanh forward program, dtanh_program the installed tanh backward program
+ * (the direct derivative fit by default, or one from poly_derive_program).
+ * POLY_EINVAL if alpha is not finite and > 0 or if A or A_inv would be zero
+ * or infinite in the target format; otherwise the conventions of
+ * poly_act_fwd / poly_act_bwd. */
+int poly_softcap_fwd(int dtype, double alpha, const void *x, void *y, int64_t n,
+                     poly_stream_t stream);
+int poly_softcap_bwd(int dtype, double alpha, const void *x, const void *dy, void *dx,
+                     int64_t n, poly_stream_t stream);
 
 /* ---- MUFU-native controls (same signatures and memory schedule) ----------
  * FP32 math on the special-function unit: sigmoid = rcp.approx(1 +

@@ -147,6 +147,47 @@ def swiglu_sigmoid_backward(sig_prog: Program, g, u, dy):
     return dg, du
 
 
+def derive(prog: Program) -> Program:
+    """Differentiated-polynomial backward (§3.3: "B2 differentiates its D4
+    tanh program and evaluates the resulting D3 program").  For an odd or
+    centred-odd program y = [1/2 +] sign(x) (c_1 t + ... + c_D t^D), the
+    derivative on |x| < Lc is the even polynomial c_1 + 2 c_2 t + ... +
+    D c_D t^(D-1); each coefficient (j+1) c_(j+1) is rounded once to the
+    target format.  The result is an even-form program of degree D - 1 with
+    the same clamp (beyond Lc it keeps the value at Lc)."""
+    assert prog.form in (CO, O)
+    c = prog.coef_values()
+    e = [(j + 1) * float(c[j + 1]) for j in range(prog.degree)]   # exact in FP64
+    bits = tuple(int(b) for b in tf.from_f64(np.array(e), prog.fmt))
+    from .reference import BWD
+    return Program(fn=prog.fn, direction=BWD, fmt=prog.fmt, degree=prog.degree - 1,
+                   li=prog.li, lc=prog.lc, coef=bits, lc_bits=prog.lc_bits,
+                   info={"derived_from_degree": prog.degree})
+
+
+def softcap_consts(alpha: float, fmt: str):
+    """alpha and 1/alpha rounded once to the target format."""
+    return int(tf.from_f64(alpha, fmt)), int(tf.from_f64(1.0 / alpha, fmt))
+
+
+def softcap_forward(tanh_prog: Program, alpha: float, x):
+    """softcap_alpha(x) = alpha tanh(x / alpha) (§2.3 eq. 1): z = x * (1/alpha),
+    y = alpha * tanh_program(z), each product rounded once."""
+    fmt = tanh_prog.fmt
+    a, ia = softcap_consts(alpha, fmt)
+    z = tf.mul(x, np.uint16(ia), fmt)
+    return tf.mul(np.uint16(a), forward(tanh_prog, z), fmt)
+
+
+def softcap_backward(dtanh_prog: Program, alpha: float, x, dy):
+    """d/dx softcap = tanh'(x / alpha) (eq. 12: the scale cancels):
+    dx = dy * dtanh_program(x * (1/alpha)), each product rounded once."""
+    fmt = dtanh_prog.fmt
+    _, ia = softcap_consts(alpha, fmt)
+    z = tf.mul(x, np.uint16(ia), fmt)
+    return tf.mul(dy, forward(dtanh_prog, z), fmt)
+
+
 def evaluate_real(form, coef_values, lc, x):
     """Real-arithmetic replay (FP64, no intermediate rounding): the Table 2
     metric evaluates the rounded coefficients this way (§4.1)."""

@@ -30,6 +30,7 @@ EXPORTS = [
     "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
     "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
+    "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd",
 ]
 POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID = 0, 1
 POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
@@ -85,6 +86,9 @@ def lib():
     L.poly_status_str.restype = ctypes.c_char_p
     L.poly_status_str.argtypes = [_i]
     L.poly_set_swiglu_variant.argtypes = [_i]
+    L.poly_derive_program.argtypes = [ctypes.POINTER(PolyProgram), ctypes.POINTER(PolyProgram)]
+    L.poly_softcap_fwd.argtypes = [_i, ctypes.c_double, _p, _p, _i64, _p]
+    L.poly_softcap_bwd.argtypes = [_i, ctypes.c_double, _p, _p, _p, _i64, _p]
     for name in ("poly_last_cuda_error", "poly_abi_version", "poly_reset_programs",
                  "poly_get_swiglu_variant"):
         getattr(L, name).restype = _i
@@ -284,3 +288,21 @@ def poly_diag_packed(op, dtype, a, b, c, out, n=None, stream=None):
     n = a.numel() if n is None else n
     _check(lib().poly_diag_packed(op, dtype, _ptr(a), _ptr(b), _ptr(c), _ptr(out), n,
                                   _stream(stream)), "poly_diag_packed")
+
+
+def poly_derive_program(fwd: PolyProgram):
+    out = PolyProgram()
+    _check(lib().poly_derive_program(ctypes.byref(fwd), ctypes.byref(out)), "poly_derive_program")
+    return out
+
+
+def poly_softcap_fwd(dtype, alpha, x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_softcap_fwd(dtype, float(alpha), _ptr(x), _ptr(y), n, _stream(stream)),
+           "poly_softcap_fwd")
+
+
+def poly_softcap_bwd(dtype, alpha, x, dy, dx, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_softcap_bwd(dtype, float(alpha), _ptr(x), _ptr(dy), _ptr(dx), n,
+                                  _stream(stream)), "poly_softcap_bwd")

@@ -13,8 +13,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpolyact.so")
-SOURCES = ["kern_act.cu", "kern_swiglu.cu", "kern_ctrl.cu", "kern_common.cu", "capi.cpp",
-           "fit.cpp"]
+SOURCES = ["kern_act.cu", "kern_swiglu.cu", "kern_ctrl.cu", "kern_common.cu", "kern_softcap.cu",
+           "capi.cpp", "fit.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # host code: no floating-point contraction, so the fitter's FP64 arithmetic is
 # the same on x86-64 and aarch64

@@ -5,12 +5,14 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/polyact.h"
 #include "fit_internal.h"
 #include "launch.h"
+#include "softhalf.h"
 
 using namespace polyact;
 
@@ -43,7 +45,9 @@ DevProg dev_prog(const poly_program &p) {
 
 int check_program(const poly_program &p) {
   if (!valid_fn(p.fn) || !valid_dir(p.dir) || !valid_dtype(p.dtype)) return POLY_ENOPROG;
-  if (p.degree < POLY_MIN_DEGREE || p.degree > POLY_MAX_DEGREE) return POLY_ENOPROG;
+  // even programs may have degree 2 (derived from a degree-3 forward program)
+  const int min_degree = p.form == POLY_FORM_E ? 2 : POLY_MIN_DEGREE;
+  if (p.degree < min_degree || p.degree > POLY_MAX_DEGREE) return POLY_ENOPROG;
   if (p.form != form_of_fn(p.fn, p.dir)) return POLY_ENOPROG;
   if (p.version != POLY_PROGRAM_VERSION) return POLY_ENOPROG;
   const bool even = p.form == POLY_FORM_E;
@@ -271,6 +275,15 @@ int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
   return fit_program(fn, dir, dtype, degree, o, out);
 }
 
+int poly_derive_program(const poly_program *fwd, poly_program *out) {
+  if (fwd == nullptr || out == nullptr) return POLY_EINVAL;
+  int st = check_program(*fwd);
+  if (st != POLY_OK) return st;
+  if (fwd->dir != POLY_FWD || (fwd->form != POLY_FORM_O && fwd->form != POLY_FORM_CO))
+    return POLY_EINVAL;
+  return derive_program(*fwd, out);
+}
+
 int poly_set_program(const poly_program *p) {
   if (p == nullptr) return POLY_EINVAL;
   int st = check_program(*p);
@@ -429,6 +442,45 @@ int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u, const void *
                            int64_t cols, int32_t *status, poly_stream_t stream) {
   return ragged_call(true, dtype, g, u, dy, dg, du, seg_off, num_segments, cap_rows, cols,
                      status, stream);
+}
+
+// Shared part of the softcap calls: alpha must give finite, non-zero
+// target-format constants alpha and 1/alpha (1/alpha formed in FP64, then
+// rounded once).
+static int softcap_call(bool bwd, int dtype, double alpha, const void *x, const void *dy,
+                        void *out, int64_t n, poly_stream_t stream) {
+  if (!valid_dtype(dtype) || n < 0 || !(alpha > 0) || !std::isfinite(alpha)) return POLY_EINVAL;
+  const uint16_t a = from_double(alpha, dtype), ia = from_double(1.0 / alpha, dtype);
+  auto usable = [&](uint16_t b) {
+    const double v = to_double(b, dtype);
+    return std::isfinite(v) && v != 0.0;
+  };
+  if (!usable(a) || !usable(ia)) return POLY_EINVAL;
+  if (n == 0) return POLY_OK;
+  if (x == nullptr || out == nullptr || (bwd && dy == nullptr)) return POLY_EINVAL;
+  if (!even_address(x) || !even_address(out) || (bwd && !even_address(dy))) return POLY_EINVAL;
+  Span si[2] = {span_flat(x, n), span_flat(bwd ? dy : x, n)};
+  Span so[1] = {span_flat(out, n)};
+  if (!aliasing_ok(si, bwd ? 2 : 1, so, 1)) return POLY_EINVAL;
+  const void *ptrs[3] = {x, bwd ? dy : x, out};
+  Layout l = flat_layout(ptrs, 3, n);
+  poly_program p;
+  int st = registry_get(POLY_TANH, bwd ? POLY_BWD : POLY_FWD, dtype, &p);
+  if (st != POLY_OK) return st;
+  Streams s{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dy), nullptr,
+            static_cast<uint16_t *>(out), nullptr};
+  return cuda_status(launch_softcap(bwd ? 1 : 0, dtype, p.degree, s, l, dev_prog(p), a, ia,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int poly_softcap_fwd(int dtype, double alpha, const void *x, void *y, int64_t n,
+                     poly_stream_t stream) {
+  return softcap_call(false, dtype, alpha, x, nullptr, y, n, stream);
+}
+
+int poly_softcap_bwd(int dtype, double alpha, const void *x, const void *dy, void *dx, int64_t n,
+                     poly_stream_t stream) {
+  return softcap_call(true, dtype, alpha, x, dy, dx, n, stream);
 }
 
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c, void *out,

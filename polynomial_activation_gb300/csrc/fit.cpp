@@ -270,6 +270,41 @@ static double table2_metric(int fn, int dir, int dtype, int form, int degree, co
   return worst;
 }
 
+// Differentiated-polynomial backward (§3.3): an odd / centred-odd program
+// y = [1/2 +] sign(x) (c_1 t + ... + c_D t^D) has, on |x| < Lc, the even
+// derivative c_1 + 2 c_2 t + ... + D c_D t^(D-1); each coefficient is formed
+// exactly in FP64 and rounded once.  Same clamp; degree D - 1.
+int derive_program(const poly_program &f, poly_program *out) {
+  poly_program d;
+  std::memset(&d, 0, sizeof(d));
+  d.fn = f.fn;
+  d.dir = POLY_BWD;
+  d.dtype = f.dtype;
+  d.form = POLY_FORM_E;
+  d.degree = f.degree - 1;
+  for (int j = 0; j < f.degree; ++j)
+    d.coef[j] = from_double((j + 1) * to_double(f.coef[j + 1], f.dtype), f.dtype);
+  d.lc_bits = f.lc_bits;
+  d.li = f.li;
+  d.lc = f.lc;
+  d.search_score = -1;       // not searched: derived from a searched program
+  d.deployed_score = -1;
+  d.rank = -1;
+  d.version = POLY_PROGRAM_VERSION;
+  double bound = 0;
+  for (uint32_t b = 0; b < 65536; ++b) {
+    const uint16_t x = (uint16_t)b;
+    const double xv = to_double(x, d.dtype);
+    if (!std::isfinite(xv)) continue;
+    const uint16_t yy = replay_one(d.form, d.coef, d.degree, d.lc_bits, x, d.dtype, true);
+    bound = std::max(bound, std::fabs(to_double(yy, d.dtype) - fn_value(d.fn, POLY_BWD, xv)));
+  }
+  d.stated_max_abs_err = bound;
+  d.table2 = table2_metric(d.fn, POLY_BWD, d.dtype, d.form, d.degree, d.coef, d.lc);
+  *out = d;
+  return POLY_OK;
+}
+
 int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
                 poly_program *out) {
   const int form = form_of_fn(fn, dir);

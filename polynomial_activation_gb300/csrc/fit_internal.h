@@ -16,5 +16,6 @@ double replay_real(int form, const double *c, int degree, double lc, double x);
 void fit_coefficients(int fn, int dir, int degree, double li, int n_nodes, double *c);
 int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
                 poly_program *out);
+int derive_program(const poly_program &fwd, poly_program *out);
 
 }  // namespace polyact

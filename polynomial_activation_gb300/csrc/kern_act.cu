@@ -22,6 +22,11 @@ static cudaError_t act_deg(int kind, int deg, const Streams &s, const Layout &l,
     }                                                                            \
     return cudaErrorInvalidValue;
   switch (deg) {
+    case 2:   // only even programs derived from degree-3 forward programs
+      if constexpr (FORM == POLY_FORM_E) {
+        if (kind == kActBwd) return launch_op<OpBwd<DT, POLY_FORM_E, 2>>(s, l, p, st);
+      }
+      return cudaErrorInvalidValue;
     POLYACT_CASE(3)
     POLYACT_CASE(4)
     POLYACT_CASE(5)

@@ -55,6 +55,12 @@ cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, cons
 cudaError_t launch_ctrl(int kind, int dtype, int fn, const Streams &s, const Layout &l,
                         cudaStream_t stream);
 
+// Tanh softcap: forward with the odd tanh program, backward with an even
+// derivative program; alpha and 1/alpha as target-format bit patterns.
+cudaError_t launch_softcap(int bwd, int dtype, int degree, const Streams &s, const Layout &l,
+                           const DevProg &p, uint16_t alpha, uint16_t inv_alpha,
+                           cudaStream_t stream);
+
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
                         cudaStream_t stream);

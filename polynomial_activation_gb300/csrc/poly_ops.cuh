@@ -20,7 +20,7 @@ namespace dev {
 
 template <int DT, int FORM, int D>
 __device__ __forceinline__ uint32_t eval_prog(uint32_t x, const DevProg &p) {
-  static_assert(D >= POLY_MIN_DEGREE && D <= POLY_MAX_DEGREE, "degree");
+  static_assert(D >= 2 && D <= POLY_MAX_DEGREE, "degree");
   const uint32_t a = x & 0x7FFF7FFFu;
   const uint32_t t = pmin_nan<DT>(a, p.lc);
   constexpr int last = FORM == POLY_FORM_E ? 0 : 1;

@@ -172,3 +172,41 @@ def test_swiglu_variant_switch(L):
         assert B.poly_get_swiglu_variant() == B.POLY_SWIGLU_SIGMOID
     finally:
         B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("fn,D", [(0, 3), (1, 4), (2, 4), (3, 4)])
+def test_derive_program_matches_oracle(L, fmt, fn, D):
+    """poly_derive_program (C++) equals the oracle's differentiated program."""
+    from oracle.replay import derive
+    dt = B.POLY_F16 if fmt == "f16" else B.POLY_BF16
+    if fn in (2, 3):        # SiLU / GELU forward are x/2 + even: not differentiable this way
+        p = B.poly_fit(fn, 0, dt, 3)
+        out = B.PolyProgram()
+        assert L.poly_derive_program(ctypes.byref(p), ctypes.byref(out)) == B.POLY_EINVAL
+        return
+    p = B.poly_fit(fn, 0, dt, D)
+    d = B.poly_derive_program(p)
+    od = derive(gp.get(fn, 0, fmt, D))
+    assert d.form == B.POLY_FORM_E and d.dir == B.POLY_BWD and d.degree == D - 1
+    assert d.coefficients() == list(od.coef) and d.lc_bits == od.lc_bits
+    from oracle import fit
+    assert d.stated_max_abs_err == pytest.approx(fit.exhaustive_error(od)[0], rel=1e-12)
+    B.poly_set_program(d)                     # degree 2 / 3 even programs install
+    assert B.poly_get_program(fn, 1, dt).degree == D - 1
+    B.poly_reset_programs()
+    # a backward program cannot be differentiated again
+    e = B.PolyProgram()
+    assert L.poly_derive_program(ctypes.byref(d), ctypes.byref(e)) == B.POLY_EINVAL
+    assert L.poly_derive_program(None, ctypes.byref(e)) == B.POLY_EINVAL
+
+
+def test_softcap_rejects_bad_alpha(L):
+    s = None
+    for dt, alpha in [(0, 0.0), (0, -1.0), (0, float("nan")), (0, float("inf")),
+                      (0, 1e6), (0, 1e10), (1, 1e39), (1, 1e-39)]:
+        assert L.poly_softcap_fwd(dt, alpha, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL, (dt, alpha)
+        assert L.poly_softcap_bwd(dt, alpha, FAKE, FAKE + 4096, FAKE + 8192, 8, s) == B.POLY_EINVAL
+    assert L.poly_softcap_fwd(0, 30.0, None, None, 0, s) == B.POLY_OK
+    assert L.poly_softcap_fwd(0, 30.0, FAKE, FAKE + 2, 8, s) == B.POLY_EINVAL
+    assert L.poly_softcap_bwd(1, 30.0, FAKE, None, FAKE + 8192, 8, s) == B.POLY_EINVAL

@@ -483,3 +483,52 @@ def test_swiglu_sigmoid_rule_dense_full_size_sampled(sigmoid_swiglu):
     wdg, wdu = swiglu_sigmoid_backward(sig, gf[s], uf[s], dyf[s])
     assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
     assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+
+
+# ------------------------------------------------- softcap, derived programs
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("alpha", [1.0, 30.0, 50.0])
+def test_softcap_exhaustive(dt, alpha):
+    """alpha tanh(x / alpha) forward and tanh'(x / alpha) backward over every
+    input pattern, bit for bit."""
+    from oracle.replay import softcap_backward, softcap_forward
+    fmt = FMT[dt]
+    tp = oracle_program(B.POLY_TANH, B.POLY_FWD, dt)
+    dp = oracle_program(B.POLY_TANH, B.POLY_BWD, dt)
+    x = X_ALL
+    dy = _rand_bits(np.random.default_rng(29), x.size, fmt)
+    xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+    out = torch.empty_like(xd)
+    B.poly_softcap_fwd(dt, alpha, xd, out)
+    assert np.array_equal(from_dev(out), softcap_forward(tp, alpha, x))
+    B.poly_softcap_bwd(dt, alpha, xd, dyd, out)
+    assert np.array_equal(from_dev(out), softcap_backward(dp, alpha, x, dy))
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("fn,D", [(B.POLY_TANH, 4), (B.POLY_SIGMOID, 3)])
+def test_derived_program_backward_exhaustive(dt, fn, D):
+    """The differentiated forward program installed as the backward program
+    (degree 3 for tanh, degree 2 for sigmoid), through poly_act_bwd and, for
+    tanh, the softcap backward."""
+    from oracle.replay import derive, softcap_backward
+    fmt = FMT[dt]
+    fwd = B.poly_get_program(fn, B.POLY_FWD, dt)
+    assert fwd.degree == D
+    d = B.poly_derive_program(fwd)
+    od = derive(oracle_program(fn, B.POLY_FWD, dt))
+    assert d.coefficients() == list(od.coef)
+    B.poly_set_program(d)
+    try:
+        x = X_ALL
+        dy = _rand_bits(np.random.default_rng(31), x.size, fmt)
+        xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+        out = torch.empty_like(xd)
+        B.poly_act_bwd(fn, dt, xd, dyd, out)
+        assert np.array_equal(from_dev(out), backward(od, x, dy))
+        if fn == B.POLY_TANH:
+            B.poly_softcap_bwd(dt, 30.0, xd, dyd, out)
+            assert np.array_equal(from_dev(out), softcap_backward(od, 30.0, x, dy))
+    finally:
+        B.poly_reset_programs()

@@ -238,3 +238,82 @@ def test_swiglu_sigmoid_rule_vs_exact_and_fp64(fmt):
     # s' = p + x p (1 - p): |d s'| <= e_p (1 + |x| |1 - 2p|) + rounding
     bound = e_p * (1 + np.abs(xv)) + 4 * ulp * (1 + np.abs(xv))
     assert np.all(np.abs(sd - ref.dsilu(xv)) <= bound)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("fn", [ref.TANH, ref.SIGMOID])
+def test_derived_program_is_the_polynomial_derivative(fmt, fn):
+    """The differentiated program's coefficients are the derivative of the
+    forward polynomial (numpy polyder) rounded once; multiples by powers of
+    two are exact; in real arithmetic the two agree to the coefficient
+    rounding."""
+    from oracle.replay import derive
+    D = 4 if fn == ref.TANH else 3
+    p = PROGS[gp.key(fn, ref.FWD, fmt, D)]
+    d = derive(p)
+    assert d.form == "E" and d.degree == D - 1 and d.lc_bits == p.lc_bits
+    c = p.coef_values()
+    e = d.coef_values()
+    want = npoly.polyder(c)                        # c_1 + 2 c_2 t + ... (c_0 = 0)
+    assert e[0] == want[0] and e[1] == want[1]     # 1 x c_1 and 2 x c_2: exact
+    if D >= 4:
+        assert e[3] == want[3]                     # 4 x c_4: exact
+    ulp = 2.0 ** (-10 if fmt == "f16" else -7)
+    assert np.all(np.abs(e - want) <= np.abs(want) * ulp / 2 + 1e-30)
+    t = np.linspace(0, p.lc, 501)
+    assert np.max(np.abs(npoly.polyval(t, e) - npoly.polyval(t, want))) <= \
+        np.sum(np.abs(want) * ulp / 2 * p.lc ** np.arange(D))
+    # it approximates the true derivative, but worse than the direct
+    # derivative fit: "backward has its own error profile" (Appendix D,
+    # item 2; §5.1 on the backward sweeps)
+    f = ref.function(fn, ref.BWD)
+    x = X[tf.finite_mask(X, fmt)]
+    y = tf.decode(forward(d, x), fmt)
+    err = np.max(np.abs(y - f(tf.decode(x, fmt))))
+    direct = PROGS[gp.key(fn, ref.BWD, fmt, 4)]
+    assert direct.info["stated_max_abs_err"] < err < 0.15
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_softcap_alpha_one_is_the_tanh_program(fmt):
+    from oracle.replay import softcap_forward
+    p = PROGS[gp.key(ref.TANH, ref.FWD, fmt, 4)]
+    assert np.array_equal(softcap_forward(p, 1.0, X), forward(p, X))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("alpha", [30.0, 50.0, 2.5])
+def test_softcap_symmetry_error_and_products(fmt, alpha):
+    """softcap is odd and its derivative even, bit for bit; the error against
+    FP64 alpha tanh(x / alpha) stays within alpha times the tanh program's
+    bound plus the two scalings' roundings; each product rounds once."""
+    from oracle.replay import softcap_backward, softcap_consts, softcap_forward
+    p = PROGS[gp.key(ref.TANH, ref.FWD, fmt, 4)]
+    dp = PROGS[gp.key(ref.TANH, ref.BWD, fmt, 4)]
+    y, yn = softcap_forward(p, alpha, X), softcap_forward(p, alpha, _neg(X))
+    nan = tf.is_nan(X, fmt)
+    assert np.array_equal(y[~nan], yn[~nan] ^ np.uint16(0x8000))
+    ones = np.full(X.size, int(tf.from_f64(1.0, fmt)), np.uint16)
+    d, dn = softcap_backward(dp, alpha, X, ones), softcap_backward(dp, alpha, _neg(X), ones)
+    assert np.array_equal(d, dn)
+    a, ia = softcap_consts(alpha, fmt)
+    av, iav = float(tf.decode(np.uint16(a), fmt)), float(tf.decode(np.uint16(ia), fmt))
+    fin = tf.finite_mask(X, fmt) & (np.abs(tf.decode(X, fmt)) < 1e4)
+    xv = tf.decode(X[fin], fmt)
+    z = tf.decode(tf.mul(X[fin], np.uint16(ia), fmt), fmt)
+    yv = tf.decode(y[fin], fmt)
+    ulp = 2.0 ** (-10 if fmt == "f16" else -7)
+    bound = (av * p.info["stated_max_abs_err"] + av * np.abs(z - xv / alpha) + abs(av - alpha)
+             + ulp * np.abs(yv))
+    assert np.all(np.abs(yv - alpha * np.tanh(xv / alpha)) <= bound + 1e-12)
+    rng = np.random.default_rng(23)
+    xs = tf.from_f64(rng.normal(0, alpha, 500), fmt)
+    dys = tf.from_f64(rng.normal(0, 1, 500), fmt)
+    ys = softcap_forward(p, alpha, xs)
+    ds = softcap_backward(dp, alpha, xs, dys)
+    zs = tf.mul(xs, np.uint16(ia), fmt)
+    th, dth = forward(p, zs), forward(dp, zs)
+    for i in range(500):
+        assert int(zs[i]) == ex.mul(int(xs[i]), ia, fmt)
+        assert int(ys[i]) == ex.mul(a, int(th[i]), fmt)
+        assert int(ds[i]) == ex.mul(int(dys[i]), int(dth[i]), fmt)
