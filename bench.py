@@ -366,6 +366,7 @@ def main():
     # ---- extras: SwiGLU and the L2-resident sweep
     if not args.no_extras:
         result["softcap"] = softcap_extras(x, dy, outs[0], n, stream, peak)
+        result["exp2"] = exp2_extras(dev, stream, peak)
         result["swiglu"] = swiglu_extras(args, dev, stream, peak)
         result["l2_resident"] = l2_extras(dev, stream)
 
@@ -428,6 +429,24 @@ def softcap_extras(x, dy, y, n, stream, peak, alpha=30.0):
         B.poly_reset_programs()
         for name, dd, D in SIX:
             B.poly_get_program(FN[name], dd, f16)
+    return res
+
+
+def exp2_extras(dev, stream, peak, n=1 << 27):
+    """2^x on FP32 tensors of 2^27 elements (512 MiB each, larger than L2)
+    through each fractional core and the MUFU control (Appendix B.1)."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    x = torch.from_numpy(np.random.default_rng(7).uniform(-60, 10, n).astype(np.float32)).to(dev)
+    y = torch.empty_like(x)
+    res = {"config": f"{n} FP32 elements, x ~ U[-60, 10]"}
+    for label, fn in [("D1", lambda: B.poly_exp2(B.POLY_EXP2_D1, x, y)),
+                      ("PWL2", lambda: B.poly_exp2(B.POLY_EXP2_PWL2, x, y)),
+                      ("D2", lambda: B.poly_exp2(B.POLY_EXP2_D2, x, y)),
+                      ("D3", lambda: B.poly_exp2(B.POLY_EXP2_D3, x, y)),
+                      ("mufu_ex2", lambda: B.poly_ctrl_exp2(x, y))]:
+        ms = _time(fn, stream, 20)
+        res[label] = {"ms": ms, "gbs": 8 * n / ms / 1e6, "frac": 8 * n / ms / 1e6 / peak}
     return res
 
 

@@ -247,6 +247,26 @@ int poly_softcap_fwd(int dtype, double alpha, const void *x, void *y, int64_t n,
 int poly_softcap_bwd(int dtype, double alpha, const void *x, const void *dy, void *dx,
                      int64_t n, poly_stream_t stream);
 
+/* ---- exp2 with a polynomial fractional core (Appendix B.1, eq. 16-19) -----
+ * y[i] = 2^x[i] for FP32 x, y (device addresses, n elements, y == x allowed):
+ * xc = min(max(x, -126), 128); n = floor(xc); f = xc - n (FP32, one
+ * rounding); h = f rounded to FP16; p = core(h) in packed FP16 arithmetic
+ * (one rounding per operation); y = float(p) scaled by 2^n through its
+ * exponent bits; NaN in -> 0x7FFFFFFF; x < -126 gives 2^-126.
+ * Cores (constants rounded to FP16 from the paper's parameters):
+ *   POLY_EXP2_D1    p = 1 + f                                   one FMA
+ *   POLY_EXP2_PWL2  p = 1 + a f + b max(f - 1/2, 0), a = 0.7980513010,
+ *                   b = 2 (1 - a) -> 0.7978515625, 0.40380859375 (eq. 17)
+ *   POLY_EXP2_D2    p = 1 + a f + (1 - a) f^2, a = 0.6602339719 (eq. 18)
+ *   POLY_EXP2_D3    FA4's cubic (eq. 19)
+ *   order: PWL2 p = fma(h, a, 1), m = max(fma(h, 1, -1/2), 0), p = fma(m, b, p);
+ *          D2 p = fma(fma(b, h, a), h, 1); D3 Horner from the top coefficient.
+ * POLY_EINVAL for an unknown core, n < 0, NULL or misaligned (not 4-byte)
+ * pointers, or partial overlap. */
+enum { POLY_EXP2_D1 = 0, POLY_EXP2_PWL2 = 1, POLY_EXP2_D2 = 2, POLY_EXP2_D3 = 3,
+       POLY_EXP2_MUFU = 4 };
+int poly_exp2(int core, const float *x, float *y, int64_t n, poly_stream_t stream);
+
 /* ---- MUFU-native controls (same signatures and memory schedule) ----------
  * FP32 math on the special-function unit: sigmoid = rcp.approx(1 +
  * ex2.approx(-x log2 e)); tanh = tanh.approx; SiLU = the overflow-safe form
@@ -263,6 +283,9 @@ int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy,
 int poly_ctrl_swiglu_fwd(int dtype, const void *g, const void *u, void *y,
                          int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
                          int64_t ldy, poly_stream_t stream);
+/* 2^x by ex2.approx.ftz.f32 on the special-function unit, same memory
+ * schedule and validation as poly_exp2. */
+int poly_ctrl_exp2(const float *x, float *y, int64_t n, poly_stream_t stream);
 int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u,
                          const void *dy, void *dg, void *du, int64_t rows,
                          int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,

@@ -30,8 +30,10 @@ EXPORTS = [
     "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
     "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
-    "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd",
+    "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd", "poly_exp2",
+    "poly_ctrl_exp2",
 ]
+POLY_EXP2_D1, POLY_EXP2_PWL2, POLY_EXP2_D2, POLY_EXP2_D3 = 0, 1, 2, 3
 POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID = 0, 1
 POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
 
@@ -87,6 +89,8 @@ def lib():
     L.poly_status_str.argtypes = [_i]
     L.poly_set_swiglu_variant.argtypes = [_i]
     L.poly_derive_program.argtypes = [ctypes.POINTER(PolyProgram), ctypes.POINTER(PolyProgram)]
+    L.poly_exp2.argtypes = [_i, _p, _p, _i64, _p]
+    L.poly_ctrl_exp2.argtypes = [_p, _p, _i64, _p]
     L.poly_softcap_fwd.argtypes = [_i, ctypes.c_double, _p, _p, _i64, _p]
     L.poly_softcap_bwd.argtypes = [_i, ctypes.c_double, _p, _p, _p, _i64, _p]
     for name in ("poly_last_cuda_error", "poly_abi_version", "poly_reset_programs",
@@ -306,3 +310,13 @@ def poly_softcap_bwd(dtype, alpha, x, dy, dx, n=None, stream=None):
     n = x.numel() if n is None else n
     _check(lib().poly_softcap_bwd(dtype, float(alpha), _ptr(x), _ptr(dy), _ptr(dx), n,
                                   _stream(stream)), "poly_softcap_bwd")
+
+
+def poly_exp2(core, x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_exp2(core, _ptr(x), _ptr(y), n, _stream(stream)), "poly_exp2")
+
+
+def poly_ctrl_exp2(x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    _check(lib().poly_ctrl_exp2(_ptr(x), _ptr(y), n, _stream(stream)), "poly_ctrl_exp2")

@@ -483,6 +483,49 @@ int poly_softcap_bwd(int dtype, double alpha, const void *x, const void *dy, voi
   return softcap_call(true, dtype, alpha, x, dy, dx, n, stream);
 }
 
+// FP16 constants of each exp2 core, from the paper's printed parameters
+// (Appendix B.1 eq. 17-19); PWL2's b = 2 (1 - a) and D2's 1 - a are formed
+// in FP64 (D2's from the already rounded a, which keeps p(1) = 2 exact).
+static void exp2_constants(int core, uint16_t *c) {
+  c[0] = c[1] = c[2] = 0;
+  if (core == POLY_EXP2_PWL2) {
+    const double a = 0.7980513010;
+    c[0] = from_double(a, POLY_F16);
+    c[1] = from_double(2.0 * (1.0 - a), POLY_F16);
+  } else if (core == POLY_EXP2_D2) {
+    c[0] = from_double(0.6602339719, POLY_F16);
+    c[1] = from_double(1.0 - to_double(c[0], POLY_F16), POLY_F16);
+  } else if (core == POLY_EXP2_D3) {
+    c[0] = from_double(0.6951461434, POLY_F16);
+    c[1] = from_double(0.2275643945, POLY_F16);
+    c[2] = from_double(0.0771190897, POLY_F16);
+  }
+}
+
+static int exp2_call(int core, const float *x, float *y, int64_t n, poly_stream_t stream) {
+  if (core < POLY_EXP2_D1 || core > POLY_EXP2_MUFU || n < 0) return POLY_EINVAL;
+  if (n == 0) return POLY_OK;
+  if (x == nullptr || y == nullptr) return POLY_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return POLY_EINVAL;
+  Span si[1] = {{reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + (uintptr_t)n * 4}};
+  Span so[1] = {{reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + (uintptr_t)n * 4}};
+  if (!aliasing_ok(si, 1, so, 1)) return POLY_EINVAL;
+  const int vec = ((reinterpret_cast<uintptr_t>(x) ^ reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+  uint16_t c[3];
+  exp2_constants(core, c);
+  return cuda_status(launch_exp2(core, x, y, n, vec, c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int poly_exp2(int core, const float *x, float *y, int64_t n, poly_stream_t stream) {
+  if (core == POLY_EXP2_MUFU) return POLY_EINVAL;   // the control has its own entry point
+  return exp2_call(core, x, y, n, stream);
+}
+
+int poly_ctrl_exp2(const float *x, float *y, int64_t n, poly_stream_t stream) {
+  return exp2_call(POLY_EXP2_MUFU, x, y, n, stream);
+}
+
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c, void *out,
                      int64_t n, poly_stream_t stream) {
   if (op < POLY_DIAG_FMA || op > POLY_DIAG_GT || !valid_dtype(dtype) || n < 0)

@@ -61,6 +61,11 @@ cudaError_t launch_softcap(int bwd, int dtype, int degree, const Streams &s, con
                            const DevProg &p, uint16_t alpha, uint16_t inv_alpha,
                            cudaStream_t stream);
 
+// exp2 with a polynomial fractional core (core = POLY_EXP2_*; c = up to
+// three FP16 constants of the core).
+cudaError_t launch_exp2(int core, const float *x, float *y, int64_t n, int vec,
+                        const uint16_t *c, cudaStream_t stream);
+
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
                         cudaStream_t stream);

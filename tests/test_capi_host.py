@@ -210,3 +210,15 @@ def test_softcap_rejects_bad_alpha(L):
     assert L.poly_softcap_fwd(0, 30.0, None, None, 0, s) == B.POLY_OK
     assert L.poly_softcap_fwd(0, 30.0, FAKE, FAKE + 2, 8, s) == B.POLY_EINVAL
     assert L.poly_softcap_bwd(1, 30.0, FAKE, None, FAKE + 8192, 8, s) == B.POLY_EINVAL
+
+
+def test_exp2_rejects_bad_arguments(L):
+    s = None
+    assert L.poly_exp2(9, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    assert L.poly_exp2(4, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL      # control has its own call
+    assert L.poly_exp2(1, FAKE + 2, FAKE + 4096, 8, s) == B.POLY_EINVAL  # not 4-byte aligned
+    assert L.poly_exp2(1, FAKE, FAKE + 4, 8, s) == B.POLY_EINVAL         # partial overlap
+    assert L.poly_exp2(1, None, FAKE, 8, s) == B.POLY_EINVAL
+    assert L.poly_exp2(1, FAKE, FAKE, -1, s) == B.POLY_EINVAL
+    assert L.poly_exp2(1, None, None, 0, s) == B.POLY_OK
+    assert L.poly_ctrl_exp2(FAKE + 2, FAKE + 4096, 8, s) == B.POLY_EINVAL

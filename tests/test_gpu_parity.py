@@ -532,3 +532,44 @@ def test_derived_program_backward_exhaustive(dt, fn, D):
             assert np.array_equal(from_dev(out), softcap_backward(od, 30.0, x, dy))
     finally:
         B.poly_reset_programs()
+
+
+# ------------------------------------------------------------------- exp2
+
+def _exp2_inputs():
+    rng = np.random.default_rng(41)
+    dense = rng.uniform(-130, 130, 1 << 22).astype(np.float32)
+    halfs = tf.all_patterns().view(np.float16).astype(np.float32)           # every FP16 value
+    grid = (np.arange(-260, 261) / 2).astype(np.float32)                    # integers, halves
+    near = np.nextafter(grid, np.float32(np.inf)).astype(np.float32)
+    near2 = np.nextafter(grid, np.float32(-np.inf)).astype(np.float32)
+    sp = np.array([np.nan, np.inf, -np.inf, 0.0, -0.0, 1e-30, -1e-30, 127.999, 128.0, 1e30,
+                   -1e30, -126.0, -126.5, -125.999], dtype=np.float32)
+    return np.concatenate([dense, halfs, grid, near, near2, sp])
+
+
+@pytest.mark.parametrize("core", [B.POLY_EXP2_D1, B.POLY_EXP2_PWL2, B.POLY_EXP2_D2,
+                                  B.POLY_EXP2_D3])
+def test_exp2_cores_bit_exact(core):
+    from oracle import exp2 as e2
+    x = _exp2_inputs()
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.empty_like(xd)
+    B.poly_exp2(core, xd, y)
+    got = y.cpu().numpy().view(np.uint32)
+    want = e2.exp2_replay(e2.VARIANTS[core], x)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(x[i]), hex(got[i]), hex(want[i])) for i in bad[:6]]
+    # unaligned start and odd length: scalar head and tail
+    y2 = torch.empty(x.size + 3, dtype=torch.float32, device=DEV)
+    B.poly_exp2(core, xd[1:], y2[2:2 + x.size - 1], x.size - 1)
+    assert np.array_equal(y2[2:2 + x.size - 1].cpu().numpy().view(np.uint32), want[1:])
+
+
+def test_exp2_mufu_control_accuracy():
+    x = np.random.default_rng(43).uniform(-120, 120, 1 << 20).astype(np.float32)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.empty_like(xd)
+    B.poly_ctrl_exp2(xd, y)
+    rel = np.abs(y.cpu().numpy().astype(np.float64) / np.exp2(x.astype(np.float64)) - 1)
+    assert rel.max() < 2e-6
