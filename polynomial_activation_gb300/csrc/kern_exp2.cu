@@ -68,8 +68,8 @@ __device__ __forceinline__ float2 exp2_pair(float x0, float x1, const Exp2Params
   }
 }
 
-// One-pass grid over n floats: 16-byte chunks (4 floats) when x and y share
-// their address modulo 16, scalar head and tail otherwise.
+// One-pass grid over n floats: two 16-byte chunks (8 floats) per thread when
+// x and y share their address modulo 16, scalar head and tail otherwise.
 template <int CORE>
 __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restrict__ x,
                                                            float *__restrict__ y, int64_t n,
@@ -85,16 +85,29 @@ __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restr
   const int64_t gid = (int64_t)blockIdx.x * kExp2Threads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kExp2Threads;
 #pragma unroll 1
-  for (int64_t i = gid; i < nvec; i += stride) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(x + head + (i << 2)));
-    const float2 a = exp2_pair<CORE>(v.x, v.y, p), b = exp2_pair<CORE>(v.z, v.w, p);
-    asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :
-                 : "l"(y + head + (i << 2)), "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y)
-                 : "memory");
+  for (int64_t base = (int64_t)blockIdx.x * (2 * kExp2Threads) + threadIdx.x; base < nvec;
+       base += (int64_t)gridDim.x * (2 * kExp2Threads)) {
+    float4 v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t i = base + u * kExp2Threads;
+      if (i < nvec)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[u].x), "=f"(v[u].y), "=f"(v[u].z), "=f"(v[u].w)
+                     : "l"(x + head + (i << 2)));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t i = base + u * kExp2Threads;
+      if (i < nvec) {
+        const float2 a = exp2_pair<CORE>(v[u].x, v[u].y, p);
+        const float2 b = exp2_pair<CORE>(v[u].z, v[u].w, p);
+        asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :
+                     : "l"(y + head + (i << 2)), "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y)
+                     : "memory");
+      }
+    }
   }
   const int64_t ntail = n - body_end;
 #pragma unroll 1
@@ -108,7 +121,7 @@ __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restr
 template <int CORE>
 static cudaError_t go(const float *x, float *y, int64_t n, int vec, const Exp2Params &p,
                       cudaStream_t st) {
-  const int64_t per_block = (int64_t)kExp2Threads * (vec ? 4 : 1);
+  const int64_t per_block = (int64_t)kExp2Threads * (vec ? 8 : 1);
   int64_t blocks = (n + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
   if (blocks < 1) blocks = 1;
