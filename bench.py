@@ -368,6 +368,7 @@ def main():
     if not args.no_extras:
         result["softcap"] = softcap_extras(x, dy, outs[0], n, stream, peak)
         result["exp2"] = exp2_extras(dev, stream, peak)
+        result["rope"] = rope_extras(dev, stream, peak)
         result["swiglu"] = swiglu_extras(args, dev, stream, peak)
         result["l2_resident"] = l2_extras(dev, stream)
 
@@ -448,6 +449,38 @@ def exp2_extras(dev, stream, peak, n=1 << 27):
                       ("mufu_ex2", lambda: B.poly_ctrl_exp2(x, y))]:
         ms = _time(fn, stream, 20)
         res[label] = {"ms": ms, "gbs": 8 * n / ms / 1e6, "frac": 8 * n / ms / 1e6 / peak}
+    return res
+
+
+def rope_extras(dev, stream, peak, b=4, s=4096, hq=32, hkv=8, d=128):
+    """Fused RoPE (Appendix B.2): FP16 Q [B, S, Hq, D] and K [B, S, Hkv, D] to
+    the transposed layouts, with polynomial, MUFU and cached-table sine /
+    cosine sharing the rotation and memory schedule."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    g = torch.Generator(device=dev).manual_seed(0)
+    q = torch.randn((b, s, hq, d), generator=g, device=dev).to(torch.float16)
+    k = torch.randn((b, s, hkv, d), generator=g, device=dev).to(torch.float16)
+    qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=dev)
+    ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=dev)
+    delta = torch.from_numpy(B.poly_rope_turn_increments(d).view(np.int32)).to(dev)
+    # cached tables [S, D/2] from the polynomial variant's own values
+    eye = torch.zeros((1, s, 1, d), dtype=torch.float16, device=dev)
+    eye[..., 0::2] = 1.0
+    cs_o = torch.empty((1, 1, s, d), dtype=torch.float16, device=dev)
+    B.poly_rope_fwd(B.POLY_ROPE_POLY, eye, None, cs_o, None, delta, batch=1, seq=s, hq=1, hkv=0,
+                    head_dim=d)
+    cos_t, sin_t = cs_o[0, 0, :, 0::2].contiguous(), cs_o[0, 0, :, 1::2].contiguous()
+    nbytes = 2 * 2 * (q.numel() + k.numel())
+    res = {"config": f"FP16 B={b} S={s} Hq={hq} Hkv={hkv} D={d}, base 10000"}
+    for label, fn in [
+        ("poly_fwd", lambda: B.poly_rope_fwd(B.POLY_ROPE_POLY, q, k, qo, ko, delta)),
+        ("mufu_fwd", lambda: B.poly_rope_fwd(B.POLY_ROPE_MUFU, q, k, qo, ko, delta)),
+        ("table_fwd", lambda: B.poly_rope_fwd(B.POLY_ROPE_TABLE, q, k, qo, ko, None, cos_t, sin_t)),
+        ("poly_bwd", lambda: B.poly_rope_bwd(B.POLY_ROPE_POLY, qo, ko, q, k, delta)),
+    ]:
+        ms = _time(fn, stream, 20)
+        res[label] = {"us": ms * 1e3, "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak}
     return res
 
 

@@ -267,6 +267,47 @@ enum { POLY_EXP2_D1 = 0, POLY_EXP2_PWL2 = 1, POLY_EXP2_D2 = 2, POLY_EXP2_D3 = 3,
        POLY_EXP2_MUFU = 4 };
 int poly_exp2(int core, const float *x, float *y, int64_t n, poly_stream_t stream);
 
+/* ---- fused RoPE with paired polynomial sine / cosine (Appendix B.2) -------
+ * FP16 only.  Frequencies omega_i = base^(-2i/D), i < D/2, act on the
+ * interleaved pairs (x_2i, x_2i+1) as complex numbers.  The caller passes
+ * delta: a DEVICE array of D/2 Q0.32 turn increments
+ * Delta_i = round(omega_i 2^32 / 2 pi) (poly_rope_turn_increments fills one
+ * on the host).  At position p = pos_offset + s the phase is
+ * (p Delta_i) mod 2^32; as a signed value it is a Q31 half-turn coordinate,
+ * folded into [-1/2, 1/2] half-turns (sin(pi u) = sin(pi (+-1 - u)), cosine
+ * negated), then truncated to the signed Q15 coordinate q.
+ * Variants:
+ *   POLY_ROPE_POLY   u = FP16(q) 2^-15, w = u u, sin = fma(fma(s5, w, s3), w, s1) u,
+ *                    cos = fma(fma(fma(c6, w, c4), w, c2), w, 1) (packed FP16,
+ *                    one rounding per op; D5 sine and D6 cosine fitted as in
+ *                    eq. 7-8 with the end value at u = 1/2 exact)
+ *   POLY_ROPE_MUFU   sin.approx / cos.approx of pi u in FP32, rounded to FP16
+ *   POLY_ROPE_TABLE  cos_tab / sin_tab: DEVICE FP16 [S, D/2]; row s serves
+ *                    position pos_offset + s (delta may be NULL)
+ * Rotation of (a, b) by (c, s): out = (fma(a, c, -(b s)), fma(b, c, a s)).
+ * Forward: q [B, S, Hq, D], k [B, S, Hkv, D] -> q_out [B, Hq, S, D],
+ *          k_out [B, Hkv, S, D].
+ * Backward: the same call shape with gradients in [B, H, S, D] in and
+ *          [B, S, H, D] out, rotated by -theta.
+ * Contiguous tensors; every pointer 16-byte aligned; head_dim a multiple of 8;
+ * hq or hkv may be 0 (its pointers then unused); outputs may not overlap any
+ * input; pos_offset + seq <= 2^32.  POLY_EINVAL otherwise. */
+enum { POLY_ROPE_POLY = 0, POLY_ROPE_MUFU = 1, POLY_ROPE_TABLE = 2 };
+int poly_rope_fwd(int variant, const void *q, const void *k, void *q_out, void *k_out,
+                  const uint32_t *delta, const void *cos_tab, const void *sin_tab,
+                  int64_t batch, int64_t seq, int64_t hq, int64_t hkv, int64_t head_dim,
+                  int64_t pos_offset, poly_stream_t stream);
+int poly_rope_bwd(int variant, const void *dq, const void *dk, void *dq_out, void *dk_out,
+                  const uint32_t *delta, const void *cos_tab, const void *sin_tab,
+                  int64_t batch, int64_t seq, int64_t hq, int64_t hkv, int64_t head_dim,
+                  int64_t pos_offset, poly_stream_t stream);
+/* Host: out[i] = round(base^(-2i/head_dim) 2^32 / 2 pi), i < head_dim / 2.
+ * POLY_EINVAL unless head_dim is positive and even, base > 1, out non-NULL. */
+int poly_rope_turn_increments(int head_dim, double base, uint32_t *out);
+/* Host: the FP16 bit patterns of the sine (s1, s3, s5) and cosine
+ * (c2, c4, c6) coefficients the POLY_ROPE_POLY variant uses. */
+int poly_rope_programs(uint16_t *sin_coef, uint16_t *cos_coef);
+
 /* ---- MUFU-native controls (same signatures and memory schedule) ----------
  * FP32 math on the special-function unit: sigmoid = rcp.approx(1 +
  * ex2.approx(-x log2 e)); tanh = tanh.approx; SiLU = the overflow-safe form

@@ -31,8 +31,10 @@ EXPORTS = [
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
     "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
     "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd", "poly_exp2",
-    "poly_ctrl_exp2",
+    "poly_ctrl_exp2", "poly_rope_fwd", "poly_rope_bwd", "poly_rope_turn_increments",
+    "poly_rope_programs",
 ]
+POLY_ROPE_POLY, POLY_ROPE_MUFU, POLY_ROPE_TABLE = 0, 1, 2
 POLY_EXP2_D1, POLY_EXP2_PWL2, POLY_EXP2_D2, POLY_EXP2_D3 = 0, 1, 2, 3
 POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID = 0, 1
 POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
@@ -90,6 +92,11 @@ def lib():
     L.poly_set_swiglu_variant.argtypes = [_i]
     L.poly_derive_program.argtypes = [ctypes.POINTER(PolyProgram), ctypes.POINTER(PolyProgram)]
     L.poly_exp2.argtypes = [_i, _p, _p, _i64, _p]
+    for name in ("poly_rope_fwd", "poly_rope_bwd"):
+        getattr(L, name).argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64,
+                                     _i64, _i64, _p]
+    L.poly_rope_turn_increments.argtypes = [_i, ctypes.c_double, _p]
+    L.poly_rope_programs.argtypes = [_p, _p]
     L.poly_ctrl_exp2.argtypes = [_p, _p, _i64, _p]
     L.poly_softcap_fwd.argtypes = [_i, ctypes.c_double, _p, _p, _i64, _p]
     L.poly_softcap_bwd.argtypes = [_i, ctypes.c_double, _p, _p, _p, _i64, _p]
@@ -320,3 +327,47 @@ def poly_exp2(core, x, y, n=None, stream=None):
 def poly_ctrl_exp2(x, y, n=None, stream=None):
     n = x.numel() if n is None else n
     _check(lib().poly_ctrl_exp2(_ptr(x), _ptr(y), n, _stream(stream)), "poly_ctrl_exp2")
+
+
+def poly_rope_turn_increments(head_dim, base=10000.0):
+    """Host array of the D/2 Q0.32 turn increments (numpy uint32)."""
+    import numpy as np
+    out = np.zeros(head_dim // 2, dtype=np.uint32)
+    _check(lib().poly_rope_turn_increments(head_dim, float(base), out.ctypes.data),
+           "poly_rope_turn_increments")
+    return out
+
+
+def poly_rope_programs():
+    s = (ctypes.c_uint16 * 3)()
+    c = (ctypes.c_uint16 * 3)()
+    _check(lib().poly_rope_programs(ctypes.cast(s, ctypes.c_void_p), ctypes.cast(c, ctypes.c_void_p)),
+           "poly_rope_programs")
+    return list(s), list(c)
+
+
+def _rope(fn, name, variant, q, k, q_out, k_out, delta, cos_tab, sin_tab, shape,
+          pos_offset, stream):
+    batch, seq, hq, hkv, head_dim = shape
+    _check(fn(variant, _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(delta), _ptr(cos_tab),
+              _ptr(sin_tab), batch, seq, hq, hkv, head_dim, pos_offset, _stream(stream)), name)
+
+
+def poly_rope_fwd(variant, q, k, q_out, k_out, delta, cos_tab=None, sin_tab=None, batch=None,
+                  seq=None, hq=None, hkv=None, head_dim=None, pos_offset=0, stream=None):
+    """q [B, S, Hq, D], k [B, S, Hkv, D] -> q_out [B, Hq, S, D], k_out [B, Hkv, S, D]."""
+    shape = (batch if batch is not None else q.shape[0], seq if seq is not None else q.shape[1],
+             hq if hq is not None else q.shape[2], hkv if hkv is not None else k.shape[2],
+             head_dim if head_dim is not None else q.shape[3])
+    _rope(lib().poly_rope_fwd, "poly_rope_fwd", variant, q, k, q_out, k_out, delta, cos_tab,
+          sin_tab, shape, pos_offset, stream)
+
+
+def poly_rope_bwd(variant, dq, dk, dq_out, dk_out, delta, cos_tab=None, sin_tab=None, batch=None,
+                  seq=None, hq=None, hkv=None, head_dim=None, pos_offset=0, stream=None):
+    """dq [B, Hq, S, D], dk [B, Hkv, S, D] -> dq_out [B, S, Hq, D], dk_out [B, S, Hkv, D]."""
+    shape = (batch if batch is not None else dq.shape[0], seq if seq is not None else dq.shape[2],
+             hq if hq is not None else dq.shape[1], hkv if hkv is not None else dk.shape[1],
+             head_dim if head_dim is not None else dq.shape[3])
+    _rope(lib().poly_rope_bwd, "poly_rope_bwd", variant, dq, dk, dq_out, dk_out, delta, cos_tab,
+          sin_tab, shape, pos_offset, stream)

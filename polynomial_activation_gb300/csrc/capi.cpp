@@ -526,6 +526,97 @@ int poly_ctrl_exp2(const float *x, float *y, int64_t n, poly_stream_t stream) {
   return exp2_call(POLY_EXP2_MUFU, x, y, n, stream);
 }
 
+namespace {
+std::once_flag g_sincos_once;
+uint16_t g_sin16[3], g_cos16[3];
+void sincos_init() { std::call_once(g_sincos_once, [] { fit_sincos(g_sin16, g_cos16); }); }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+int poly_rope_programs(uint16_t *sin_coef, uint16_t *cos_coef) {
+  if (sin_coef == nullptr || cos_coef == nullptr) return POLY_EINVAL;
+  sincos_init();
+  for (int j = 0; j < 3; ++j) {
+    sin_coef[j] = g_sin16[j];
+    cos_coef[j] = g_cos16[j];
+  }
+  return POLY_OK;
+}
+
+int poly_rope_turn_increments(int head_dim, double base, uint32_t *out) {
+  if (head_dim <= 0 || (head_dim & 1) || !(base > 1.0) || !std::isfinite(base) || !out)
+    return POLY_EINVAL;
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double omega = std::pow(base, -2.0 * i / head_dim);
+    out[i] = (uint32_t)std::llround(omega * 4294967296.0 / (2.0 * M_PI));
+  }
+  return POLY_OK;
+}
+
+static int rope_call(int inv, int variant, const void *q, const void *k, void *q_out,
+                     void *k_out, const uint32_t *delta, const void *cos_tab,
+                     const void *sin_tab, int64_t batch, int64_t seq, int64_t hq, int64_t hkv,
+                     int64_t head_dim, int64_t pos_offset, poly_stream_t stream) {
+  if (variant < POLY_ROPE_POLY || variant > POLY_ROPE_TABLE) return POLY_EINVAL;
+  if (batch < 0 || seq < 0 || hq < 0 || hkv < 0 || head_dim <= 0 || (head_dim & 7) ||
+      pos_offset < 0 || pos_offset + seq > (int64_t(1) << 32))
+    return POLY_EINVAL;
+  if (batch == 0 || seq == 0 || hq + hkv == 0) return POLY_OK;
+  Span si[4], so[2];
+  int nin = 0, nout = 0;
+  if (hq > 0) {
+    if (!q || !q_out || !aligned16(q) || !aligned16(q_out)) return POLY_EINVAL;
+    si[nin++] = span_flat(q, batch * seq * hq * head_dim);
+    so[nout++] = span_flat(q_out, batch * seq * hq * head_dim);
+  }
+  if (hkv > 0) {
+    if (!k || !k_out || !aligned16(k) || !aligned16(k_out)) return POLY_EINVAL;
+    si[nin++] = span_flat(k, batch * seq * hkv * head_dim);
+    so[nout++] = span_flat(k_out, batch * seq * hkv * head_dim);
+  }
+  if (variant == POLY_ROPE_TABLE) {
+    if (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)) return POLY_EINVAL;
+    si[nin++] = span_flat(cos_tab, seq * head_dim / 2);
+    si[nin++] = span_flat(sin_tab, seq * head_dim / 2);
+  } else if (!delta || !aligned16(delta)) {
+    return POLY_EINVAL;
+  }
+  // transposed layouts: an output may not touch any input, nor the other output
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(so[o], si[i])) return POLY_EINVAL;
+    for (int o2 = o + 1; o2 < nout; ++o2)
+      if (overlaps(so[o], so[o2])) return POLY_EINVAL;
+  }
+  sincos_init();
+  RopeConsts kc;
+  for (int j = 0; j < 3; ++j) {
+    kc.s[j] = (uint32_t)g_sin16[j] * 0x00010001u;
+    kc.c[j] = (uint32_t)g_cos16[j] * 0x00010001u;
+  }
+  RopeArgs a{static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+             static_cast<uint16_t *>(q_out), static_cast<uint16_t *>(k_out), delta,
+             static_cast<const uint16_t *>(cos_tab), static_cast<const uint16_t *>(sin_tab),
+             batch, seq, hq, hkv, head_dim, pos_offset};
+  return cuda_status(launch_rope(variant, inv, a, kc, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int poly_rope_fwd(int variant, const void *q, const void *k, void *q_out, void *k_out,
+                  const uint32_t *delta, const void *cos_tab, const void *sin_tab,
+                  int64_t batch, int64_t seq, int64_t hq, int64_t hkv, int64_t head_dim,
+                  int64_t pos_offset, poly_stream_t stream) {
+  return rope_call(0, variant, q, k, q_out, k_out, delta, cos_tab, sin_tab, batch, seq, hq, hkv,
+                   head_dim, pos_offset, stream);
+}
+
+int poly_rope_bwd(int variant, const void *dq, const void *dk, void *dq_out, void *dk_out,
+                  const uint32_t *delta, const void *cos_tab, const void *sin_tab,
+                  int64_t batch, int64_t seq, int64_t hq, int64_t hkv, int64_t head_dim,
+                  int64_t pos_offset, poly_stream_t stream) {
+  return rope_call(1, variant, dq, dk, dq_out, dk_out, delta, cos_tab, sin_tab, batch, seq, hq,
+                   hkv, head_dim, pos_offset, stream);
+}
+
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c, void *out,
                      int64_t n, poly_stream_t stream) {
   if (op < POLY_DIAG_FMA || op > POLY_DIAG_GT || !valid_dtype(dtype) || n < 0)

@@ -305,6 +305,44 @@ int derive_program(const poly_program &f, poly_program *out) {
   return POLY_OK;
 }
 
+// Paired sine / cosine programs for RoPE (Appendix B.2: packed FP16 D5 sine
+// and D6 cosine sharing the squared input), on the folded half-turn
+// coordinate u in [0, 1/2]: sin(pi u) ~ s1 u + s3 u^3 + s5 u^5 and
+// cos(pi u) ~ 1 + c2 u^2 + c4 u^4 + c6 u^6, least squares on 2,000 Chebyshev
+// nodes with the end value exact (sin = 1, cos = 0 at u = 1/2), the last
+// coefficient eliminated through that constraint (the eq. 7-8 construction).
+static void constrained_fit3(bool sine, double *coef) {
+  const int m = 2000;
+  const double xe = 0.5;
+  const int p[3] = {sine ? 1 : 2, sine ? 3 : 4, sine ? 5 : 6};
+  const double fixed_end = sine ? 0.0 : 1.0, end_value = sine ? 1.0 : 0.0;
+  const double r = end_value - fixed_end;
+  const double pe = std::pow(xe, p[2]);
+  std::vector<double> A((size_t)m * 2), y(m);
+  for (int i = 0; i < m; ++i) {
+    const double x = 0.5 * xe * (1.0 + std::cos((2.0 * i + 1.0) * M_PI / (2.0 * m)));
+    const double f = sine ? std::sin(M_PI * x) : std::cos(M_PI * x) - 1.0;
+    const double xl = std::pow(x, p[2]);
+    for (int k = 0; k < 2; ++k) A[(size_t)k * m + i] = std::pow(x, p[k]) - xl * (std::pow(xe, p[k]) / pe);
+    y[i] = f - xl * (r / pe);
+  }
+  double a[2];
+  householder_lstsq(A, m, 2, y, a);
+  coef[0] = a[0];
+  coef[1] = a[1];
+  coef[2] = (r - a[0] * std::pow(xe, p[0]) - a[1] * std::pow(xe, p[1])) / pe;
+}
+
+void fit_sincos(uint16_t *s, uint16_t *c) {
+  double sv[3], cv[3];
+  constrained_fit3(true, sv);
+  constrained_fit3(false, cv);
+  for (int j = 0; j < 3; ++j) {
+    s[j] = from_double(sv[j], POLY_F16);
+    c[j] = from_double(cv[j], POLY_F16);
+  }
+}
+
 int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
                 poly_program *out) {
   const int form = form_of_fn(fn, dir);

@@ -17,5 +17,7 @@ void fit_coefficients(int fn, int dir, int degree, double li, int n_nodes, doubl
 int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
                 poly_program *out);
 int derive_program(const poly_program &fwd, poly_program *out);
+// FP16 RoPE programs: s = (s1, s3, s5), c = (c2, c4, c6).
+void fit_sincos(uint16_t *s, uint16_t *c);
 
 }  // namespace polyact

@@ -66,6 +66,21 @@ cudaError_t launch_softcap(int bwd, int dtype, int degree, const Streams &s, con
 cudaError_t launch_exp2(int core, const float *x, float *y, int64_t n, int vec,
                         const uint16_t *c, cudaStream_t stream);
 
+// Fused RoPE (FP16): inputs / outputs in [B, S, H, D] or [B, H, S, D] order.
+struct RopeArgs {
+  const uint16_t *in_q, *in_k;
+  uint16_t *out_q, *out_k;
+  const uint32_t *delta;                 // Q0.32 turn increment per frequency
+  const uint16_t *cos_tab, *sin_tab;     // table variant: [S, D/2] FP16
+  int64_t batch, seq, hq, hkv, head_dim, pos_offset;
+};
+// FP16 sine (s1, s3, s5) and cosine (c2, c4, c6) coefficients, duplicated pairs.
+struct RopeConsts {
+  uint32_t s[3], c[3];
+};
+cudaError_t launch_rope(int variant, int inv, const RopeArgs &a, const RopeConsts &k,
+                        cudaStream_t stream);
+
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
                         cudaStream_t stream);

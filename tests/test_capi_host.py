@@ -7,6 +7,7 @@ import json
 import os
 import re
 
+import numpy as np
 import pytest
 
 import golden_programs as gp
@@ -222,3 +223,35 @@ def test_exp2_rejects_bad_arguments(L):
     assert L.poly_exp2(1, FAKE, FAKE, -1, s) == B.POLY_EINVAL
     assert L.poly_exp2(1, None, None, 0, s) == B.POLY_OK
     assert L.poly_ctrl_exp2(FAKE + 2, FAKE + 4096, 8, s) == B.POLY_EINVAL
+
+
+def test_rope_programs_and_increments_match_oracle(L):
+    from oracle import rope
+    s, c = B.poly_rope_programs()
+    os_, oc = rope.sincos_coefficients()
+    assert tuple(s) == os_ and tuple(c) == oc
+    for D, base in [(128, 10000.0), (64, 500000.0), (8, 10000.0)]:
+        assert np.array_equal(B.poly_rope_turn_increments(D, base), rope.turn_increments(D, base))
+    out = np.zeros(4, dtype=np.uint32)
+    assert L.poly_rope_turn_increments(7, 10000.0, out.ctypes.data) == B.POLY_EINVAL
+    assert L.poly_rope_turn_increments(8, 1.0, out.ctypes.data) == B.POLY_EINVAL
+    assert L.poly_rope_programs(None, None) == B.POLY_EINVAL
+
+
+def test_rope_rejects_bad_arguments(L):
+    s = None
+    args = lambda **kw: [kw.get("variant", 0), kw.get("q", FAKE), kw.get("k", FAKE + 0x100000),
+                         kw.get("qo", FAKE + 0x200000), kw.get("ko", FAKE + 0x300000),
+                         kw.get("delta", FAKE + 0x400000), None, None,
+                         kw.get("b", 1), kw.get("s", 4), kw.get("hq", 2), kw.get("hkv", 1),
+                         kw.get("d", 16), kw.get("pos", 0), s]
+    assert L.poly_rope_fwd(*args(variant=3)) == B.POLY_EINVAL
+    assert L.poly_rope_fwd(*args(d=12)) == B.POLY_EINVAL               # not a multiple of 8
+    assert L.poly_rope_fwd(*args(q=FAKE + 8)) == B.POLY_EINVAL         # not 16-byte aligned
+    assert L.poly_rope_fwd(*args(delta=None)) == B.POLY_EINVAL
+    assert L.poly_rope_fwd(*args(qo=FAKE + 64)) == B.POLY_EINVAL       # output overlaps input
+    assert L.poly_rope_fwd(*args(pos=(1 << 32) - 2)) == B.POLY_EINVAL  # positions past 2^32
+    assert L.poly_rope_fwd(*args(variant=2)) == B.POLY_EINVAL          # table variant, no tables
+    assert L.poly_rope_bwd(*args(b=-1)) == B.POLY_EINVAL
+    assert L.poly_rope_fwd(*args(b=0)) == B.POLY_OK
+    assert L.poly_rope_fwd(*args(hq=0, hkv=0)) == B.POLY_OK

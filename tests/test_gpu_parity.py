@@ -574,3 +574,93 @@ def test_exp2_mufu_control_accuracy():
     B.poly_ctrl_exp2(xd, y)
     rel = np.abs(y.cpu().numpy().astype(np.float64) / np.exp2(x.astype(np.float64)) - 1)
     assert rel.max() < 2e-6
+
+
+# --------------------------------------------------------------------- RoPE
+
+def _rope_case(rng, b, s, hq, hkv, d):
+    q = tf.from_f64(rng.normal(0, 1, (b, s, hq, d)), "f16")
+    k = tf.from_f64(rng.normal(0, 1, (b, s, hkv, d)), "f16")
+    return q, k
+
+
+@pytest.mark.parametrize("shape,pos", [((2, 37, 4, 2, 16), 0), ((1, 300, 3, 1, 128), 0),
+                                       ((3, 5, 2, 0, 8), 123456), ((1, 64, 0, 2, 64), (1 << 32) - 64),
+                                       ((2, 129, 8, 8, 128), 7)])
+def test_rope_poly_bit_exact(shape, pos):
+    from oracle import rope
+    b, s, hq, hkv, d = shape
+    rng = np.random.default_rng(sum(shape))
+    q, k = _rope_case(rng, b, s, hq, hkv, d)
+    delta = rope.turn_increments(d)
+    dd = torch.from_numpy(delta.view(np.int32)).to(DEV)
+    qd, kd = to_dev(q, 0), to_dev(k, 0)
+    qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=DEV)
+    ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=DEV)
+    B.poly_rope_fwd(B.POLY_ROPE_POLY, qd, kd, qo, ko, dd, batch=b, seq=s, hq=hq, hkv=hkv,
+                    head_dim=d, pos_offset=pos)
+    wq, wk = rope.rope_forward(q, k, delta, pos)
+    assert np.array_equal(from_dev(qo).reshape(wq.shape), wq)
+    assert np.array_equal(from_dev(ko).reshape(wk.shape), wk)
+    # backward: gradients in [B, H, S, D] -> [B, S, H, D], rotated by -theta
+    gq = torch.empty((b, s, hq, d), dtype=torch.float16, device=DEV)
+    gk = torch.empty((b, s, hkv, d), dtype=torch.float16, device=DEV)
+    B.poly_rope_bwd(B.POLY_ROPE_POLY, qo, ko, gq, gk, dd, batch=b, seq=s, hq=hq, hkv=hkv,
+                    head_dim=d, pos_offset=pos)
+    bq, bk = rope.rope_backward(wq, wk, delta, pos)
+    assert np.array_equal(from_dev(gq).reshape(bq.shape), bq)
+    assert np.array_equal(from_dev(gk).reshape(bk.shape), bk)
+    # the cached-table variant, given the oracle's tables, applies the same rotation
+    cs, sn = rope.tables(s, delta, pos)
+    ct = torch.from_numpy(cs.view(np.int16)).to(DEV)
+    st = torch.from_numpy(sn.view(np.int16)).to(DEV)
+    qo2, ko2 = torch.empty_like(qo), torch.empty_like(ko)
+    B.poly_rope_fwd(B.POLY_ROPE_TABLE, qd, kd, qo2, ko2, None, ct, st, batch=b, seq=s, hq=hq,
+                    hkv=hkv, head_dim=d, pos_offset=pos)
+    assert torch.equal(qo2.view(torch.int16), qo.view(torch.int16))
+    assert torch.equal(ko2.view(torch.int16), ko.view(torch.int16))
+
+
+def test_rope_mufu_variant_accuracy():
+    from oracle import rope
+    b, s, hq, hkv, d = 1, 512, 4, 2, 128
+    rng = np.random.default_rng(5)
+    q, k = _rope_case(rng, b, s, hq, hkv, d)
+    dd = torch.from_numpy(rope.turn_increments(d).view(np.int32)).to(DEV)
+    qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=DEV)
+    ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=DEV)
+    B.poly_rope_fwd(B.POLY_ROPE_MUFU, to_dev(q, 0), to_dev(k, 0), qo, ko, dd, batch=b, seq=s,
+                    hq=hq, hkv=hkv, head_dim=d)
+    qv = tf.decode(q, "f16")
+    z = qv[..., 0::2] + 1j * qv[..., 1::2]
+    omega = 10000.0 ** (-2.0 * np.arange(d // 2) / d)
+    zr = z * np.exp(1j * np.arange(s)[None, :, None, None] * omega)
+    want = np.empty_like(qv)
+    want[..., 0::2], want[..., 1::2] = zr.real, zr.imag
+    got = tf.decode(from_dev(qo).reshape(b, hq, s, d), "f16").transpose(0, 2, 1, 3)
+    assert np.max(np.abs(got - want)) < 2e-2
+
+
+def test_rope_full_size_sampled():
+    """B = 4, S = 4096, Hq = 32, Hkv = 8, D = 128 (the paper's GQA geometry at
+    batch 4): sampled rows of every output head."""
+    from oracle import rope
+    b, s, hq, hkv, d = 4, 4096, 32, 8, 128
+    rng = np.random.default_rng(11)
+    qd = torch.randn((b, s, hq, d), generator=torch.Generator(device=DEV).manual_seed(1),
+                     device=DEV, dtype=torch.float32).to(torch.float16)
+    kd = torch.randn((b, s, hkv, d), generator=torch.Generator(device=DEV).manual_seed(2),
+                     device=DEV, dtype=torch.float32).to(torch.float16)
+    delta = rope.turn_increments(d)
+    dd = torch.from_numpy(delta.view(np.int32)).to(DEV)
+    qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=DEV)
+    ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=DEV)
+    B.poly_rope_fwd(B.POLY_ROPE_POLY, qd, kd, qo, ko, dd)
+    cs, sn = rope.tables(s, delta)
+    for _ in range(64):
+        bb, ss = int(rng.integers(0, b)), int(rng.integers(0, s))
+        xq = from_dev(qd[bb, ss])                           # [Hq, D]
+        want = rope.rotate(xq, cs[ss][None, :], sn[ss][None, :])
+        assert np.array_equal(from_dev(qo[bb, :, ss, :]), want)
+        xk = from_dev(kd[bb, ss])
+        assert np.array_equal(from_dev(ko[bb, :, ss, :]), rope.rotate(xk, cs[ss][None, :], sn[ss][None, :]))
