@@ -5,8 +5,9 @@
 // rotated tensors transposed to [B, Hq, S, D] and [B, Hkv, S, D]; backward
 // reads gradients in the transposed layout, rotates by -theta and writes
 // [B, S, H, D].  One thread owns four frequencies (a 16-byte chunk of a
-// head: four interleaved complex pairs) of one (batch, position): it forms
-// the four phases once and reuses the sine / cosine across every head.
+// head: four interleaved complex pairs) of one (batch, position) and up to
+// eight heads: it forms the four phases once and reuses the sine / cosine
+// across those heads.
 //
 // Phase: phi = (pos * Delta_i) mod 2^32 (Q0.32 turns); as a signed 32-bit
 // value it is a Q31 half-turn coordinate in [-1, 1); beyond +-1/2 it folds
@@ -30,6 +31,7 @@ namespace dev {
 
 constexpr int kRopeThreads = 256;
 constexpr int kHeadUnroll = 4;
+constexpr int kHeadsPerThread = 8;   // heads a thread rotates with one sine / cosine set
 
 __device__ __forceinline__ uint32_t swap_lanes(uint32_t x) { return __byte_perm(x, 0, 0x1032); }
 __device__ __forceinline__ uint32_t lane_lo2(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
@@ -108,13 +110,29 @@ __device__ __forceinline__ void st16(uint16_t *p, const uint4 &v) {
 template <int VARIANT, int INV>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeConsts k) {
   const int64_t groups = a.head_dim >> 3;                // chunks of 4 frequencies
-  const int64_t total = a.batch * a.seq * groups;
   const int64_t H = a.hq + a.hkv;
+  const int64_t hchunks = (H + kHeadsPerThread - 1) / kHeadsPerThread;
+  const int64_t total = a.batch * a.seq * hchunks * groups;
   for (int64_t t = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * kRopeThreads) {
-    const int64_t j = t % groups;
-    const int64_t bs = t / groups;
-    const int64_t b = bs / a.seq, s = bs - b * a.seq;
+    int64_t j, hc, b, s;
+    if (total <= 0xFFFFFFFFll) {   // 32-bit index arithmetic (the common case)
+      const uint32_t t32 = (uint32_t)t, g32 = (uint32_t)groups, h32 = (uint32_t)hchunks;
+      const uint32_t r = t32 / g32, bs = r / h32;
+      j = t32 - r * g32;
+      hc = r - bs * h32;
+      b = bs / (uint32_t)a.seq;
+      s = bs - (uint32_t)b * (uint32_t)a.seq;
+    } else {
+      j = t % groups;
+      const int64_t r = t / groups;
+      hc = r % hchunks;
+      const int64_t bs = r / hchunks;
+      b = bs / a.seq;
+      s = bs - b * a.seq;
+    }
+    const int64_t h_begin = hc * kHeadsPerThread;
+    const int64_t h_end = h_begin + kHeadsPerThread < H ? h_begin + kHeadsPerThread : H;
     // ---- four (cos, sin) pairs for frequencies 4j .. 4j+3
     uint32_t cA, sA, cB, sB;
     if constexpr (VARIANT == POLY_ROPE_TABLE) {
@@ -139,12 +157,13 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
     const uint32_t cc[4] = {lane_lo2(cA), lane_hi2(cA), lane_lo2(cB), lane_hi2(cB)};
     const uint32_t ss[4] = {lane_lo2(sA), lane_hi2(sA), lane_lo2(sB), lane_hi2(sB)};
     // ---- every head of this (batch, position): [B, S, H, D] <-> [B, H, S, D]
-    for (int64_t h0 = 0; h0 < H; h0 += kHeadUnroll) {
+#pragma unroll 1
+    for (int64_t h0 = h_begin; h0 < h_end; h0 += kHeadUnroll) {
       uint4 v[kHeadUnroll];
 #pragma unroll
       for (int u = 0; u < kHeadUnroll; ++u) {
         const int64_t h = h0 + u;
-        if (h < H) {
+        if (h < h_end) {
           const bool isq = h < a.hq;
           const int64_t hh = isq ? h : h - a.hq, nh = isq ? a.hq : a.hkv;
           const uint16_t *base = isq ? a.in_q : a.in_k;
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
 #pragma unroll
       for (int u = 0; u < kHeadUnroll; ++u) {
         const int64_t h = h0 + u;
-        if (h < H) {
+        if (h < h_end) {
           const bool isq = h < a.hq;
           const int64_t hh = isq ? h : h - a.hq, nh = isq ? a.hq : a.hkv;
           uint16_t *base = isq ? a.out_q : a.out_k;
@@ -174,7 +193,9 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
 
 template <int VARIANT>
 static cudaError_t rope_go(int inv, const RopeArgs &a, const RopeConsts &k, cudaStream_t st) {
-  const int64_t total = a.batch * a.seq * (a.head_dim >> 3);
+  const int64_t H = a.hq + a.hkv;
+  const int64_t total =
+      a.batch * a.seq * ((H + kHeadsPerThread - 1) / kHeadsPerThread) * (a.head_dim >> 3);
   int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
   if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
   if (blocks < 1) blocks = 1;
