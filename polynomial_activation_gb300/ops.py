@@ -54,3 +54,119 @@ def swiglu_bwd_ragged(g, u, dy, seg_off, dg=None, du=None, status=None):
     du = torch.empty_like(g) if du is None else du
     B.poly_swiglu_bwd_ragged(_dt(g), g, u, dy, dg, du, seg_off, status=status)
     return dg, du
+
+
+# ---- autograd: drop-in modules for training code --------------------------
+# Each forward saves its inputs and the backward recomputes the programs from
+# them (the paper's backward constructions evaluate from x, §4.2, §5.2.4), so
+# no activation tensor is kept.
+
+class PolyActivation(torch.autograd.Function):
+    """y = program_fwd(fn)(x); dx = dy * program_bwd(fn)(x)."""
+
+    @staticmethod
+    def forward(ctx, x, fn: str):
+        x = x.contiguous()
+        ctx.save_for_backward(x)
+        ctx.fn = fn
+        return act_fwd(fn, x)
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x,) = ctx.saved_tensors
+        return act_bwd(ctx.fn, x, dy.contiguous()), None
+
+
+def sigmoid(x):
+    return PolyActivation.apply(x, "sigmoid")
+
+
+def tanh(x):
+    return PolyActivation.apply(x, "tanh")
+
+
+def silu(x):
+    return PolyActivation.apply(x, "silu")
+
+
+def gelu(x):
+    return PolyActivation.apply(x, "gelu")
+
+
+class PolySwiGLU(torch.autograd.Function):
+    """y = SiLU(g) * u with the library's current SwiGLU rule."""
+
+    @staticmethod
+    def forward(ctx, g, u):
+        g, u = g.contiguous(), u.contiguous()
+        ctx.save_for_backward(g, u)
+        return swiglu_fwd(g, u)
+
+    @staticmethod
+    def backward(ctx, dy):
+        g, u = ctx.saved_tensors
+        return swiglu_bwd(g, u, dy.contiguous())
+
+
+def swiglu(g, u):
+    return PolySwiGLU.apply(g, u)
+
+
+class PolySoftcap(torch.autograd.Function):
+    """alpha * tanh(x / alpha) (attention-logit softcap)."""
+
+    @staticmethod
+    def forward(ctx, x, alpha: float):
+        x = x.contiguous()
+        ctx.save_for_backward(x)
+        ctx.alpha = alpha
+        y = torch.empty_like(x)
+        B.poly_softcap_fwd(_dt(x), alpha, x, y)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x,) = ctx.saved_tensors
+        dx = torch.empty_like(x)
+        B.poly_softcap_bwd(_dt(x), ctx.alpha, x, dy.contiguous(), dx)
+        return dx, None
+
+
+def softcap(x, alpha: float):
+    return PolySoftcap.apply(x, alpha)
+
+
+class PolyRoPE(torch.autograd.Function):
+    """q [B, S, Hq, D], k [B, S, Hkv, D] (FP16) -> rotated q [B, Hq, S, D],
+    k [B, Hkv, S, D] with polynomial sine / cosine."""
+
+    @staticmethod
+    def forward(ctx, q, k, delta, pos_offset: int):
+        q, k = q.contiguous(), k.contiguous()
+        b, s, hq, d = q.shape
+        hkv = k.shape[2]
+        qo = torch.empty((b, hq, s, d), dtype=q.dtype, device=q.device)
+        ko = torch.empty((b, hkv, s, d), dtype=k.dtype, device=k.device)
+        B.poly_rope_fwd(B.POLY_ROPE_POLY, q, k, qo, ko, delta, pos_offset=pos_offset)
+        ctx.save_for_backward(delta)
+        ctx.meta = (b, s, hq, hkv, d, pos_offset)
+        return qo, ko
+
+    @staticmethod
+    def backward(ctx, dqo, dko):
+        (delta,) = ctx.saved_tensors
+        b, s, hq, hkv, d, pos = ctx.meta
+        dqo = torch.zeros((b, hq, s, d), dtype=torch.float16, device=delta.device) \
+            if dqo is None else dqo.contiguous()
+        dko = torch.zeros((b, hkv, s, d), dtype=torch.float16, device=delta.device) \
+            if dko is None else dko.contiguous()
+        dq = torch.empty((b, s, hq, d), dtype=dqo.dtype, device=dqo.device)
+        dk = torch.empty((b, s, hkv, d), dtype=dko.dtype, device=dko.device)
+        B.poly_rope_bwd(B.POLY_ROPE_POLY, dqo, dko, dq, dk, delta, pos_offset=pos)
+        return dq, dk, None, None
+
+
+def rope(q, k, delta, pos_offset: int = 0):
+    """delta: device uint32/int32 tensor of D/2 turn increments
+    (``binding.poly_rope_turn_increments``)."""
+    return PolyRoPE.apply(q, k, delta, pos_offset)

@@ -664,3 +664,45 @@ def test_rope_full_size_sampled():
         assert np.array_equal(from_dev(qo[bb, :, ss, :]), want)
         xk = from_dev(kd[bb, ss])
         assert np.array_equal(from_dev(ko[bb, :, ss, :]), rope.rotate(xk, cs[ss][None, :], sn[ss][None, :]))
+
+
+# ------------------------------------------------------------------ autograd
+
+def test_autograd_wrappers_match_direct_calls():
+    """The torch.autograd wrappers return exactly what the C-ABI calls give."""
+    from polynomial_activation_gb300 import ops
+    from oracle import rope
+    rng = np.random.default_rng(77)
+    for dt in DTS:
+        x = to_dev(_rand_bits(rng, 10_000, FMT[dt]), dt).requires_grad_(True)
+        dy = to_dev(_rand_bits(rng, 10_000, FMT[dt]), dt)
+        for name, f in [("sigmoid", ops.sigmoid), ("tanh", ops.tanh), ("silu", ops.silu),
+                        ("gelu", ops.gelu)]:
+            x.grad = None
+            y = f(x)
+            y.backward(dy)
+            assert torch.equal(y.detach().view(torch.int16), ops.act_fwd(name, x.detach()).view(torch.int16))
+            assert torch.equal(x.grad.view(torch.int16), ops.act_bwd(name, x.detach(), dy).view(torch.int16))
+        g = to_dev(_rand_bits(rng, 64 * 256, FMT[dt]), dt).view(64, 256).requires_grad_(True)
+        u = to_dev(_rand_bits(rng, 64 * 256, FMT[dt]), dt).view(64, 256).requires_grad_(True)
+        dyy = to_dev(_rand_bits(rng, 64 * 256, FMT[dt]), dt).view(64, 256)
+        y = ops.swiglu(g, u)
+        y.backward(dyy)
+        dg, du = ops.swiglu_bwd(g.detach(), u.detach(), dyy)
+        assert torch.equal(g.grad.view(torch.int16), dg.view(torch.int16))
+        assert torch.equal(u.grad.view(torch.int16), du.view(torch.int16))
+        x.grad = None
+        y = ops.softcap(x, 30.0)
+        y.backward(dy)
+        ref = torch.empty_like(dy)
+        B.poly_softcap_bwd(dt, 30.0, x.detach(), dy, ref)
+        assert torch.equal(x.grad.view(torch.int16), ref.view(torch.int16))
+    q = torch.randn(2, 16, 4, 64, device=DEV).half().requires_grad_(True)
+    k = torch.randn(2, 16, 2, 64, device=DEV).half().requires_grad_(True)
+    delta = torch.from_numpy(rope.turn_increments(64).view(np.int32)).to(DEV)
+    qo, ko = ops.rope(q, k, delta, 5)
+    (qo.float().sum() + 2 * ko.float().sum()).backward()
+    gq, gk = rope.rope_backward(np.ones((2, 4, 16, 64), np.uint16) * 0x3C00,
+                                np.ones((2, 2, 16, 64), np.uint16) * 0x4000, rope.turn_increments(64), 5)
+    assert np.array_equal(from_dev(q.grad).reshape(gq.shape), gq)
+    assert np.array_equal(from_dev(k.grad).reshape(gk.shape), gk)
