@@ -591,7 +591,7 @@ def l2_extras(dev, stream):
     return res
 
 
-def e2e(args, dev, stream, xh, dyh, chunks=16):
+def e2e(args, dev, stream, xh, dyh, chunks=8):
     """Same step through the public API with host buffers.  Per step: the
     inputs are copied from pinned host memory in `chunks` pieces on a copy
     stream, and the six kernels of each piece (waiting only for that piece)

@@ -5,11 +5,12 @@ Cases: the raw packed instructions against the oracle's arithmetic; every
 program over all 65,536 input patterns (±0, subnormals, ±inf, NaN); sizes
 1..67 at element offsets 0..7 with guard bands; in-place calls; the
 L2-resident (4,194,304) and HBM-resident (268,435,456) FP16 sweeps at full
-size (forward: every element through the oracle's exhaustive table;
-backward: sampled elements); dense SwiGLU [8192 x 14336] BF16 (sampled) and
-small contiguous and strided cases (every element); ragged routed-expert
-SwiGLU with Zipf segments (sampled, plus untouched rows past the last
-offset and the offset-validation status).
+size (every element: the program through the oracle's exhaustive table,
+products rounded once -- a product of two 16-bit values is exact in FP32 --
+plus oracle replay of sampled elements); dense SwiGLU [8192 x 14336] BF16 and
+ragged routed-expert SwiGLU with Zipf segments, every element the same way
+(plus untouched rows past the last offset and the offset-validation status);
+small contiguous and strided cases replayed element by element.
 """
 import numpy as np
 import pytest
@@ -182,6 +183,24 @@ def _lut(op):
     return torch.from_numpy(forward(op, X_ALL).view(np.int16)).to(DEV)
 
 
+def _apply_lut(op, xd):
+    """program(x) for every element, from the oracle's exhaustive table."""
+    idx = (xd.view(torch.int16).to(torch.int32) & 0xFFFF).long()
+    return _lut(op)[idx].view(xd.dtype)
+
+
+def _rn_mul(a, b):
+    """a * b rounded once to the 16-bit format: the product of two FP16 or
+    BF16 values is exact in FP32, and torch rounds its FP32 result once."""
+    return (a.float() * b.float()).to(a.dtype)
+
+
+def _equal_bits(got, want):
+    g, w = got.view(torch.int16), want.view(torch.int16)
+    nan = torch.isnan(want.float())
+    return bool(torch.equal(g[~nan], w[~nan])) and bool(torch.isnan(got.float()[nan]).all())
+
+
 def test_hbm_resident_sweep_full_size():
     """268,435,456 FP16 elements (512 MiB per tensor), 1 % outliers in
     [-40, 40].  Forward: every element equals the oracle's exhaustive table
@@ -205,6 +224,8 @@ def test_hbm_resident_sweep_full_size():
             B.poly_act_bwd(fn, dt, xd, dyd, out)
             got = from_dev(out[torch.from_numpy(sample).to(DEV)])
             assert np.array_equal(got, backward(op, x[sample], dy[sample])), fn
+            # every element: dy * program(x), one rounding
+            assert _equal_bits(out, _rn_mul(dyd, _apply_lut(op, xd))), fn
     del idx_x
     torch.cuda.empty_cache()
 
@@ -285,6 +306,11 @@ def test_dense_swiglu_full_size_sampled():
     wdg, wdu = swiglu_backward(s_op, d_op, gf[s], uf[s], dyf[s])
     assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
     assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+    # every element through the oracle's exhaustive tables
+    sg, sdg = _apply_lut(s_op, gd), _apply_lut(d_op, gd)
+    assert _equal_bits(y, _rn_mul(sg, ud))
+    assert _equal_bits(dg, _rn_mul(_rn_mul(dyd, ud), sdg))
+    assert _equal_bits(du, _rn_mul(dyd, sg))
 
 
 def test_ragged_swiglu_full_size_sampled():
@@ -321,6 +347,12 @@ def test_ragged_swiglu_full_size_sampled():
     wdg, wdu = swiglu_backward(s_op, d_op, gf[s], uf[s], dyf[s])
     assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
     assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+    # every row of every segment through the oracle's exhaustive tables
+    gs, us, dys = gd[:rows], ud[:rows], dyd[:rows]
+    sg, sdg = _apply_lut(s_op, gs), _apply_lut(d_op, gs)
+    assert _equal_bits(y[:rows], _rn_mul(sg, us))
+    assert _equal_bits(dg[:rows], _rn_mul(_rn_mul(dys, us), sdg))
+    assert _equal_bits(du[:rows], _rn_mul(dys, sg))
 
 
 @pytest.mark.parametrize("dt", DTS)
