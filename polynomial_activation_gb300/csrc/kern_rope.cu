@@ -30,7 +30,7 @@ namespace polyact {
 namespace dev {
 
 constexpr int kRopeThreads = 256;
-constexpr int kHeadUnroll = 4;
+constexpr int kHeadUnroll = 8;
 constexpr int kHeadsPerThread = 8;   // heads a thread rotates with one sine / cosine set
 
 __device__ __forceinline__ uint32_t swap_lanes(uint32_t x) { return __byte_perm(x, 0, 0x1032); }
@@ -154,8 +154,6 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
       sA ^= 0x80008000u;
       sB ^= 0x80008000u;
     }
-    const uint32_t cc[4] = {lane_lo2(cA), lane_hi2(cA), lane_lo2(cB), lane_hi2(cB)};
-    const uint32_t ss[4] = {lane_lo2(sA), lane_hi2(sA), lane_lo2(sB), lane_hi2(sB)};
     // ---- every head of this (batch, position): [B, S, H, D] <-> [B, H, S, D]
 #pragma unroll 1
     for (int64_t h0 = h_begin; h0 < h_end; h0 += kHeadUnroll) {
@@ -180,10 +178,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
           uint16_t *base = isq ? a.out_q : a.out_k;
           const int64_t row = INV ? ((b * a.seq + s) * nh + hh) : ((b * nh + hh) * a.seq + s);
           uint4 o;
-          o.x = rotate(v[u].x, cc[0], ss[0]);
-          o.y = rotate(v[u].y, cc[1], ss[1]);
-          o.z = rotate(v[u].z, cc[2], ss[2]);
-          o.w = rotate(v[u].w, cc[3], ss[3]);
+          o.x = rotate(v[u].x, lane_lo2(cA), lane_lo2(sA));
+          o.y = rotate(v[u].y, lane_hi2(cA), lane_hi2(sA));
+          o.z = rotate(v[u].z, lane_lo2(cB), lane_lo2(sB));
+          o.w = rotate(v[u].w, lane_hi2(cB), lane_hi2(sB));
           st16(base + row * a.head_dim + 8 * j, o);
         }
       }
