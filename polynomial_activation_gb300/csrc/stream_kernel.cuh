@@ -42,6 +42,16 @@ __device__ __forceinline__ void st_stream(uint16_t *p, const uint4 &v) {
                : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled as soon as every block of this one is, and wait here until the
+// previous kernel has completed and its writes are visible.  Ordering
+// between kernels is unchanged; only launch latency is hidden.  (Both are
+// no-ops for a launch without the programmatic-serialisation attribute.)
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
   uint16_t v;
   asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -91,6 +101,7 @@ __device__ __forceinline__ void apply_one(const uint16_t *const *in, uint16_t *c
 template <class Op>
 __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
                                                           typename Op::Params p) {
+  pdl_enter();
   constexpr int U = chunks_per_thread<Op>();
   int64_t n = l.n, off = 0;
   if (l.mode == kRagged) {
@@ -162,6 +173,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
 template <class Op>
 __global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
                                                            typename Op::Params p) {
+  pdl_enter();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
   const int64_t gid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -202,6 +214,23 @@ __global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
 // a persistent grid striding over the tensor).
 int64_t grid_for(const Layout &l, int per_thread);
 
+// Launch with the programmatic-stream-serialisation attribute (see pdl_enter).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launch an op on a flat / ragged layout (every op) or, when the op allows
 // it (TWO_D), on a strided one.
 template <class Op>
@@ -210,14 +239,12 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
   if constexpr (Op::TWO_D) {
     if (l.mode == kStrided) {
       const int64_t blocks = grid_for(l, l.vec ? 8 : 1);
-      strided_kernel<Op><<<(unsigned)blocks, kThreads, 0, stream>>>(s, l, p);
-      return cudaGetLastError();
+      return launch_pdl(strided_kernel<Op>, blocks, kThreads, stream, s, l, p);
     }
   }
   if (l.mode == kStrided) return cudaErrorInvalidValue;
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
-  stream_kernel<Op><<<(unsigned)blocks, kThreads, 0, stream>>>(s, l, p);
-  return cudaGetLastError();
+  return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);
 }
 
 }  // namespace dev
