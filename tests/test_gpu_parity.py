@@ -738,3 +738,26 @@ def test_autograd_wrappers_match_direct_calls():
                                 np.ones((2, 2, 16, 64), np.uint16) * 0x4000, rope.turn_increments(64), 5)
     assert np.array_equal(from_dev(q.grad).reshape(gq.shape), gq)
     assert np.array_equal(from_dev(k.grad).reshape(gk.shape), gk)
+
+
+def test_must_fail_perturbed_program_on_gpu():
+    """The parity check can fail: install a program whose c_2 is one ulp off
+    and the GPU output no longer equals the oracle's replay of the fitted
+    program (while it equals the replay of the perturbed one)."""
+    from oracle import fit
+    dt = B.POLY_BF16
+    p = B.poly_get_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    bad = B.PolyProgram.from_buffer_copy(bytes(p))
+    bad.coef[2] += 1
+    B.poly_set_program(bad)
+    try:
+        xd = to_dev(X_ALL, dt)
+        out = torch.empty_like(xd)
+        B.poly_act_fwd(B.POLY_SIGMOID, dt, xd, out)
+        got = from_dev(out)
+        good = fit.make_program(0, 0, "bf16", p.degree, p.li, p.lc, p.coefficients())
+        perturbed = fit.make_program(0, 0, "bf16", bad.degree, bad.li, bad.lc, bad.coefficients())
+        assert not np.array_equal(got, forward(good, X_ALL))
+        assert np.array_equal(got, forward(perturbed, X_ALL))
+    finally:
+        B.poly_reset_programs()
