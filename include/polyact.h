@@ -98,8 +98,10 @@ typedef struct poly_program {
 
 /* Search options of the fitter (§3.2 steps 1-7).  poly_fit_defaults fills:
  * Li in {1, 1.25, ..., 12}; Lc in {1, 1.25, ..., Li + 1}; 2,000 Chebyshev
- * nodes; 8,000 score points over [0, 12]; 8 finalists re-scored in deployed
- * order. */
+ * nodes; 8,000 score points over [0, 12]; top_k = 0 (every gated candidate is
+ * re-scored in deployed order; k > 0 keeps the k best by split-order score);
+ * lc_refine_ulps = 0 (k > 0 also re-scores each finalist with its clamp moved
+ * by 1..k target-format ulps either way, at most 64). */
 typedef struct poly_fit_opts {
   double li_min, li_max, li_step;
   double lc_min, lc_step;
@@ -107,6 +109,7 @@ typedef struct poly_fit_opts {
   int32_t n_score;
   double score_hi;
   int32_t top_k;
+  int32_t lc_refine_ulps;
 } poly_fit_opts;
 
 /* ---- status / metadata ------------------------------------------------ */
@@ -134,8 +137,9 @@ int poly_fit_defaults(poly_fit_opts *opts);
  * per multiply and per add, scored as max abs error over the score grid and
  * gated (finite; exact P(0) = f(0); range for sigmoid/tanh/sigma'/tanh';
  * monotone real-arithmetic replay for functions monotone on t >= 0); the
- * top_k candidates are re-scored in the deployed fused order and the best is
- * written to *out.  opts NULL = defaults.  Deterministic.  Host memory only.
+ * candidates (top_k of them if top_k > 0) are re-scored in the deployed fused
+ * order and gated again, and the one with the smallest deployed-order error
+ * (ties: better split rank, then the smaller clamp offset) is written to *out.  opts NULL = defaults.  Deterministic.  Host memory only.
  * Returns POLY_EINVAL (bad enum, degree outside [3, 6], bad opts, out NULL)
  * or POLY_ENOFIT (no candidate passed). */
 int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,

@@ -15,8 +15,8 @@ in its order:
    sign restoration and offset as the kernel (step 5);
 4. score the maximum absolute error on 8,000 points over [0, 12] and reject
    shape or boundary violations (step 6) and non-monotone outputs (step 7);
-5. replay the best candidates in the deployed packed-FMA order (one rounding
-   per FMA) and keep the best of those ("final acceptance", §3.2 closing
+5. replay the candidates in the deployed packed-FMA order (one rounding per
+   FMA) and keep the best of those ("final acceptance", §3.2 closing
    paragraph).
 
 Readings where the paper is silent (each also listed in the design notes):
@@ -27,8 +27,11 @@ Readings where the paper is silent (each also listed in the design notes):
   true range where its bounds are exact (sigmoid, tanh, sigma', tanh'); for
   functions monotone on t >= 0, a monotone real-arithmetic replay along the
   grid (rounded coefficients, clamp applied, no intermediate rounding).
-* Ties in score go to the smaller Li, then the smaller Lc.
-* The 8 best split-order candidates are re-scored in deployed order.
+* Every gated candidate is replayed again in deployed order and the smallest
+  deployed-order error wins; ties go to the smaller split-order error, then
+  the smaller Li, then the smaller Lc.  (With this reading the D4 centred
+  sigmoid of Figure 2 lands on the paper's Li = 5.0, with the error of the
+  printed (5.0, 5.28125) configuration.)
 * The stated error bound is the maximum over every finite target-format input
   of |deployed output - FP64 function|.
 """
@@ -45,7 +48,7 @@ from .replay import Program, evaluate, evaluate_real
 N_NODES = 2000
 N_SCORE = 8000
 SCORE_HI = 12.0
-TOP_K = 8
+TOP_K = 0          # 0: every gated candidate is replayed in deployed order
 
 
 def chebyshev_nodes(li: float, n: int = N_NODES) -> np.ndarray:
@@ -130,14 +133,28 @@ def exhaustive_error(prog: Program):
 
 
 def search(fn: int, direction: int, fmt: str, degree: int,
-           li_grid=None, lc_step: float = 0.25, top_k: int = TOP_K) -> Program:
-    """The §3.2 search; returns the accepted program (None if none passes)."""
+           li_grid=None, lc_step: float = 0.25, top_k: int = TOP_K,
+           lc_refine_ulps: int = 0) -> Program:
+    """The §3.2 search; returns the accepted program (None if none passes).
+
+    Every (Li, Lc) on the grid is replayed with split rounding (the search
+    emulator) and gated; the gated candidates are replayed again in the
+    deployed fused order, and the accepted program is the one with the
+    smallest deployed-order error ("final selection replays the deployed
+    packed-FMA order"); ties go to the smaller split-order error, then the
+    smaller Li, then the smaller Lc.  top_k > 0 restricts the deployed replay
+    to the top_k candidates by split-order error.  lc_refine_ulps = k > 0
+    also replays each such candidate with its clamp moved by 1..k
+    target-format ulps either way (Figure 2's selected clamp 5.28125 is one
+    BF16 ulp above the grid value 5.25); offsets are taken in the order
+    0, -1, +1, -2, +2, ... and only a strictly smaller error replaces."""
     if li_grid is None:
         li_grid = [1.0 + 0.25 * i for i in range(45)]
     x = score_grid(fmt)
     truth = ref.function(fn, direction)(tf.decode(x, fmt))
     form = ref.form_of(fn, direction)
-    cands = []
+    offsets = [0] + [sg * j for j in range(1, lc_refine_ulps + 1) for sg in (-1, 1)]
+    split = []            # (split_err, li, lc, cb) of every gated grid candidate
     for li in li_grid:
         cb = tf.from_f64(fit_coefficients(fn, direction, degree, li), fmt)
         n_lc = int(round(li / lc_step)) + 1           # 1, 1+step, ..., Li+1
@@ -148,22 +165,39 @@ def search(fn: int, direction: int, fmt: str, degree: int,
         err = np.max(np.abs(tf.decode(y, fmt) - truth), axis=-1)
         for k in range(n_lc):
             if ok[k]:
-                cands.append((float(err[k]), li, float(lcs[k]), cb))
-    if not cands:
+                split.append((float(err[k]), li, float(lcs[k]), cb))
+    if not split:
         return None
-    cands.sort(key=lambda c: (c[0], c[1], c[2]))
+    split.sort(key=lambda c: (c[0], c[1], c[2]))
+    finalists = split if top_k <= 0 else split[:top_k]
+    # deployed-order replay, grouped by Li (one set of coefficients each)
+    by_li = {}
+    for rank, (split_err, li, lc, cb) in enumerate(finalists):
+        by_li.setdefault(li, []).append((rank, split_err, lc, cb))
     best = None
-    for rank, (split_err, li, lc, cb) in enumerate(cands[:top_k]):
-        lcb = tf.from_f64(lc, fmt)
+    for li, group in by_li.items():
+        cb = group[0][3]
+        rows = []
+        for rank, split_err, lc0, _ in group:
+            for oi, off in enumerate(offsets):
+                lcb = int(tf.from_f64(lc0, fmt)) + off
+                lc = float(tf.decode(np.uint16(lcb), fmt))
+                if 0.0 < lc <= li + 1.0:
+                    rows.append((rank, oi, split_err, lc, lcb))
+        lcb = np.array([r[4] for r in rows], dtype=np.uint16)[:, None]
+        lcv = np.array([r[3] for r in rows])[:, None]
         y = evaluate(form, tuple(cb), lcb, x, fmt, fused=True)
-        if not _gates(fn, direction, y[None, :], fmt, cb, lc, x)[0]:
-            continue
-        err = float(np.max(np.abs(tf.decode(y, fmt) - truth)))
-        if best is None or err < best[0]:
-            best = (err, rank, split_err, li, lc, cb)
+        ok = _gates(fn, direction, y, fmt, cb, lcv, x)
+        err = np.max(np.abs(tf.decode(y, fmt) - truth), axis=-1)
+        for (rank, oi, split_err, lc, _), e, g in zip(rows, err, ok):
+            if not g:
+                continue
+            key = (float(e), rank, oi)
+            if best is None or key < best[0]:
+                best = (key, split_err, li, lc, cb)
     if best is None:
         return None
-    err, rank, split_err, li, lc, cb = best
+    (err, rank, _), split_err, li, lc, cb = best
     prog = make_program(fn, direction, fmt, degree, li, lc, cb)
     bound, at = exhaustive_error(prog)
     prog.info = {"search_score": split_err, "deployed_score": err, "rank": rank,

@@ -22,6 +22,9 @@ POLY_MAX_DEGREE = 6
 POLY_PROGRAM_VERSION = 1
 FN = {"sigmoid": POLY_SIGMOID, "tanh": POLY_TANH, "silu": POLY_SILU, "gelu": POLY_GELU}
 
+# version of include/polyact.h this binding marshals for (poly_abi_version)
+ABI_VERSION = 2
+
 # every function declared in include/polyact.h
 EXPORTS = [
     "poly_status_str", "poly_last_cuda_error", "poly_abi_version", "poly_form_of",
@@ -61,6 +64,7 @@ class PolyFitOpts(ctypes.Structure):
         ("lc_min", ctypes.c_double), ("lc_step", ctypes.c_double),
         ("n_nodes", ctypes.c_int32), ("n_score", ctypes.c_int32),
         ("score_hi", ctypes.c_double), ("top_k", ctypes.c_int32),
+        ("lc_refine_ulps", ctypes.c_int32),
     ]
 
 
@@ -125,6 +129,9 @@ def lib():
     for name in EXPORTS:
         if name not in ("poly_status_str",):
             getattr(L, name).restype = _i
+    if L.poly_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{LIB_PATH}: ABI version {L.poly_abi_version()}, "
+                           f"this binding expects {ABI_VERSION}; rebuild the library")
     _LIB = L
     return L
 

@@ -230,7 +230,7 @@ const char *poly_status_str(int status) {
 
 int poly_last_cuda_error(void) { return t_last_cuda_error; }
 
-int poly_abi_version(void) { return 1; }
+int poly_abi_version(void) { return 2; }
 
 int poly_form_of(int fn, int dir) {
   if (!valid_fn(fn) || !valid_dir(dir)) return POLY_EINVAL;
@@ -254,7 +254,8 @@ int poly_fit_defaults(poly_fit_opts *o) {
   o->n_nodes = 2000;
   o->n_score = 8000;
   o->score_hi = 12.0;
-  o->top_k = 8;
+  o->top_k = 0;
+  o->lc_refine_ulps = 0;
   return POLY_OK;
 }
 
@@ -270,7 +271,7 @@ int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
     o = *opts;
   if (!(o.li_min > 0) || !(o.li_step > 0) || !(o.li_max >= o.li_min) || !(o.lc_min > 0) ||
       !(o.lc_step > 0) || o.n_nodes < degree || o.n_score < 2 || !(o.score_hi > 0) ||
-      o.top_k < 1 || o.li_max > 1e4 || (o.li_max - o.li_min) / o.li_step > 1e5)
+      o.top_k < 0 || o.lc_refine_ulps < 0 || o.lc_refine_ulps > 64 || o.li_max > 1e4 || (o.li_max - o.li_min) / o.li_step > 1e5)
     return POLY_EINVAL;
   return fit_program(fn, dir, dtype, degree, o, out);
 }

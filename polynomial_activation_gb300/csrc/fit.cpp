@@ -9,14 +9,15 @@
 //      add, with the kernel's reduction, clamp, sign restoration and offset;
 //   4. score the maximum absolute error on 8,000 points over [0, 12] and
 //      reject clamps with Lc > Li + 1 and shape or boundary violations;
-//   5. re-score the best candidates in the deployed packed-FMA order (one
+//   5. re-score the candidates in the deployed packed-FMA order (one
 //      rounding per FMA) and accept the best of those.
 // Readings where the paper is silent: first-kind Chebyshev nodes; Li on
 // {1, 1.25, ..., 12} and Lc on {1, 1.25, ..., Li + 1}; the score points are
 // linspace(0, 12, 8000) rounded to the format; gates = finite outputs, exact
 // P(0) = f(0), output range for sigmoid / tanh / sigma' / tanh', and a
-// monotone real-arithmetic replay for functions monotone on t >= 0; ties go
-// to the smaller Li then the smaller Lc; 8 finalists.
+// monotone real-arithmetic replay for functions monotone on t >= 0; every
+// gated candidate is re-scored in deployed order (ties to the smaller split
+// error, then the smaller Li, then the smaller Lc).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -409,29 +410,79 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
   }
   std::vector<Cand> cands;
   for (auto &v : per_li) cands.insert(cands.end(), v.begin(), v.end());
-  std::vector<uint16_t> y(grid.size());
   if (cands.empty()) return POLY_ENOFIT;
   std::stable_sort(cands.begin(), cands.end(), [](const Cand &a, const Cand &b) {
     if (a.score != b.score) return a.score < b.score;
     if (a.li != b.li) return a.li < b.li;
     return a.lc < b.lc;
   });
-  int best = -1;
-  double best_err = 0;
-  const int k = std::min<int>(o.top_k, (int)cands.size());
+  // deployed-order replay of the finalists (all gated candidates when top_k
+  // is 0), each clamp also moved by 1..lc_refine_ulps format ulps either way
+  // in the order 0, -1, +1, -2, +2, ...; the smallest deployed-order error
+  // wins, ties to the better split rank, then the earlier offset
+  const int k = o.top_k > 0 ? std::min<int>(o.top_k, (int)cands.size()) : (int)cands.size();
+  std::vector<int> offsets{0};
+  for (int j = 1; j <= o.lc_refine_ulps; ++j) {
+    offsets.push_back(-j);
+    offsets.push_back(j);
+  }
+  const uint32_t inf_bits = dtype == POLY_F16 ? 0x7C00u : 0x7F80u;
+  struct Trial {
+    int rank, off_idx;
+    uint16_t lcb;
+    double lc, err;
+    bool ok;
+  };
+  std::vector<Trial> trials;
   for (int r = 0; r < k; ++r) {
-    const uint16_t lcb = from_double(cands[r].lc, dtype);
-    double worst = 0;
-    for (size_t i = 0; i < grid.size(); ++i) {
-      y[i] = replay_one(form, cands[r].coef, degree, lcb, grid[i], dtype, true);
-      worst = std::max(worst, std::fabs(to_double(y[i], dtype) - truth[i]));
-    }
-    if (!gates(fn, dir, dtype, form, degree, cands[r].coef, cands[r].lc, grid, y)) continue;
-    if (best < 0 || worst < best_err) {
-      best = r;
-      best_err = worst;
+    const int lcb0 = from_double(cands[r].lc, dtype);
+    for (size_t oi = 0; oi < offsets.size(); ++oi) {
+      const int b = lcb0 + offsets[oi];
+      if (b <= 0 || (uint32_t)b >= inf_bits) continue;
+      const double lc = to_double((uint16_t)b, dtype);
+      if (!(lc > 0.0 && lc <= cands[r].li + 1.0)) continue;
+      trials.push_back(Trial{r, (int)oi, (uint16_t)b, lc, 0.0, false});
     }
   }
+  auto deployed = [&](size_t first, size_t stride) {
+    std::vector<uint16_t> y(grid.size());
+    for (size_t t = first; t < trials.size(); t += stride) {
+      Trial &tr = trials[t];
+      const Cand &c = cands[tr.rank];
+      double worst = 0;
+      for (size_t i = 0; i < grid.size(); ++i) {
+        y[i] = replay_one(form, c.coef, degree, tr.lcb, grid[i], dtype, true);
+        worst = std::max(worst, std::fabs(to_double(y[i], dtype) - truth[i]));
+      }
+      tr.err = worst;
+      tr.ok = gates(fn, dir, dtype, form, degree, c.coef, tr.lc, grid, y);
+    }
+  };
+  unsigned nth2 = std::thread::hardware_concurrency();
+  if (nth2 == 0) nth2 = 1;
+  if (nth2 > trials.size()) nth2 = (unsigned)trials.size();
+  if (nth2 <= 1) {
+    deployed(0, 1);
+  } else {
+    std::vector<std::thread> pool;
+    for (unsigned t = 0; t < nth2; ++t) pool.emplace_back(deployed, (size_t)t, (size_t)nth2);
+    for (auto &th : pool) th.join();
+  }
+  int bt = -1;
+  for (int t = 0; t < (int)trials.size(); ++t) {
+    const Trial &tr = trials[t];
+    if (!tr.ok) continue;
+    if (bt < 0) {
+      bt = t;
+      continue;
+    }
+    const Trial &b = trials[bt];
+    if (tr.err < b.err || (tr.err == b.err && (tr.rank < b.rank ||
+                                               (tr.rank == b.rank && tr.off_idx < b.off_idx))))
+      bt = t;
+  }
+  const int best = bt < 0 ? -1 : trials[bt].rank;
+  const double best_err = bt < 0 ? 0.0 : trials[bt].err;
   if (best < 0) return POLY_ENOFIT;
   const Cand &w = cands[best];
   poly_program p;
@@ -442,9 +493,9 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
   p.form = form;
   p.degree = degree;
   for (int j = 0; j <= degree; ++j) p.coef[j] = w.coef[j];
-  p.lc_bits = from_double(w.lc, dtype);
+  p.lc_bits = trials[bt].lcb;
   p.li = w.li;
-  p.lc = w.lc;
+  p.lc = trials[bt].lc;
   p.search_score = w.score;
   p.deployed_score = best_err;
   p.rank = best;

@@ -69,6 +69,23 @@ def test_cpp_fitter_reproduces_oracle_programs(k):
     assert p.table2 == pytest.approx(g["table2"], rel=1e-9)
 
 
+@pytest.mark.parametrize("fn,D,top_k,refine", [(0, 3, 8, 0), (3, 5, 8, 0), (0, 4, 0, 2),
+                                                (1, 4, 3, 1)])
+def test_cpp_fitter_options_match_oracle(fn, D, top_k, refine):
+    """top_k (deployed replay of the k best split-order candidates) and
+    lc_refine_ulps (clamp moved by up to k BF16 ulps) select the same program
+    in the C++ fitter as in the oracle fitter."""
+    from oracle import fit
+    o = B.poly_fit_defaults()
+    assert (o.top_k, o.lc_refine_ulps) == (0, 0)
+    o.top_k, o.lc_refine_ulps = top_k, refine
+    p = B.poly_fit(fn, 0, B.POLY_BF16, D, o)
+    q = fit.search(fn, 0, "bf16", D, top_k=top_k, lc_refine_ulps=refine)
+    assert p.coefficients() == [int(c) for c in q.coef]
+    assert (p.li, p.lc, p.lc_bits, p.rank) == (q.li, q.lc, int(q.lc_bits), q.info["rank"])
+    assert p.deployed_score == q.info["deployed_score"]
+
+
 def test_fit_is_deterministic_and_registry_roundtrip():
     a = B.poly_fit(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16, 4)
     b = B.poly_fit(B.POLY_TANH, B.POLY_FWD, B.POLY_BF16, 4)
@@ -96,6 +113,11 @@ def test_fit_argument_errors(L):
     o.li_step = 0.0
     assert L.poly_fit(0, 0, 0, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_EINVAL
     assert L.poly_fit_defaults(None) == B.POLY_EINVAL
+    for field, value in (("top_k", -1), ("lc_refine_ulps", -1), ("lc_refine_ulps", 65)):
+        o = B.poly_fit_defaults()
+        setattr(o, field, value)
+        assert L.poly_fit(0, 0, 0, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_EINVAL
+    assert L.poly_abi_version() == B.ABI_VERSION == 2
     # no admissible clamp at all: Lc starts above Li + 1
     o = B.poly_fit_defaults()
     o.li_max, o.lc_min = 2.0, 5.0

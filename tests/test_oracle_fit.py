@@ -99,11 +99,12 @@ def _table2_rows():
 
 
 # How close the accepted program's Table 2 metric must come to the printed
-# value.  sigma' D4 lands on the paper's value; the others are order-of-
-# magnitude checks, because the paper's exact (Li, Lc) choice is not
-# reproducible from its text (its Lc values are off the stated 0.25 grid).
-T2_FACTOR = {("bwd", "sigmoid"): 1.02, ("fwd", "sigmoid"): 1.25, ("fwd", "tanh"): 1.5,
-             ("fwd", "silu"): 2.0, ("fwd", "gelu"): 5.0}
+# value.  sigma' D4 and the D3 centred sigmoid land within 1% of the paper's
+# values; the others are order-of-magnitude checks, because the paper's exact
+# (Li, Lc) choice is not reproducible from its text (its Lc values are off
+# the stated 0.25 grid).
+T2_FACTOR = {("bwd", "sigmoid"): 1.02, ("fwd", "sigmoid"): 1.02, ("fwd", "tanh"): 1.5,
+             ("fwd", "silu"): 2.0, ("fwd", "gelu"): 3.0}
 
 
 @pytest.mark.parametrize("row", _table2_rows())
@@ -118,11 +119,12 @@ def test_table2_magnitudes(row):
     assert printed / k <= m <= printed * k, (name, m, printed)
 
 
-def test_figure2_configuration_is_competitive():
-    """The D4 centred sigmoid at the paper's selected (Li, Lc) = (5.0,
-    5.28125) (Fig. 2b) scores at least as well, in deployed order, as the
-    program our 0.25-grid search accepts -- its Lc is one BF16 ulp above the
-    grid value 5.25."""
+def test_figure2_configuration_is_reproduced():
+    """The D4 centred sigmoid search lands on the fit interval of the paper's
+    selected (Li, Lc) = (5.0, 5.28125) (Fig. 2b) and on a clamp one BF16 ulp
+    below it (the printed Lc is off the 0.25 grid), with exactly the same
+    maximum error over every finite BF16 input; allowing the clamp to move by
+    one ulp does not find a better program."""
     with open(os.path.join(GOLDEN, "figure2_selected.txt")) as f:
         name, d, D, li, lc = [l for l in f if not l.startswith("#")][0].split()
     li, lc, D = float(li), float(lc), int(D)
@@ -131,8 +133,26 @@ def test_figure2_configuration_is_competitive():
     p = fit.make_program(ref.SIGMOID, ref.FWD, "bf16", D, li, lc, cb)
     err_fig2 = fit.exhaustive_error(p)[0]
     ours = fit.search(ref.SIGMOID, ref.FWD, "bf16", D)
-    assert err_fig2 <= ours.info["stated_max_abs_err"]
-    assert err_fig2 < 6e-3
+    assert ours.li == li and int(ours.lc_bits) == int(tf.from_f64(lc, "bf16")) - 1
+    assert err_fig2 == ours.info["stated_max_abs_err"] < 6e-3
+    refined = fit.search(ref.SIGMOID, ref.FWD, "bf16", D, lc_refine_ulps=1)
+    assert (refined.li, refined.lc) == (ours.li, ours.lc)
+
+
+def test_top_k_restricts_the_deployed_replay():
+    """Keeping only the 8 best split-order candidates for the deployed replay
+    can only do as well as replaying them all (the D3 centred sigmoid and the
+    D5 GELU do strictly worse with 8)."""
+    for fn, D in ((ref.SIGMOID, 3), (ref.GELU, 5)):
+        every = fit.search(fn, ref.FWD, "bf16", D)
+        top8 = fit.search(fn, ref.FWD, "bf16", D, top_k=8)
+        assert every.info["deployed_score"] < top8.info["deployed_score"]
+        assert top8.info["rank"] < 8 <= every.info["rank"]
+
+
+def _stated_bound(args):
+    fn, d, D = args
+    return fit.search(fn, d, "bf16", D).info["stated_max_abs_err"]
 
 
 @pytest.mark.slow
@@ -140,10 +160,16 @@ def test_higher_degree_can_be_worse_figs_4_5():
     """In each of the six BF16 sweeps (sigmoid, tanh, SiLU forward; their
     derivatives backward), at least one higher-degree program has a larger
     maximum error than a lower-degree one after replay (§5.1, Figs. 4-5)."""
-    for fn in (ref.SIGMOID, ref.TANH, ref.SILU):
-        for d in (ref.FWD, ref.BWD):
-            errs = [fit.search(fn, d, "bf16", D).info["stated_max_abs_err"] for D in (3, 4, 5, 6)]
-            assert any(errs[j] > errs[i] for i in range(4) for j in range(i + 1, 4)), (fn, d, errs)
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    sweeps = [(fn, d) for fn in (ref.SIGMOID, ref.TANH, ref.SILU) for d in (ref.FWD, ref.BWD)]
+    jobs = [(fn, d, D) for fn, d in sweeps for D in (3, 4, 5, 6)]
+    workers = max(1, min(len(jobs), os.cpu_count() or 1))
+    with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+        bounds = list(ex.map(_stated_bound, jobs))
+    for i, (fn, d) in enumerate(sweeps):
+        errs = bounds[4 * i:4 * i + 4]
+        assert any(errs[j] > errs[i2] for i2 in range(4) for j in range(i2 + 1, 4)), (fn, d, errs)
 
 
 @pytest.mark.slow
