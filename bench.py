@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -83,7 +84,10 @@ def recorded_traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+    """nvidia-smi clock / throttle-reason samples every 200 ms.  start()
+    returns once the first sample has arrived, so the sampler is running when
+    the timed region begins; stop() keeps only the samples that arrived after
+    start() returned."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -92,6 +96,16 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.first = threading.Event()
+        self.reader = None
+        self.skip = 0
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+            self.first.set()
+        self.first.set()
 
     def start(self):
         try:
@@ -101,15 +115,21 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        self.first.wait(timeout=10)
+        self.skip = len(self.lines)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        self.proc.wait(timeout=10)
+        self.reader.join(timeout=10)
         sm, smax, mem, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.lines[self.skip:]:
             v = [s.strip() for s in line.split(",")]
             if len(v) < 7:
                 continue
@@ -298,10 +318,10 @@ def main():
     clocks.start()
     # the timed region: K steps back to back (no events between kernels)
     total_ms, _ = timed_steps(False, args.steps, per_kernel=False)
-    clk = clocks.stop()
-    # per-kernel durations for the roofline: a second pass with an event pair
-    # around every launch
+    # per-kernel durations for the roofline: a second timed pass with an event
+    # pair around every launch; the clock samples cover both passes
     _, per_ms = timed_steps(False, max(50, args.steps // 4))
+    clk = clocks.stop()
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     elems_per_step = 6 * n * world
