@@ -2,14 +2,18 @@
 
 Against: (1) an independent exact-rational model (tests/exact_t.py) on
 structured exhaustive domains and on random triples with every special value
-mixed in; (2) library routines that are correctly rounded in special cases:
-numpy's float64 -> float16 conversion, and float32 -> bfloat16 conversion of
-torch, on products that are exact in the wider type.
+mixed in; (2) a second exact model in scaled integers (tests/exact_int.py,
+itself pinned to the rational one here), which is fast enough to check ten
+million random triples per format and exhaustive rows of mul and add;
+(3) library routines that are correctly rounded in special cases: numpy's
+float64 -> float16 conversion, and float32 -> bfloat16 conversion of torch, on
+products that are exact in the wider type.
 """
 import numpy as np
 import pytest
 import torch
 
+import exact_int as ei
 import exact_t as ex
 from oracle import tformat as tf
 
@@ -182,3 +186,82 @@ def test_from_f64_vs_exact(fmt):
     got = tf.from_f64(vals, fmt)
     for v, g in zip(vals, got):
         assert int(g) == ex.from_fraction(Fraction(float(v)), fmt), v
+
+
+# ------------------------------------------------ the scaled-integer model
+
+def _cancelling(rng, n, fmt):
+    """Triples whose addend is within a few ulps of -a*b (heavy cancellation),
+    with a and b of moderate magnitude."""
+    lo, hi = (0x2000, 0x5800) if fmt == "f16" else (0x3800, 0x4300)
+    a = rng.integers(lo, hi, n).astype(np.uint16) | (rng.integers(0, 2, n).astype(np.uint16) << 15)
+    b = rng.integers(lo, hi, n).astype(np.uint16) | (rng.integers(0, 2, n).astype(np.uint16) << 15)
+    p = ei.mul(a, b, fmt) ^ np.uint16(0x8000)
+    c = (p.astype(np.int64) + rng.integers(-3, 4, n)).astype(np.uint16)
+    return a, b, c
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_integer_model_matches_rationals(fmt):
+    """The scaled-integer model agrees with the exact-rational model on mixed
+    random triples (specials included) and on cancelling triples."""
+    rng = np.random.default_rng(21 if fmt == "f16" else 22)
+    n = 15000
+    a, b, c = (_rand_bits(rng, n, fmt) for _ in range(3))
+    a2, b2, c2 = _cancelling(rng, 5000, fmt)
+    a, b, c = np.concatenate([a, a2]), np.concatenate([b, b2]), np.concatenate([c, c2])
+    got = ei.fma(a, b, c, fmt)
+    for i in range(a.size):
+        assert int(got[i]) == ex.fma(int(a[i]), int(b[i]), int(c[i]), fmt), (
+            hex(a[i]), hex(b[i]), hex(c[i]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fma_ten_million_triples(fmt):
+    """10^7 triples per format: oracle fma, mul and add equal the exact
+    integer model bit for bit.  Each block of 10^6 mixes uniform patterns,
+    moderate magnitudes and specials (_rand_bits) or holds cancelling triples."""
+    rng = np.random.default_rng(31 if fmt == "f16" else 32)
+    block = 1_000_000
+    for k in range(10):
+        if k % 3 == 2:
+            a, b, c = _cancelling(rng, block, fmt)
+        else:
+            a, b, c = (_rand_bits(rng, block, fmt) for _ in range(3))
+        want = ei.fma(a, b, c, fmt)
+        got = tf.fma(a, b, c, fmt)
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, [(hex(a[i]), hex(b[i]), hex(c[i]), hex(got[i]), hex(want[i]))
+                               for i in bad[:5]]
+        if k < 4:
+            assert _same(tf.mul(a, b, fmt), ei.mul(a, b, fmt))
+            assert _same(tf.add(a, c, fmt), ei.add(a, c, fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mul_add_exhaustive_rows(fmt):
+    """Every pattern as the first operand against 48 second operands (the
+    specials and random patterns): mul and add equal the integer model."""
+    x = tf.all_patterns()
+    rng = np.random.default_rng(41)
+    ys = list(SPECIALS[fmt]) + [int(v) for v in rng.integers(0, 65536, 48 - len(SPECIALS[fmt]))]
+    for y in ys:
+        yy = np.uint16(y)
+        assert _same(tf.mul(x, yy, fmt), ei.mul(x, yy, fmt)), hex(y)
+        assert _same(tf.add(x, yy, fmt), ei.add(x, yy, fmt)), hex(y)
+
+
+def test_integer_model_catches_double_rounding():
+    """Must-fail control: an fma that rounds a*b + c in FP64 and then again to
+    BF16 (a plausible oracle mistake) disagrees with the integer model on
+    random BF16 triples, whose exponent range lets the FP64 sum be inexact.
+    (For FP16 the same shortcut gives the correctly rounded result: with its
+    narrow exponent range, whatever the FP64 sum drops lies far from every
+    FP16 rounding boundary unless the result overflows.)"""
+    rng = np.random.default_rng(51)
+    a, b, c = (_rand_bits(rng, 200_000, "bf16") for _ in range(3))
+    with np.errstate(all="ignore"):
+        naive = tf.from_f64(tf.decode(a, "bf16") * tf.decode(b, "bf16") + tf.decode(c, "bf16"),
+                            "bf16")
+    assert np.count_nonzero(naive != ei.fma(a, b, c, "bf16")) > 0
