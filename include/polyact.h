@@ -353,6 +353,18 @@ enum { POLY_DIAG_FMA = 0, POLY_DIAG_MUL = 1, POLY_DIAG_MIN_NAN = 2, POLY_DIAG_MA
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c,
                      void *out, int64_t n, poly_stream_t stream);
 
+/* ---- failure injection (host only; no counterpart in the paper) ----------
+ * poly_debug_fail_launches: the next `count` kernel launches, from any entry
+ * point above, are not enqueued; each of those calls returns POLY_ECUDA and
+ * sets poly_last_cuda_error() to `cuda_error`, exactly as a failed launch
+ * would.  Validation still runs first, and calls that launch nothing (n == 0,
+ * invalid arguments) do not consume a failure.  This lets a caller's handling
+ * of launch failures be tested without faulting a GPU.  Process-wide and
+ * thread-safe; count == 0 clears pending failures.  Returns the number of
+ * failures that were still pending, or POLY_EINVAL (cuda_error <= 0 or
+ * count < 0). */
+int poly_debug_fail_launches(int cuda_error, int count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,7 @@ EXPORTS = [
     "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
     "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
+    "poly_debug_fail_launches",
     "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd", "poly_exp2",
     "poly_ctrl_exp2", "poly_rope_fwd", "poly_rope_bwd", "poly_rope_turn_increments",
     "poly_rope_programs",
@@ -126,6 +127,7 @@ def lib():
     L.poly_swiglu_fwd_ragged.argtypes = [_i, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
     L.poly_swiglu_bwd_ragged.argtypes = [_i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
     L.poly_diag_packed.argtypes = [_i, _i, _p, _p, _p, _p, _i64, _p]
+    L.poly_debug_fail_launches.argtypes = [_i, _i]
     for name in EXPORTS:
         if name not in ("poly_status_str",):
             getattr(L, name).restype = _i
@@ -306,6 +308,15 @@ def poly_diag_packed(op, dtype, a, b, c, out, n=None, stream=None):
     n = a.numel() if n is None else n
     _check(lib().poly_diag_packed(op, dtype, _ptr(a), _ptr(b), _ptr(c), _ptr(out), n,
                                   _stream(stream)), "poly_diag_packed")
+
+
+def poly_debug_fail_launches(cuda_error, count):
+    """Make the next `count` launches report `cuda_error` without running;
+    returns how many injected failures were still pending."""
+    st = lib().poly_debug_fail_launches(cuda_error, count)
+    if st < 0:
+        _check(st, "poly_debug_fail_launches")
+    return st
 
 
 def poly_derive_program(fwd: PolyProgram):

@@ -35,6 +35,25 @@ int cuda_status(cudaError_t e) {
   return POLY_ECUDA;
 }
 
+// Injected launch failures (poly_debug_fail_launches).
+std::mutex g_fail_mu;
+int g_fail_pending = 0;
+int g_fail_code = 0;
+
+// Runs the launch unless an injected failure is pending, in which case the
+// launch is skipped and that failure is reported instead.
+template <class Launch>
+int launch_status(Launch &&launch) {
+  {
+    std::lock_guard<std::mutex> lk(g_fail_mu);
+    if (g_fail_pending > 0) {
+      --g_fail_pending;
+      return cuda_status((cudaError_t)g_fail_code);
+    }
+  }
+  return cuda_status(launch());
+}
+
 DevProg dev_prog(const poly_program &p) {
   DevProg d;
   std::memset(&d, 0, sizeof(d));
@@ -232,6 +251,15 @@ int poly_last_cuda_error(void) { return t_last_cuda_error; }
 
 int poly_abi_version(void) { return 2; }
 
+int poly_debug_fail_launches(int cuda_error, int count) {
+  if (cuda_error <= 0 || count < 0) return POLY_EINVAL;
+  std::lock_guard<std::mutex> lk(g_fail_mu);
+  const int pending = g_fail_pending;
+  g_fail_pending = count;
+  g_fail_code = cuda_error;
+  return pending;
+}
+
 int poly_form_of(int fn, int dir) {
   if (!valid_fn(fn) || !valid_dir(dir)) return POLY_EINVAL;
   return form_of_fn(fn, dir);
@@ -330,12 +358,13 @@ static int act_call(bool ctrl, int kind, int fn, int dtype, const void *x, const
   Streams s{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dy), nullptr,
             static_cast<uint16_t *>(y), nullptr};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (ctrl) return cuda_status(launch_ctrl(kind, dtype, fn, s, l, cs));
+  if (ctrl) return launch_status([&] { return launch_ctrl(kind, dtype, fn, s, l, cs); });
   poly_program p;
   int st = registry_get(fn, bwd ? POLY_BWD : POLY_FWD, dtype, &p);
   if (st != POLY_OK) return st;
   DevProg d = dev_prog(p);
-  return cuda_status(launch_poly(kind, dtype, p.form, p.degree, 0, s, l, d, d, cs));
+  return launch_status(
+      [&] { return launch_poly(kind, dtype, p.form, p.degree, 0, s, l, d, d, cs); });
 }
 
 int poly_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n, poly_stream_t stream) {
@@ -372,13 +401,15 @@ static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void
             static_cast<uint16_t *>(o1)};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int kind = bwd ? kSwigluBwd : kSwigluFwd;
-  if (ctrl) return cuda_status(launch_ctrl(kind, dtype, POLY_SILU, s, l, cs));
+  if (ctrl) return launch_status([&] { return launch_ctrl(kind, dtype, POLY_SILU, s, l, cs); });
   const int variant = g_swiglu_variant.load();
   poly_program ps, pd;
   st = swiglu_programs(variant, dtype, bwd, &ps, &pd);
   if (st != POLY_OK) return st;
-  return cuda_status(launch_poly(kind, dtype, ps.form, ps.degree, pd.degree, s, l,
-                                 dev_prog(ps), dev_prog(pd), cs, variant));
+  return launch_status([&] {
+    return launch_poly(kind, dtype, ps.form, ps.degree, pd.degree, s, l, dev_prog(ps),
+                       dev_prog(pd), cs, variant);
+  });
 }
 
 int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
@@ -426,9 +457,11 @@ static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const 
   Streams s{static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(u),
             static_cast<const uint16_t *>(dy), static_cast<uint16_t *>(o0),
             static_cast<uint16_t *>(o1)};
-  return cuda_status(launch_poly(bwd ? kSwigluBwd : kSwigluFwd, dtype, ps.form, ps.degree,
-                                 pd.degree, s, l, dev_prog(ps), dev_prog(pd),
-                                 reinterpret_cast<cudaStream_t>(stream), variant));
+  return launch_status([&] {
+    return launch_poly(bwd ? kSwigluBwd : kSwigluFwd, dtype, ps.form, ps.degree, pd.degree, s,
+                       l, dev_prog(ps), dev_prog(pd), reinterpret_cast<cudaStream_t>(stream),
+                       variant);
+  });
 }
 
 int poly_swiglu_fwd_ragged(int dtype, const void *g, const void *u, void *y,
@@ -470,8 +503,10 @@ static int softcap_call(bool bwd, int dtype, double alpha, const void *x, const 
   if (st != POLY_OK) return st;
   Streams s{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dy), nullptr,
             static_cast<uint16_t *>(out), nullptr};
-  return cuda_status(launch_softcap(bwd ? 1 : 0, dtype, p.degree, s, l, dev_prog(p), a, ia,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status([&] {
+    return launch_softcap(bwd ? 1 : 0, dtype, p.degree, s, l, dev_prog(p), a, ia,
+                          reinterpret_cast<cudaStream_t>(stream));
+  });
 }
 
 int poly_softcap_fwd(int dtype, double alpha, const void *x, void *y, int64_t n,
@@ -515,7 +550,8 @@ static int exp2_call(int core, const float *x, float *y, int64_t n, poly_stream_
   const int vec = ((reinterpret_cast<uintptr_t>(x) ^ reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   uint16_t c[3];
   exp2_constants(core, c);
-  return cuda_status(launch_exp2(core, x, y, n, vec, c, reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status(
+      [&] { return launch_exp2(core, x, y, n, vec, c, reinterpret_cast<cudaStream_t>(stream)); });
 }
 
 int poly_exp2(int core, const float *x, float *y, int64_t n, poly_stream_t stream) {
@@ -599,7 +635,8 @@ static int rope_call(int inv, int variant, const void *q, const void *k, void *q
              static_cast<uint16_t *>(q_out), static_cast<uint16_t *>(k_out), delta,
              static_cast<const uint16_t *>(cos_tab), static_cast<const uint16_t *>(sin_tab),
              batch, seq, hq, hkv, head_dim, pos_offset};
-  return cuda_status(launch_rope(variant, inv, a, kc, reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status(
+      [&] { return launch_rope(variant, inv, a, kc, reinterpret_cast<cudaStream_t>(stream)); });
 }
 
 int poly_rope_fwd(int variant, const void *q, const void *k, void *q_out, void *k_out,
@@ -635,7 +672,8 @@ int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void
   Layout l = flat_layout(ptrs, 4, n);
   Streams s{static_cast<const uint16_t *>(a), static_cast<const uint16_t *>(b),
             static_cast<const uint16_t *>(c), static_cast<uint16_t *>(out), nullptr};
-  return cuda_status(launch_diag(op, dtype, s, l, reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status(
+      [&] { return launch_diag(op, dtype, s, l, reinterpret_cast<cudaStream_t>(stream)); });
 }
 
 }  // extern "C"

@@ -186,6 +186,21 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_last_cuda_error() == 0
 
 
+def test_failure_injection_is_consumed_only_by_launches(L):
+    """Injected launch failures (poly_debug_fail_launches) wait for a call
+    that would launch: invalid or empty calls leave them pending."""
+    assert L.poly_debug_fail_launches(0, 1) == B.POLY_EINVAL
+    assert L.poly_debug_fail_launches(-5, 1) == B.POLY_EINVAL
+    assert L.poly_debug_fail_launches(701, -1) == B.POLY_EINVAL
+    assert L.poly_debug_fail_launches(701, 2) == 0
+    try:
+        assert L.poly_act_fwd(0, 0, FAKE + 1, FAKE + 4096, 8, None) == B.POLY_EINVAL
+        assert L.poly_act_fwd(0, 0, None, None, 0, None) == B.POLY_OK
+        assert L.poly_last_cuda_error() == 0
+    finally:
+        assert L.poly_debug_fail_launches(701, 0) == 2       # both still pending; cleared
+
+
 def test_swiglu_variant_switch(L):
     assert B.poly_get_swiglu_variant() == B.POLY_SWIGLU_DIRECT
     try:

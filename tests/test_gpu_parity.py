@@ -139,6 +139,40 @@ def test_small_sizes_offsets_and_guards(dt):
             assert guards_intact(buf, n, G, off_y), (n, off_x, off_y)
 
 
+def test_injected_launch_failures_leave_outputs_and_context_intact():
+    """Two injected launch failures (poly_debug_fail_launches): the next two
+    launching calls -- an activation and a SwiGLU -- raise POLY_ECUDA with the
+    injected CUDA code and write nothing; the third call runs and is exact,
+    and the CUDA context stays usable."""
+    dt, fmt = B.POLY_BF16, "bf16"
+    n, G = 4099, 64
+    x = _rand_bits(np.random.default_rng(12), n, fmt)
+    xb = to_dev(x, dt)
+    buf, y = sentinel_buffer(n, G, dt, 0)
+    before = from_dev(buf).copy()
+    g, u = (to_dev(_rand_bits(np.random.default_rng(s), 8 * 64, fmt), dt).view(8, 64)
+            for s in (13, 14))
+    ys = torch.full((8, 64), 0x1234, dtype=torch.int16, device=DEV).view(TDT[dt])
+    assert B.poly_debug_fail_launches(701, 2) == 0
+    try:
+        with pytest.raises(B.PolyError) as e1:
+            B.poly_act_fwd(B.POLY_SIGMOID, dt, xb, y, n)
+        assert e1.value.status == B.POLY_ECUDA and "cudaError 701" in str(e1.value)
+        assert B.lib().poly_last_cuda_error() == 701
+        with pytest.raises(B.PolyError) as e2:
+            B.poly_swiglu_fwd(dt, g, u, ys)
+        assert e2.value.status == B.POLY_ECUDA
+    finally:
+        assert B.poly_debug_fail_launches(701, 0) == 0        # both consumed
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(buf), before)
+    assert np.array_equal(from_dev(ys), np.full(8 * 64, 0x1234, np.uint16).reshape(8, 64))
+    B.poly_act_fwd(B.POLY_SIGMOID, dt, xb, y, n)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(y), forward(oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt), x))
+    assert guards_intact(buf, n, G, 0)
+
+
 @pytest.mark.parametrize("dt", DTS)
 def test_in_place(dt):
     fmt = FMT[dt]
