@@ -449,6 +449,22 @@ def softcap_extras(x, dy, y, n, stream, peak, alpha=30.0):
     return res
 
 
+_COPY_MS = {}
+
+
+def same_bytes_copy_ms(nbytes, dev, stream):
+    """Time of a plain device copy that reads and writes nbytes in total: the
+    attainable bandwidth at a kernel's own size (launch ramp and drain keep a
+    ~50-100 us kernel below the long-copy peak)."""
+    import torch
+    if nbytes not in _COPY_MS:
+        src = torch.empty(nbytes // 4, dtype=torch.int16, device=dev).random_(-30000, 30000)
+        dst = torch.empty_like(src)
+        _COPY_MS[nbytes] = _time(lambda: dst.copy_(src), stream, 20)
+        del src, dst
+    return _COPY_MS[nbytes]
+
+
 def exp2_extras(dev, stream, peak, n=1 << 27):
     """2^x on FP32 tensors of 2^27 elements (512 MiB each, larger than L2)
     through each fractional core and the MUFU control (Appendix B.1)."""
@@ -463,7 +479,8 @@ def exp2_extras(dev, stream, peak, n=1 << 27):
                       ("D3", lambda: B.poly_exp2(B.POLY_EXP2_D3, x, y)),
                       ("mufu_ex2", lambda: B.poly_ctrl_exp2(x, y))]:
         ms = _time(fn, stream, 20)
-        res[label] = {"ms": ms, "gbs": 8 * n / ms / 1e6, "frac": 8 * n / ms / 1e6 / peak}
+        res[label] = {"ms": ms, "gbs": 8 * n / ms / 1e6, "frac": 8 * n / ms / 1e6 / peak,
+                      "vs_same_bytes_copy": same_bytes_copy_ms(8 * n, dev, stream) / ms}
     return res
 
 
@@ -496,6 +513,11 @@ def rope_extras(dev, stream, peak, b=4, s=4096, hq=32, hkv=8, d=128):
     ]:
         ms = _time(fn, stream, 20)
         res[label] = {"us": ms * 1e3, "gbs": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak}
+    ms = same_bytes_copy_ms(nbytes, dev, stream)
+    res["same_bytes_copy"] = {"us": ms * 1e3, "gbs": nbytes / ms / 1e6,
+                              "frac": nbytes / ms / 1e6 / peak}
+    for label in ("poly_fwd", "mufu_fwd", "table_fwd", "poly_bwd"):
+        res[label]["vs_same_bytes_copy"] = ms * 1e3 / res[label]["us"]
     return res
 
 
@@ -520,7 +542,8 @@ def swiglu_extras(args, dev, stream, peak):
     ]:
         ms = _time(fn, stream, reps)
         out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
-                      "frac": nbytes * n / ms / 1e6 / peak}
+                      "frac": nbytes * n / ms / 1e6 / peak,
+                      "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
     # the paper's deployed B1/B4 rule: sigmoid program recomputed
     B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
     try:
@@ -530,7 +553,8 @@ def swiglu_extras(args, dev, stream, peak):
         ]:
             ms = _time(fn, stream, reps)
             out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
-                          "frac": nbytes * n / ms / 1e6 / peak}
+                          "frac": nbytes * n / ms / 1e6 / peak,
+                          "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
     finally:
         B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
     del gd, ud, dyd, y, dg, du
@@ -546,7 +570,8 @@ def swiglu_extras(args, dev, stream, peak):
     ]:
         ms = _time(fn, stream, reps)
         out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
-                      "frac": nbytes * n / ms / 1e6 / peak}
+                      "frac": nbytes * n / ms / 1e6 / peak,
+                      "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
     out["config"] = {"dense": "BF16 [8192 x 14336], gate/up 2 N(0,1), dy N(0,1)",
                      "ragged": "BF16 131,072 x 2048 rows from 64 Zipf(1.1) segments, N(0,1.5^2)"}
     return out
