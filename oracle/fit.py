@@ -28,8 +28,8 @@ Readings where the paper is silent (each also listed in the design notes):
   functions monotone on t >= 0, a monotone real-arithmetic replay along the
   grid (rounded coefficients, clamp applied, no intermediate rounding).
 * Every gated candidate is replayed again in deployed order and the smallest
-  deployed-order error wins; ties go to the smaller split-order error, then
-  the smaller Li, then the smaller Lc.  (With this reading the D4 centred
+  deployed-order error wins; exact ties go to the smaller Table 2 metric,
+  then the smaller Li, then the smaller Lc.  (With this reading the D4 centred
   sigmoid of Figure 2 lands on the paper's Li = 5.0, with the error of the
   printed (5.0, 5.28125) configuration.)
 * The stated error bound is the maximum over every finite target-format input
@@ -141,13 +141,13 @@ def search(fn: int, direction: int, fmt: str, degree: int,
     emulator) and gated; the gated candidates are replayed again in the
     deployed fused order, and the accepted program is the one with the
     smallest deployed-order error ("final selection replays the deployed
-    packed-FMA order"); ties go to the smaller split-order error, then the
-    smaller Li, then the smaller Lc.  top_k > 0 restricts the deployed replay
-    to the top_k candidates by split-order error.  lc_refine_ulps = k > 0
-    also replays each such candidate with its clamp moved by 1..k
-    target-format ulps either way (Figure 2's selected clamp 5.28125 is one
-    BF16 ulp above the grid value 5.25); offsets are taken in the order
-    0, -1, +1, -2, +2, ... and only a strictly smaller error replaces."""
+    packed-FMA order"); exact ties go to the smaller Table 2 metric, then
+    the smaller Li, then the smaller Lc.  Ranks are positions by split-order
+    error (ties: smaller Li, then smaller Lc); top_k > 0 restricts the
+    deployed replay to the top_k of them.  lc_refine_ulps = k > 0 also
+    replays each such candidate with its clamp moved by 1..k target-format
+    ulps either way (Figure 2's selected clamp 5.28125 is one BF16 ulp above
+    the grid value 5.25)."""
     if li_grid is None:
         li_grid = [1.0 + 0.25 * i for i in range(45)]
     x = score_grid(fmt)
@@ -174,30 +174,37 @@ def search(fn: int, direction: int, fmt: str, degree: int,
     by_li = {}
     for rank, (split_err, li, lc, cb) in enumerate(finalists):
         by_li.setdefault(li, []).append((rank, split_err, lc, cb))
-    best = None
+    passed = []           # (deployed_err, rank, split_err, li, lc, cb) of every gated trial
     for li, group in by_li.items():
         cb = group[0][3]
         rows = []
         for rank, split_err, lc0, _ in group:
-            for oi, off in enumerate(offsets):
+            for off in offsets:
                 lcb = int(tf.from_f64(lc0, fmt)) + off
+                if lcb <= 0:
+                    continue
                 lc = float(tf.decode(np.uint16(lcb), fmt))
                 if 0.0 < lc <= li + 1.0:
-                    rows.append((rank, oi, split_err, lc, lcb))
-        lcb = np.array([r[4] for r in rows], dtype=np.uint16)[:, None]
-        lcv = np.array([r[3] for r in rows])[:, None]
+                    rows.append((rank, split_err, lc, lcb))
+        lcb = np.array([r[3] for r in rows], dtype=np.uint16)[:, None]
+        lcv = np.array([r[2] for r in rows])[:, None]
         y = evaluate(form, tuple(cb), lcb, x, fmt, fused=True)
         ok = _gates(fn, direction, y, fmt, cb, lcv, x)
         err = np.max(np.abs(tf.decode(y, fmt) - truth), axis=-1)
-        for (rank, oi, split_err, lc, _), e, g in zip(rows, err, ok):
-            if not g:
-                continue
-            key = (float(e), rank, oi)
-            if best is None or key < best[0]:
-                best = (key, split_err, li, lc, cb)
-    if best is None:
+        for (rank, split_err, lc, _), e, g in zip(rows, err, ok):
+            if g:
+                passed.append((float(e), rank, split_err, li, lc, cb))
+    if not passed:
         return None
-    (err, rank, _), split_err, li, lc, cb = best
+    # smallest deployed-order error; exact ties go to the smaller Table 2
+    # metric (real arithmetic over [-Lc, Lc]), then the smaller Li, then Lc
+    err = min(c[0] for c in passed)
+    tied = [c for c in passed if c[0] == err]
+    if len(tied) > 1:
+        def t2(c):
+            return table2_metric(make_program(fn, direction, fmt, degree, c[3], c[4], c[5]))
+        tied.sort(key=lambda c: (t2(c), c[3], c[4]))
+    _, rank, split_err, li, lc, cb = tied[0]
     prog = make_program(fn, direction, fmt, degree, li, lc, cb)
     bound, at = exhaustive_error(prog)
     prog.info = {"search_score": split_err, "deployed_score": err, "rank": rank,

@@ -16,8 +16,8 @@
 // linspace(0, 12, 8000) rounded to the format; gates = finite outputs, exact
 // P(0) = f(0), output range for sigmoid / tanh / sigma' / tanh', and a
 // monotone real-arithmetic replay for functions monotone on t >= 0; every
-// gated candidate is re-scored in deployed order (ties to the smaller split
-// error, then the smaller Li, then the smaller Lc).
+// gated candidate is re-scored in deployed order (exact ties to the smaller
+// Table 2 metric, then the smaller Li, then the smaller Lc).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -418,8 +418,6 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
   });
   // deployed-order replay of the finalists (all gated candidates when top_k
   // is 0), each clamp also moved by 1..lc_refine_ulps format ulps either way
-  // in the order 0, -1, +1, -2, +2, ...; the smallest deployed-order error
-  // wins, ties to the better split rank, then the earlier offset
   const int k = o.top_k > 0 ? std::min<int>(o.top_k, (int)cands.size()) : (int)cands.size();
   std::vector<int> offsets{0};
   for (int j = 1; j <= o.lc_refine_ulps; ++j) {
@@ -428,7 +426,7 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
   }
   const uint32_t inf_bits = dtype == POLY_F16 ? 0x7C00u : 0x7F80u;
   struct Trial {
-    int rank, off_idx;
+    int rank;
     uint16_t lcb;
     double lc, err;
     bool ok;
@@ -441,7 +439,7 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
       if (b <= 0 || (uint32_t)b >= inf_bits) continue;
       const double lc = to_double((uint16_t)b, dtype);
       if (!(lc > 0.0 && lc <= cands[r].li + 1.0)) continue;
-      trials.push_back(Trial{r, (int)oi, (uint16_t)b, lc, 0.0, false});
+      trials.push_back(Trial{r, (uint16_t)b, lc, 0.0, false});
     }
   }
   auto deployed = [&](size_t first, size_t stride) {
@@ -468,18 +466,29 @@ int fit_program(int fn, int dir, int dtype, int degree, const poly_fit_opts &o,
     for (unsigned t = 0; t < nth2; ++t) pool.emplace_back(deployed, (size_t)t, (size_t)nth2);
     for (auto &th : pool) th.join();
   }
+  // smallest deployed-order error; exact ties go to the smaller Table 2
+  // metric (real arithmetic over [-Lc, Lc]), then the smaller Li, then Lc
   int bt = -1;
-  for (int t = 0; t < (int)trials.size(); ++t) {
-    const Trial &tr = trials[t];
-    if (!tr.ok) continue;
-    if (bt < 0) {
-      bt = t;
-      continue;
+  for (int t = 0; t < (int)trials.size(); ++t)
+    if (trials[t].ok && (bt < 0 || trials[t].err < trials[bt].err)) bt = t;
+  if (bt >= 0) {
+    std::vector<int> tied;
+    for (int t = 0; t < (int)trials.size(); ++t)
+      if (trials[t].ok && trials[t].err == trials[bt].err) tied.push_back(t);
+    if (tied.size() > 1) {
+      double bt2 = 0;
+      bt = -1;
+      for (int t : tied) {
+        const Cand &c = cands[trials[t].rank];
+        const double t2 = table2_metric(fn, dir, dtype, form, degree, c.coef, trials[t].lc);
+        if (bt < 0 || t2 < bt2 ||
+            (t2 == bt2 && (c.li < cands[trials[bt].rank].li ||
+                           (c.li == cands[trials[bt].rank].li && trials[t].lc < trials[bt].lc)))) {
+          bt = t;
+          bt2 = t2;
+        }
+      }
     }
-    const Trial &b = trials[bt];
-    if (tr.err < b.err || (tr.err == b.err && (tr.rank < b.rank ||
-                                               (tr.rank == b.rank && tr.off_idx < b.off_idx))))
-      bt = t;
   }
   const int best = bt < 0 ? -1 : trials[bt].rank;
   const double best_err = bt < 0 ? 0.0 : trials[bt].err;

@@ -124,7 +124,8 @@ def test_figure2_configuration_is_reproduced():
     selected (Li, Lc) = (5.0, 5.28125) (Fig. 2b) and on a clamp one BF16 ulp
     below it (the printed Lc is off the 0.25 grid), with exactly the same
     maximum error over every finite BF16 input; allowing the clamp to move by
-    one ulp does not find a better program."""
+    one ulp finds no better program (the three clamps tie in deployed order,
+    and the Table 2 tie-break takes one of them)."""
     with open(os.path.join(GOLDEN, "figure2_selected.txt")) as f:
         name, d, D, li, lc = [l for l in f if not l.startswith("#")][0].split()
     li, lc, D = float(li), float(lc), int(D)
@@ -136,7 +137,8 @@ def test_figure2_configuration_is_reproduced():
     assert ours.li == li and int(ours.lc_bits) == int(tf.from_f64(lc, "bf16")) - 1
     assert err_fig2 == ours.info["stated_max_abs_err"] < 6e-3
     refined = fit.search(ref.SIGMOID, ref.FWD, "bf16", D, lc_refine_ulps=1)
-    assert (refined.li, refined.lc) == (ours.li, ours.lc)
+    assert refined.li == li and abs(int(refined.lc_bits) - int(ours.lc_bits)) <= 1
+    assert refined.info["deployed_score"] == ours.info["deployed_score"]
 
 
 def test_top_k_restricts_the_deployed_replay():
