@@ -149,6 +149,22 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def environment(dev):
+    """GPU, driver and software the numbers were taken with."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    env = {"gpu": props.name, "sms": props.multi_processor_count,
+           "hbm_gib": round(props.total_memory / 2 ** 30, 1), "cuda_runtime": torch.version.cuda,
+           "torch": torch.__version__, "host_cores": os.cpu_count()}
+    try:
+        r = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=driver_version",
+                            "--format=csv,noheader"], capture_output=True, text=True, timeout=30)
+        env["driver"] = r.stdout.strip() or None
+    except (OSError, subprocess.TimeoutExpired):
+        env["driver"] = None
+    return env
+
+
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -335,7 +351,7 @@ def main():
                          "l2": "inputs (512 MiB per tensor) larger than L2; no flush",
                          "parallelism": f"replicas x{world}, no collective"},
               "gpu_launches": len(SIX) * args.steps,
-              "clocks": clk}
+              "clocks": clk, "env": environment(dev)}
 
     # ---- per program: poly vs MUFU control vs torch native
     for _ in range(args.warmup):

@@ -21,6 +21,7 @@ POLY_OK, POLY_EINVAL, POLY_ENOPROG, POLY_ECUDA, POLY_ENOFIT = 0, -1, -2, -3, -4
 POLY_MAX_DEGREE = 6
 POLY_PROGRAM_VERSION = 1
 FN = {"sigmoid": POLY_SIGMOID, "tanh": POLY_TANH, "silu": POLY_SILU, "gelu": POLY_GELU}
+FN_NAMES = {v: k for k, v in FN.items()}
 
 # version of include/polyact.h this binding marshals for (poly_abi_version)
 ABI_VERSION = 2
