@@ -388,7 +388,7 @@ def main():
     name, d, D = SIX[dom]
     kkey = f"{name}.{'bwd' if d else 'fwd'}.D{D}"
     ach = BYTES[d] * n / (per_ms[dom] * 1e-3) / 1e9
-    result["roofline"] = {"kernel": f"stream_kernel<OpBwd|OpFwd> {kkey}", "bound": "hbm",
+    result["roofline"] = {"kernel": f"dense_kernel<OpBwd|OpFwd> {kkey}", "bound": "hbm",
                           "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                           "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                           "algorithmic_bytes_per_launch": BYTES[d] * n,

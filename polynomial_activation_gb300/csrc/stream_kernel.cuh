@@ -9,6 +9,10 @@
 //    chunks per stream per thread;
 //  * a one-pass grid: every thread owns its chunks, blocks retire and are
 //    replaced as fast as the memory system drains them;
+//  * a dense kernel for the common case (flat, every stream 16-byte aligned,
+//    fewer than 2^31 elements) with 32-bit indices and no layout branches,
+//    which cuts the per-thread instruction count that dominates launches of
+//    L2-resident size;
 //  * a scalar head (up to the first 16-byte boundary) and tail, evaluated
 //    with the same packed instructions on one lane so that every element
 //    gets bit-identical arithmetic; streams whose addresses disagree modulo
@@ -168,6 +172,49 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
   }
 }
 
+// Dense: the flat layout when every stream starts on a 16-byte boundary and
+// n < 2^31 -- the common case -- with 32-bit indices, no layout branches and
+// no loop: the grid covers the body exactly once, and the last block also
+// evaluates the n mod 8 tail elements.
+template <class Op>
+__global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nvec,
+                                                         uint32_t ntail,
+                                                         typename Op::Params p) {
+  pdl_enter();
+  constexpr int U = chunks_per_thread<Op>();
+  const uint16_t *src[3] = {s.in0, s.in1, s.in2};
+  uint16_t *dst[2] = {s.out0, s.out1};
+  const uint32_t base = blockIdx.x * (uint32_t)(kThreads * U) + threadIdx.x;
+  uint4 r[U][Op::NIN];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t i = base + u * kThreads;
+    if (i < nvec) {
+#pragma unroll
+      for (int k = 0; k < Op::NIN; ++k) r[u][k] = ld_stream(src[k] + (size_t)i * 8);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t i = base + u * kThreads;
+    if (i < nvec) {
+      uint4 o[Op::NOUT];
+      apply_chunk<Op>(r[u], o, p);
+#pragma unroll
+      for (int k = 0; k < Op::NOUT; ++k) st_stream(dst[k] + (size_t)i * 8, o[k]);
+    }
+  }
+  if (ntail != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x < ntail) {
+    const uint16_t *in[Op::NIN];
+    uint16_t *out[Op::NOUT];
+#pragma unroll
+    for (int k = 0; k < Op::NIN; ++k) in[k] = src[k];
+#pragma unroll
+    for (int k = 0; k < Op::NOUT; ++k) out[k] = dst[k];
+    apply_one<Op>(in, out, (int64_t)nvec * 8 + threadIdx.x, p);
+  }
+}
+
 // Strided: rows x cols with a leading dimension per stream (a separate
 // kernel so that its index arithmetic does not weigh on the flat path).
 template <class Op>
@@ -231,6 +278,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Every stream of s starts on a 16-byte boundary (unused streams are null).
+inline bool aligned16(const Streams &s) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(s.in0) | reinterpret_cast<uintptr_t>(s.in1) |
+                      reinterpret_cast<uintptr_t>(s.in2) | reinterpret_cast<uintptr_t>(s.out0) |
+                      reinterpret_cast<uintptr_t>(s.out1);
+  return (a & 15u) == 0;
+}
+
 // Launch an op on a flat / ragged layout (every op) or, when the op allows
 // it (TWO_D), on a strided one.
 template <class Op>
@@ -243,6 +298,14 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     }
   }
   if (l.mode == kStrided) return cudaErrorInvalidValue;
+  if (l.mode == kFlat && l.n < (int64_t(1) << 31) && aligned16(s)) {
+    const int64_t per_block = (int64_t)kThreads * 8 * chunks_per_thread<Op>();
+    const int64_t nvec = l.n >> 3;
+    int64_t blocks = (nvec * 8 + per_block - 1) / per_block;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(dense_kernel<Op>, blocks, kThreads, stream, s, (uint32_t)nvec,
+                      (uint32_t)(l.n & 7), p);
+  }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);
 }

@@ -235,6 +235,32 @@ def _equal_bits(got, want):
     return bool(torch.equal(g[~nan], w[~nan])) and bool(torch.isnan(got.float()[nan]).all())
 
 
+@pytest.mark.parametrize("n", [(1 << 31) - 3, (1 << 31) + 13])
+def test_index_width_limits(n):
+    """Just below 2^31 elements (the dense kernel's 32-bit indices at their
+    limit) and just above (the general kernel's 64-bit path): x cycles
+    through all 65,536 FP16 patterns, so every element must equal the
+    oracle's exhaustive table at x mod 65,536 (checked in slices of 2^28)."""
+    dt = B.POLY_F16
+    op = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    lut = _lut(op)                                   # int16 [65536] on the device
+    pat = torch.from_numpy(X_ALL.view(np.int16)).to(DEV)
+    x = torch.empty(n, dtype=torch.int16, device=DEV)
+    full = n // 65536
+    x[:full * 65536].view(full, 65536).copy_(pat.expand(full, 65536))
+    x[full * 65536:] = pat[:n - full * 65536]
+    y = torch.empty_like(x)
+    B.poly_act_fwd(B.POLY_SIGMOID, dt, x.view(torch.float16), y.view(torch.float16), n)
+    torch.cuda.synchronize()
+    rows = 1 << 12                                   # 2^12 x 65,536 = 2^28 elements per slice
+    for r0 in range(0, full, rows):
+        r1 = min(full, r0 + rows)
+        got = y[r0 * 65536:r1 * 65536].view(r1 - r0, 65536)
+        assert bool((got == lut[None, :]).all()), (n, r0)
+    assert torch.equal(y[full * 65536:], lut[:n - full * 65536])
+    del x, y
+
+
 def test_hbm_resident_sweep_full_size():
     """268,435,456 FP16 elements (512 MiB per tensor), 1 % outliers in
     [-40, 40].  Forward: every element equals the oracle's exhaustive table
