@@ -9,8 +9,9 @@
 //    chunks per stream per thread;
 //  * a one-pass grid: every thread owns its chunks, blocks retire and are
 //    replaced as fast as the memory system drains them;
-//  * a dense kernel for the common case (flat, every stream 16-byte aligned,
-//    fewer than 2^31 elements) with 32-bit indices and no layout branches,
+//  * a dense kernel for the common cases (flat, or ragged rows of a multiple
+//    of 8 columns; every stream 16-byte aligned; fewer than 2^31 elements)
+//    with 32-bit indices and no layout branches,
 //    which cuts the per-thread instruction count that dominates launches of
 //    L2-resident size;
 //  * a scalar head (up to the first 16-byte boundary) and tail, evaluated
@@ -98,6 +99,27 @@ __device__ __forceinline__ void apply_one(const uint16_t *const *in, uint16_t *c
   for (int k = 0; k < Op::NOUT; ++k) out[k][e] = (uint16_t)(b[k] & 0xFFFFu);
 }
 
+// Row range [lo, hi) of a ragged call: rows [seg[0], seg[nseg]) clamped to
+// [0, cap_rows] whatever the offsets say.  If status is given, block 0 also
+// records whether the offsets were valid (seg[0] == 0, non-decreasing,
+// seg[nseg] <= cap_rows): 0 valid, 1 not.  Every thread of block 0 must call
+// this (it synchronises the block).
+__device__ __forceinline__ void ragged_rows(const int32_t *seg, int32_t nseg, int64_t cap_rows,
+                                            int32_t *status, int64_t &lo, int64_t &hi) {
+  lo = seg[0];
+  hi = seg[nseg];
+  if (lo < 0) lo = 0;
+  if (hi > cap_rows) hi = cap_rows;
+  if (hi < lo) hi = lo;
+  if (status != nullptr && blockIdx.x == 0) {
+    int bad = 0;
+    for (int e = threadIdx.x; e < nseg; e += blockDim.x) bad |= seg[e] > seg[e + 1];
+    if (threadIdx.x == 0) bad |= (seg[0] != 0) | (seg[nseg] > cap_rows);
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) *status = bad ? 1 : 0;
+  }
+}
+
 // Flat / ragged: one contiguous range of elements.  When every stream sits at
 // the same address modulo 16 (l.vec), the scalar head runs up to the first
 // 16-byte boundary and the body moves 16-byte chunks; otherwise every
@@ -109,19 +131,10 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
   constexpr int U = chunks_per_thread<Op>();
   int64_t n = l.n, off = 0;
   if (l.mode == kRagged) {
-    int64_t lo = l.seg[0], hi = l.seg[l.nseg];
-    if (lo < 0) lo = 0;
-    if (hi > l.cap_rows) hi = l.cap_rows;
-    if (hi < lo) hi = lo;
+    int64_t lo, hi;
+    ragged_rows(l.seg, l.nseg, l.cap_rows, l.status, lo, hi);
     off = lo * l.cols;
     n = (hi - lo) * l.cols;
-    if (l.status != nullptr && blockIdx.x == 0) {
-      int bad = 0;
-      for (int e = threadIdx.x; e < l.nseg; e += blockDim.x) bad |= l.seg[e] > l.seg[e + 1];
-      if (threadIdx.x == 0) bad |= (l.seg[0] != 0) | (l.seg[l.nseg] > l.cap_rows);
-      bad = __syncthreads_or(bad);
-      if (threadIdx.x == 0) *l.status = bad ? 1 : 0;
-    }
   }
   const uint16_t *in[Op::NIN];
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
@@ -175,15 +188,36 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
 // Dense: the flat layout when every stream starts on a 16-byte boundary and
 // n < 2^31 -- the common case -- with 32-bit indices, no layout branches and
 // no loop: the grid covers the body exactly once, and the last block also
-// evaluates the n mod 8 tail elements.
-template <class Op>
+// evaluates the n mod 8 tail elements.  With RAGGED the range is the rows
+// read from the device offsets (cols % 8 == 0 and cap_rows * cols < 2^31, so
+// every row starts on a 16-byte boundary and there is no tail); the grid
+// covers cap_rows and blocks past the last row only return.
+struct DenseRagged {
+  const int32_t *seg;
+  int32_t nseg;
+  int32_t cap_rows;
+  uint32_t cols;
+  int32_t *status;
+};
+
+template <class Op, bool RAGGED>
 __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nvec,
-                                                         uint32_t ntail,
+                                                         uint32_t ntail, DenseRagged g,
                                                          typename Op::Params p) {
   pdl_enter();
   constexpr int U = chunks_per_thread<Op>();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
+  if constexpr (RAGGED) {
+    int64_t lo, hi;
+    ragged_rows(g.seg, g.nseg, g.cap_rows, g.status, lo, hi);
+    const size_t off = (size_t)lo * g.cols;
+#pragma unroll
+    for (int k = 0; k < Op::NIN; ++k) src[k] += off;
+#pragma unroll
+    for (int k = 0; k < Op::NOUT; ++k) dst[k] += off;
+    nvec = (uint32_t)(((uint64_t)(hi - lo) * g.cols) >> 3);
+  }
   const uint32_t base = blockIdx.x * (uint32_t)(kThreads * U) + threadIdx.x;
   uint4 r[U][Op::NIN];
 #pragma unroll
@@ -204,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nve
       for (int k = 0; k < Op::NOUT; ++k) st_stream(dst[k] + (size_t)i * 8, o[k]);
     }
   }
-  if (ntail != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x < ntail) {
+  if (!RAGGED && ntail != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x < ntail) {
     const uint16_t *in[Op::NIN];
     uint16_t *out[Op::NOUT];
 #pragma unroll
@@ -298,13 +332,20 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     }
   }
   if (l.mode == kStrided) return cudaErrorInvalidValue;
+  const int64_t per_block = (int64_t)kThreads * 8 * chunks_per_thread<Op>();
   if (l.mode == kFlat && l.n < (int64_t(1) << 31) && aligned16(s)) {
-    const int64_t per_block = (int64_t)kThreads * 8 * chunks_per_thread<Op>();
     const int64_t nvec = l.n >> 3;
     int64_t blocks = (nvec * 8 + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(dense_kernel<Op>, blocks, kThreads, stream, s, (uint32_t)nvec,
-                      (uint32_t)(l.n & 7), p);
+    return launch_pdl(dense_kernel<Op, false>, blocks, kThreads, stream, s, (uint32_t)nvec,
+                      (uint32_t)(l.n & 7), DenseRagged{}, p);
+  }
+  if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < (int64_t(1) << 31) &&
+      aligned16(s)) {
+    const DenseRagged g{l.seg, l.nseg, (int32_t)l.cap_rows, (uint32_t)l.cols, l.status};
+    int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(dense_kernel<Op, true>, blocks, kThreads, stream, s, 0u, 0u, g, p);
   }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);

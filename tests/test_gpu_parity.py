@@ -415,12 +415,15 @@ def test_ragged_swiglu_full_size_sampled():
     assert _equal_bits(du[:rows], _rn_mul(dys, sg))
 
 
+@pytest.mark.parametrize("cols", [24, 21])
 @pytest.mark.parametrize("dt", DTS)
-def test_ragged_small_every_element_and_status(dt):
+def test_ragged_small_every_element_and_status(dt, cols):
+    """cols = 24: the dense kernel's ragged mode (rows start on 16-byte
+    boundaries); cols = 21: the general kernel (scalar head and tail)."""
     fmt = FMT[dt]
     s_op, d_op = _swiglu_ops(dt)
     rng = np.random.default_rng(51)
-    cols, cap = 24, 50
+    cap = 50
     seg = np.array([0, 3, 3, 10, 31, 40], dtype=np.int32)
     g = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
     u = _rand_bits(rng, cap * cols, fmt).reshape(cap, cols)
@@ -441,6 +444,14 @@ def test_ragged_small_every_element_and_status(dt):
     B.poly_swiglu_fwd_ragged(dt, gd, ud, y2, over, status=status)
     assert int(status.item()) == 1
     assert np.array_equal(from_dev(y2).reshape(cap, cols), swiglu_forward(s_op, g, u))
+    # first offset above 0: rows [2, 40) are processed, rows before and after untouched, status 1
+    late = torch.from_numpy(np.array([2, 3, 3, 10, 31, 40], dtype=np.int32)).to(DEV)
+    y3 = torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    B.poly_swiglu_fwd_ragged(dt, gd, ud, y3, late, status=status)
+    assert int(status.item()) == 1
+    got3 = from_dev(y3).reshape(cap, cols)
+    assert np.array_equal(got3[2:40], swiglu_forward(s_op, g[2:40], u[2:40]))
+    assert np.all(got3[:2] == 0x5A5A) and np.all(got3[40:] == 0x5A5A)
 
 
 # ---------------------------------------------------------------- controls
