@@ -16,6 +16,7 @@
 
 #include "launch.h"
 #include "packed.cuh"
+#include "stream_kernel.cuh"
 
 namespace polyact {
 namespace dev {
@@ -74,6 +75,7 @@ template <int CORE>
 __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restrict__ x,
                                                            float *__restrict__ y, int64_t n,
                                                            int vec, Exp2Params p) {
+  pdl_enter();
   int64_t head = n;
   if (vec) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(x);
@@ -125,8 +127,7 @@ static cudaError_t go(const float *x, float *y, int64_t n, int vec, const Exp2Pa
   int64_t blocks = (n + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
   if (blocks < 1) blocks = 1;
-  exp2_kernel<CORE><<<(unsigned)blocks, kExp2Threads, 0, st>>>(x, y, n, vec, p);
-  return cudaGetLastError();
+  return launch_pdl(exp2_kernel<CORE>, blocks, kExp2Threads, st, x, y, n, vec, p);
 }
 
 }  // namespace dev

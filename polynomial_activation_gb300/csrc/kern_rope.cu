@@ -25,6 +25,7 @@
 
 #include "launch.h"
 #include "packed.cuh"
+#include "stream_kernel.cuh"
 
 namespace polyact {
 namespace dev {
@@ -109,6 +110,7 @@ __device__ __forceinline__ void st16(uint16_t *p, const uint4 &v) {
 
 template <int VARIANT, int INV>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeConsts k) {
+  pdl_enter();
   const int64_t groups = a.head_dim >> 3;                // chunks of 4 frequencies
   const int64_t H = a.hq + a.hkv;
   const int64_t hchunks = (H + kHeadsPerThread - 1) / kHeadsPerThread;
@@ -197,11 +199,8 @@ static cudaError_t rope_go(int inv, const RopeArgs &a, const RopeConsts &k, cuda
   int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
   if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
   if (blocks < 1) blocks = 1;
-  if (inv)
-    rope_kernel<VARIANT, 1><<<(unsigned)blocks, kRopeThreads, 0, st>>>(a, k);
-  else
-    rope_kernel<VARIANT, 0><<<(unsigned)blocks, kRopeThreads, 0, st>>>(a, k);
-  return cudaGetLastError();
+  if (inv) return launch_pdl(rope_kernel<VARIANT, 1>, blocks, kRopeThreads, st, a, k);
+  return launch_pdl(rope_kernel<VARIANT, 0>, blocks, kRopeThreads, st, a, k);
 }
 
 }  // namespace dev
