@@ -670,6 +670,27 @@ def test_exp2_cores_bit_exact(core):
     assert np.array_equal(y2[2:2 + x.size - 1].cpu().numpy().view(np.uint32), want[1:])
 
 
+@pytest.mark.parametrize("core", [B.POLY_EXP2_D1, B.POLY_EXP2_PWL2, B.POLY_EXP2_D2,
+                                  B.POLY_EXP2_D3])
+def test_exp2_full_size_sampled(core):
+    """2^27 FP32 elements, x ~ U[-60, 10] (the bench's case, 512 MiB per
+    tensor): 2^20 sampled outputs plus the first and last 4,096, element by
+    element against the oracle."""
+    from oracle import exp2 as e2
+    n = 1 << 27
+    x = np.random.default_rng(7).uniform(-60, 10, n).astype(np.float32)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.empty_like(xd)
+    B.poly_exp2(core, xd, y)
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([np.random.default_rng(8).integers(0, n, 1 << 20),
+                                    np.arange(4096), np.arange(n - 4096, n)]))
+    got = y[torch.from_numpy(idx).to(DEV)].cpu().numpy().view(np.uint32)
+    want = e2.exp2_replay(e2.VARIANTS[core], x[idx])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(x[idx[i]]), hex(got[i]), hex(want[i])) for i in bad[:6]]
+
+
 def test_exp2_mufu_control_accuracy():
     x = np.random.default_rng(43).uniform(-120, 120, 1 << 20).astype(np.float32)
     xd = torch.from_numpy(x).to(DEV)
