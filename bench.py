@@ -661,6 +661,18 @@ def l2_extras(dev, stream):
                     "poly_gbs": BYTES[d] * n / tp / 1e6}
     res["config"] = ("4,194,304 FP16 elements, x ~ N(0, 3^2), dy ~ N(0, 1); L2-resident by "
                      "design; every call replayed from a CUDA graph of 200 launches")
+    # launch time against size (sigmoid D3 forward and a plain copy, graph-replayed): the
+    # intercept is the fixed cost of a launch, the slope the L2 streaming rate
+    big = torch.empty(1 << 24, dtype=torch.float16, device=dev)
+    big[:n].copy_(x)
+    big[n:].copy_(x.repeat(3))
+    out = torch.empty_like(big)
+    curve = {}
+    for m in (8, 1 << 18, 1 << 20, 1 << 22, 1 << 23, 1 << 24):
+        tp = _time_graph(lambda: B.poly_act_fwd(FN["sigmoid"], B.POLY_F16, big, out, m), 200)
+        tc = _time_graph(lambda: out[:m].copy_(big[:m]), 200)
+        curve[str(m)] = {"poly_us": tp * 1e3, "copy_us": tc * 1e3, "poly_gbs": 4 * m / tp / 1e6}
+    res["size_curve_sigmoid_fwd"] = curve
     return res
 
 
