@@ -1,5 +1,7 @@
 // kern_common.cu -- launch sizing and the dispatch from the C ABI layer to
 // the per-family translation units.
+#include <atomic>
+
 #include "poly_ops.cuh"
 
 namespace polyact {
@@ -9,6 +11,19 @@ cudaError_t launch_act(int kind, int dtype, int form, int deg, const Streams &s,
                        const Layout &l, const ProgPair &p, cudaStream_t st);
 cudaError_t launch_swiglu(int kind, int variant, int dtype, int ds, int dd, const Streams &s,
                           const Layout &l, const ProgPair &p, cudaStream_t st);
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
 
 int64_t grid_for(const Layout &l, int per_thread) {
   int64_t work;

@@ -65,11 +65,15 @@ __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
 
 // Chunks of 8 elements per stream per thread: two for single-input
 // operations, one for multi-input ones (measured on GB300 with a one-pass
-// grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes).
+// grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes).  A
+// single-input call too small to give every SM four blocks of two-chunk
+// threads takes one chunk per thread instead (dense kernel only): at 0.5-2 M
+// elements that keeps twice as many warps issuing loads.
 template <class Op>
 __host__ __device__ constexpr int chunks_per_thread() {
   return Op::NIN == 1 ? 2 : 1;
 }
+constexpr int kMinBlocksPerSm = 4;
 
 template <class Op>
 __device__ __forceinline__ void apply_chunk(const uint4 (&in)[Op::NIN], uint4 (&out)[Op::NOUT],
@@ -200,12 +204,11 @@ struct DenseRagged {
   int32_t *status;
 };
 
-template <class Op, bool RAGGED>
+template <class Op, bool RAGGED, int U>
 __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nvec,
                                                          uint32_t ntail, DenseRagged g,
                                                          typename Op::Params p) {
   pdl_enter();
-  constexpr int U = chunks_per_thread<Op>();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
   if constexpr (RAGGED) {
@@ -294,6 +297,8 @@ __global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
 // in one pass (measured on GB300: a one-pass grid streams 8-10 % faster than
 // a persistent grid striding over the tensor).
 int64_t grid_for(const Layout &l, int per_thread);
+// Streaming multiprocessors of the calling thread's current device (cached).
+int sm_count();
 
 // Launch with the programmatic-stream-serialisation attribute (see pdl_enter).
 template <typename... KArgs, typename... Args>
@@ -332,12 +337,21 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     }
   }
   if (l.mode == kStrided) return cudaErrorInvalidValue;
-  const int64_t per_block = (int64_t)kThreads * 8 * chunks_per_thread<Op>();
+  constexpr int U = chunks_per_thread<Op>();
+  const int64_t per_block = (int64_t)kThreads * 8 * U;
   if (l.mode == kFlat && l.n < (int64_t(1) << 31) && aligned16(s)) {
     const int64_t nvec = l.n >> 3;
     int64_t blocks = (nvec * 8 + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(dense_kernel<Op, false>, blocks, kThreads, stream, s, (uint32_t)nvec,
+    if constexpr (U > 1) {
+      if (blocks < (int64_t)kMinBlocksPerSm * sm_count()) {
+        blocks = (nvec + kThreads - 1) / kThreads;
+        if (blocks < 1) blocks = 1;
+        return launch_pdl(dense_kernel<Op, false, 1>, blocks, kThreads, stream, s,
+                          (uint32_t)nvec, (uint32_t)(l.n & 7), DenseRagged{}, p);
+      }
+    }
+    return launch_pdl(dense_kernel<Op, false, U>, blocks, kThreads, stream, s, (uint32_t)nvec,
                       (uint32_t)(l.n & 7), DenseRagged{}, p);
   }
   if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < (int64_t(1) << 31) &&
@@ -345,7 +359,7 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     const DenseRagged g{l.seg, l.nseg, (int32_t)l.cap_rows, (uint32_t)l.cols, l.status};
     int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(dense_kernel<Op, true>, blocks, kThreads, stream, s, 0u, 0u, g, p);
+    return launch_pdl(dense_kernel<Op, true, U>, blocks, kThreads, stream, s, 0u, 0u, g, p);
   }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);
