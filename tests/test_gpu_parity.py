@@ -790,6 +790,64 @@ def test_rope_full_size_sampled():
         assert np.array_equal(from_dev(ko[bb, :, ss, :]), rope.rotate(xk, cs[ss][None, :], sn[ss][None, :]))
 
 
+# ------------------------------------------------------- graphs and streams
+
+def test_cuda_graph_capture_and_replay():
+    """Calls captured into a CUDA graph (the launches, with programmatic
+    dependent launch, become graph nodes) replay to exactly the oracle's
+    values, also after the inputs are rewritten in place."""
+    dt, fmt = B.POLY_F16, "f16"
+    n = 1_000_003
+    rng = np.random.default_rng(61)
+    x0, x1 = _rand_bits(rng, n, fmt), _rand_bits(rng, n, fmt)
+    dy = _rand_bits(rng, n, fmt)
+    xd, dyd = to_dev(x0, dt), to_dev(dy, dt)
+    y1, y2 = torch.empty_like(xd), torch.empty_like(xd)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                    # warm-up (program fits) outside capture
+        B.poly_act_fwd(B.POLY_GELU, dt, xd, y1, n)
+        B.poly_act_bwd(B.POLY_TANH, dt, xd, dyd, y2, n)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.poly_act_fwd(B.POLY_GELU, dt, xd, y1, n)
+        B.poly_act_bwd(B.POLY_TANH, dt, xd, dyd, y2, n)
+    gelu = oracle_program(B.POLY_GELU, B.POLY_FWD, dt)
+    tanh_d = oracle_program(B.POLY_TANH, B.POLY_BWD, dt)
+    for x in (x0, x1):
+        xd.copy_(to_dev(x, dt))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(from_dev(y1), forward(gelu, x))
+        assert np.array_equal(from_dev(y2), backward(tanh_d, x, dy))
+
+
+def test_concurrent_streams():
+    """Different programs launched on two streams at once each produce the
+    oracle's values (kernels carry their program as a parameter; nothing is
+    shared between launches)."""
+    dt, fmt = B.POLY_BF16, "bf16"
+    n = 3_000_017
+    rng = np.random.default_rng(62)
+    xa, xb = _rand_bits(rng, n, fmt), _rand_bits(rng, n, fmt)
+    da, db = to_dev(xa, dt), to_dev(xb, dt)
+    ya, yb = torch.empty_like(da), torch.empty_like(db)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    B.poly_get_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    B.poly_get_program(B.POLY_SILU, B.POLY_FWD, dt)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            B.poly_act_fwd(B.POLY_SIGMOID, dt, da, ya, n)
+        with torch.cuda.stream(sb):
+            B.poly_act_fwd(B.POLY_SILU, dt, db, yb, n)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(ya), forward(oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt), xa))
+    assert np.array_equal(from_dev(yb), forward(oracle_program(B.POLY_SILU, B.POLY_FWD, dt), xb))
+
+
 # ------------------------------------------------------------------ autograd
 
 def test_autograd_wrappers_match_direct_calls():
