@@ -30,6 +30,9 @@
  *   16-byte-aligned data takes the 128-bit vector path, a scalar head and
  *   tail cover the rest.  Odd addresses -> POLY_EINVAL.
  * - n == 0 (or rows == 0 / cols == 0) is a valid no-op: POLY_OK, no launch.
+ * - Sizes: a tensor extent above 2^46 elements, a leading dimension or size
+ *   factor above that, or a tensor whose last byte would wrap the address
+ *   space -> POLY_EINVAL (no size computation can overflow).
  * - Aliasing: an output may be exactly the same buffer as an input (in
  *   place).  Partial overlap of an output with any other tensor ->
  *   POLY_EINVAL.

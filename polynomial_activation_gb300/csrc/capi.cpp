@@ -74,26 +74,54 @@ int check_program(const poly_program &p) {
   return POLY_OK;
 }
 
-// Byte span [lo, hi) of a tensor.
-struct Span {
-  uintptr_t lo, hi;
-};
+// Largest extent, in elements, that any call accepts (2^46, far beyond the
+// memory a GB300 system can address).  Larger sizes, and tensors whose last
+// byte would wrap the address space, are rejected, so that no size or span
+// computed below can overflow.
+constexpr int64_t kMaxElems = int64_t(1) << 46;
 
-Span span_flat(const void *p, int64_t n) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  return {a, a + (uintptr_t)n * 2};
+// a * b for non-negative sizes, or -1 if it exceeds kMaxElems.
+int64_t checked_mul(int64_t a, int64_t b) {
+  int64_t r;
+  if (a < 0 || b < 0 || __builtin_mul_overflow(a, b, &r) || r > kMaxElems) return -1;
+  return r;
 }
 
+// Byte span [lo, hi) of a tensor; ok is false when its extent is too large
+// or its end wraps the address space.
+struct Span {
+  uintptr_t lo, hi;
+  bool ok;
+};
+
+Span span_bytes(const void *p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  uintptr_t hi = 0;
+  const bool ok = bytes >= 0 && !__builtin_add_overflow(a, (uintptr_t)bytes, &hi);
+  return {a, hi, ok};
+}
+
+Span span_flat(const void *p, int64_t n) {
+  if (n < 0 || n > kMaxElems) return {0, 0, false};
+  return span_bytes(p, n * 2);
+}
+
+// rows x cols with leading dimension ld (all at most kMaxElems, ld >= cols).
 Span span_2d(const void *p, int64_t rows, int64_t cols, int64_t ld) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  return {a, a + (uintptr_t)(((rows - 1) * ld + cols) * 2)};
+  const int64_t body = checked_mul(rows - 1, ld);
+  if (body < 0 || cols > kMaxElems || body + cols > kMaxElems) return {0, 0, false};
+  return span_bytes(p, (body + cols) * 2);
 }
 
 bool overlaps(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
 
-// Outputs may coincide exactly with an input (in place), never partially
-// overlap anything, and never overlap each other.
+// Every span is valid; outputs may coincide exactly with an input (in
+// place), never partially overlap anything, and never overlap each other.
 bool aliasing_ok(const Span *in, int nin, const Span *out, int nout) {
+  for (int i = 0; i < nin; ++i)
+    if (!in[i].ok) return false;
+  for (int o = 0; o < nout; ++o)
+    if (!out[o].ok) return false;
   for (int o = 0; o < nout; ++o) {
     for (int i = 0; i < nin; ++i) {
       if (!overlaps(out[o], in[i])) continue;
@@ -145,11 +173,11 @@ int registry_get(int fn, int dir, int dtype, poly_program *out) {
 // Shared validation + layout for the dense 2-D SwiGLU calls.
 int swiglu_layout(const void *const *in, const int64_t *ld_in, int nin, void *const *out,
                   const int64_t *ld_out, int nout, int64_t rows, int64_t cols, Layout *l) {
-  if (rows < 0 || cols < 0) return POLY_EINVAL;
+  if (rows < 0 || cols < 0 || rows > kMaxElems || cols > kMaxElems) return POLY_EINVAL;
   for (int i = 0; i < nin; ++i)
-    if (ld_in[i] < cols) return POLY_EINVAL;
+    if (ld_in[i] < cols || ld_in[i] > kMaxElems) return POLY_EINVAL;
   for (int i = 0; i < nout; ++i)
-    if (ld_out[i] < cols) return POLY_EINVAL;
+    if (ld_out[i] < cols || ld_out[i] > kMaxElems) return POLY_EINVAL;
   if (rows == 0 || cols == 0) return 1;   // nothing to do
   const void *all[5];
   Span si[3], so[2];
@@ -195,7 +223,8 @@ int ragged_layout(const void *const *in, int nin, void *const *out, int nout,
   if (cap_rows == 0 || cols == 0) return 1;
   const void *all[5];
   Span si[3], so[2];
-  const int64_t n = cap_rows * cols;
+  const int64_t n = checked_mul(cap_rows, cols);
+  if (n < 0) return POLY_EINVAL;
   for (int i = 0; i < nin; ++i) {
     if (in[i] == nullptr || !even_address(in[i])) return POLY_EINVAL;
     si[i] = span_flat(in[i], n);
@@ -544,8 +573,9 @@ static int exp2_call(int core, const float *x, float *y, int64_t n, poly_stream_
   if (x == nullptr || y == nullptr) return POLY_EINVAL;
   if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u))
     return POLY_EINVAL;
-  Span si[1] = {{reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + (uintptr_t)n * 4}};
-  Span so[1] = {{reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + (uintptr_t)n * 4}};
+  if (n > kMaxElems) return POLY_EINVAL;
+  Span si[1] = {span_bytes(x, n * 4)};
+  Span so[1] = {span_bytes(y, n * 4)};
   if (!aliasing_ok(si, 1, so, 1)) return POLY_EINVAL;
   const int vec = ((reinterpret_cast<uintptr_t>(x) ^ reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   uint16_t c[3];
@@ -596,28 +626,39 @@ static int rope_call(int inv, int variant, const void *q, const void *k, void *q
                      int64_t head_dim, int64_t pos_offset, poly_stream_t stream) {
   if (variant < POLY_ROPE_POLY || variant > POLY_ROPE_TABLE) return POLY_EINVAL;
   if (batch < 0 || seq < 0 || hq < 0 || hkv < 0 || head_dim <= 0 || (head_dim & 7) ||
-      pos_offset < 0 || pos_offset + seq > (int64_t(1) << 32))
+      pos_offset < 0 || pos_offset > (int64_t(1) << 32) || seq > kMaxElems ||
+      pos_offset + seq > (int64_t(1) << 32))
     return POLY_EINVAL;
   if (batch == 0 || seq == 0 || hq + hkv == 0) return POLY_OK;
+  const int64_t rows = checked_mul(batch, seq);
+  const int64_t nq = checked_mul(checked_mul(rows, hq), head_dim);
+  const int64_t nk = checked_mul(checked_mul(rows, hkv), head_dim);
+  const int64_t ntab = checked_mul(seq, head_dim / 2);
+  if (rows < 0 || nq < 0 || nk < 0 || ntab < 0 || hq > kMaxElems || hkv > kMaxElems)
+    return POLY_EINVAL;
   Span si[4], so[2];
   int nin = 0, nout = 0;
   if (hq > 0) {
     if (!q || !q_out || !aligned16(q) || !aligned16(q_out)) return POLY_EINVAL;
-    si[nin++] = span_flat(q, batch * seq * hq * head_dim);
-    so[nout++] = span_flat(q_out, batch * seq * hq * head_dim);
+    si[nin++] = span_flat(q, nq);
+    so[nout++] = span_flat(q_out, nq);
   }
   if (hkv > 0) {
     if (!k || !k_out || !aligned16(k) || !aligned16(k_out)) return POLY_EINVAL;
-    si[nin++] = span_flat(k, batch * seq * hkv * head_dim);
-    so[nout++] = span_flat(k_out, batch * seq * hkv * head_dim);
+    si[nin++] = span_flat(k, nk);
+    so[nout++] = span_flat(k_out, nk);
   }
   if (variant == POLY_ROPE_TABLE) {
     if (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)) return POLY_EINVAL;
-    si[nin++] = span_flat(cos_tab, seq * head_dim / 2);
-    si[nin++] = span_flat(sin_tab, seq * head_dim / 2);
+    si[nin++] = span_flat(cos_tab, ntab);
+    si[nin++] = span_flat(sin_tab, ntab);
   } else if (!delta || !aligned16(delta)) {
     return POLY_EINVAL;
   }
+  for (int i = 0; i < nin; ++i)
+    if (!si[i].ok) return POLY_EINVAL;
+  for (int o = 0; o < nout; ++o)
+    if (!so[o].ok) return POLY_EINVAL;
   // transposed layouts: an output may not touch any input, nor the other output
   for (int o = 0; o < nout; ++o) {
     for (int i = 0; i < nin; ++i)

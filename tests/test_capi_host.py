@@ -173,6 +173,32 @@ def test_device_calls_reject_bad_arguments_on_host(L):
     assert L.poly_diag_packed(9, 0, FAKE, FAKE + 4096, FAKE, FAKE + 8192, 8, s) == B.POLY_EINVAL
 
 
+def test_oversized_and_wrapping_arguments_are_rejected(L):
+    """Extents above 2^46 elements, products that would overflow and spans
+    that would wrap the address space fail validation on the host."""
+    s = None
+    top = 0xFFFFFFFFFFFFF000                    # even; 4,096 FP16 elements wrap past 2^64
+    assert L.poly_act_fwd(0, 0, FAKE, FAKE + (1 << 49), 1 << 47, s) == B.POLY_EINVAL
+    assert L.poly_act_fwd(0, 0, top, FAKE, 4096, s) == B.POLY_EINVAL
+    assert L.poly_act_bwd(0, 0, FAKE, top, FAKE + 4096, 4096, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd(1, FAKE, FAKE + 8192, FAKE + 16384, 1 << 45, 16, 16, 16, 16,
+                             s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd(1, FAKE, FAKE + 8192, FAKE + 16384, 4, 16, 1 << 47, 16, 16,
+                             s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd_ragged(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 30000, 4,
+                                    1 << 40, 1 << 10, None, s) == B.POLY_EINVAL
+    assert L.poly_exp2(B.POLY_EXP2_D1, FAKE, FAKE + (1 << 50), 1 << 47, s) == B.POLY_EINVAL
+    assert L.poly_softcap_fwd(0, 30.0, FAKE, FAKE + (1 << 49), 1 << 47, s) == B.POLY_EINVAL
+    assert L.poly_diag_packed(1, 0, FAKE, FAKE, None, top, 4096, s) == B.POLY_EINVAL
+    for batch, seq, hq, hkv, d, pos in ((1 << 20, 1 << 20, 1 << 10, 0, 128, 0),
+                                        (1, 16, 1, 1, 8, 1 << 62),
+                                        (1, 1 << 40, 1, 0, 8, 0)):
+        assert L.poly_rope_fwd(B.POLY_ROPE_POLY, FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
+                               FAKE + 16384, None, None, batch, seq, hq, hkv, d, pos,
+                               s) == B.POLY_EINVAL
+    assert L.poly_last_cuda_error() == 0
+
+
 def test_empty_calls_are_no_ops(L):
     """n == 0 / rows == 0 return POLY_OK without touching CUDA (no GPU here)."""
     s = None
