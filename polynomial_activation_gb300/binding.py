@@ -169,6 +169,33 @@ def _check(status, where):
         raise PolyError(status, where)
 
 
+def _room(t, nbytes, where, name, esize=2, dtype=None):
+    """Check a tensor argument before its address crosses the C ABI (which
+    sees only pointers): device memory or pinned host memory, elements of
+    esize bytes, a declared FP16 / BF16 type that agrees with the call's
+    dtype, and at least nbytes from its first element to the end of its
+    storage.  Raw integer addresses are the caller's responsibility."""
+    if t is None or isinstance(t, int):
+        return
+    import torch
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{where}: {name} must be a CUDA tensor or pinned host memory")
+    if t.element_size() != esize:
+        raise ValueError(f"{where}: {name} has {t.element_size()}-byte elements, expected {esize}")
+    if dtype is not None and t.dtype in (torch.float16, torch.bfloat16) and _dtype_of(t) != dtype:
+        raise ValueError(f"{where}: {name} is {t.dtype}, which is not the call's dtype")
+    if nbytes > 0:
+        avail = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+        if avail < nbytes:
+            raise ValueError(f"{where}: {name} has {avail} bytes from its first element; the "
+                             f"call touches {nbytes}")
+
+
+def _extent(rows, cols, ld):
+    """Elements spanned by rows x cols with leading dimension ld."""
+    return (rows - 1) * ld + cols if rows > 0 and cols > 0 else 0
+
+
 def _ld(t, cols):
     """Leading dimension (elements) of a 2-D row-major view."""
     if t is None or isinstance(t, int):
@@ -220,23 +247,31 @@ def poly_get_swiglu_variant():
 
 def poly_act_fwd(fn, dtype, x, y, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 2 * n, "poly_act_fwd", nm, dtype=dtype)
     _check(lib().poly_act_fwd(fn, dtype, _ptr(x), _ptr(y), n, _stream(stream)), "poly_act_fwd")
 
 
 def poly_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (dy, "dy"), (dx, "dx")):
+        _room(t, 2 * n, "poly_act_bwd", nm, dtype=dtype)
     _check(lib().poly_act_bwd(fn, dtype, _ptr(x), _ptr(dy), _ptr(dx), n, _stream(stream)),
            "poly_act_bwd")
 
 
 def poly_ctrl_act_fwd(fn, dtype, x, y, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 2 * n, "poly_ctrl_act_fwd", nm, dtype=dtype)
     _check(lib().poly_ctrl_act_fwd(fn, dtype, _ptr(x), _ptr(y), n, _stream(stream)),
            "poly_ctrl_act_fwd")
 
 
 def poly_ctrl_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (dy, "dy"), (dx, "dx")):
+        _room(t, 2 * n, "poly_ctrl_act_bwd", nm, dtype=dtype)
     _check(lib().poly_ctrl_act_bwd(fn, dtype, _ptr(x), _ptr(dy), _ptr(dx), n, _stream(stream)),
            "poly_ctrl_act_bwd")
 
@@ -247,6 +282,8 @@ def _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, name):
     ldg = _ld(g, cols) if ldg is None else ldg
     ldu = _ld(u, cols) if ldu is None else ldu
     ldy = _ld(y, cols) if ldy is None else ldy
+    for t, nm, ld in ((g, "g", ldg), (u, "u", ldu), (y, "y", ldy)):
+        _room(t, 2 * _extent(rows, cols, ld), name, nm, dtype=dtype)
     _check(cfn(dtype, _ptr(g), _ptr(u), _ptr(y), rows, cols, ldg, ldu, ldy, _stream(stream)),
            name)
 
@@ -268,6 +305,8 @@ def _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, lds, stream, name):
     cols = g.shape[-1] if cols is None else cols
     ts = (g, u, dy, dg, du)
     lds = [(_ld(t, cols) if l is None else l) for t, l in zip(ts, lds)]
+    for t, nm, ld in zip(ts, ("g", "u", "dy", "dg", "du"), lds):
+        _room(t, 2 * _extent(rows, cols, ld), name, nm, dtype=dtype)
     _check(cfn(dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg), _ptr(du), rows, cols, *lds,
                _stream(stream)), name)
 
@@ -284,11 +323,20 @@ def poly_ctrl_swiglu_bwd(dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None
                 (ldg, ldu, lddy, lddg, lddu), stream, "poly_ctrl_swiglu_bwd")
 
 
+def _ragged_room(where, dtype, ts, names, seg_off, num_segments, cap_rows, cols, status):
+    for t, nm in zip(ts, names):
+        _room(t, 2 * cap_rows * cols, where, nm, dtype=dtype)
+    _room(seg_off, 4 * (num_segments + 1), where, "seg_off", esize=4)
+    _room(status, 4, where, "status", esize=4)
+
+
 def poly_swiglu_fwd_ragged(dtype, g, u, y, seg_off, num_segments=None, cap_rows=None,
                            cols=None, status=None, stream=None):
     num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
     cap_rows = g.shape[0] if cap_rows is None else cap_rows
     cols = g.shape[-1] if cols is None else cols
+    _ragged_room("poly_swiglu_fwd_ragged", dtype, (g, u, y), ("g", "u", "y"), seg_off,
+                 num_segments, cap_rows, cols, status)
     _check(lib().poly_swiglu_fwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(y), _ptr(seg_off),
                                         num_segments, cap_rows, cols, _ptr(status),
                                         _stream(stream)), "poly_swiglu_fwd_ragged")
@@ -299,6 +347,8 @@ def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, 
     num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
     cap_rows = g.shape[0] if cap_rows is None else cap_rows
     cols = g.shape[-1] if cols is None else cols
+    _ragged_room("poly_swiglu_bwd_ragged", dtype, (g, u, dy, dg, du), ("g", "u", "dy", "dg", "du"),
+                 seg_off, num_segments, cap_rows, cols, status)
     _check(lib().poly_swiglu_bwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg), _ptr(du),
                                         _ptr(seg_off), num_segments, cap_rows, cols,
                                         _ptr(status), _stream(stream)),
@@ -307,6 +357,8 @@ def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, 
 
 def poly_diag_packed(op, dtype, a, b, c, out, n=None, stream=None):
     n = a.numel() if n is None else n
+    for t, nm in ((a, "a"), (b, "b"), (c, "c"), (out, "out")):
+        _room(t, 2 * n, "poly_diag_packed", nm, dtype=dtype)
     _check(lib().poly_diag_packed(op, dtype, _ptr(a), _ptr(b), _ptr(c), _ptr(out), n,
                                   _stream(stream)), "poly_diag_packed")
 
@@ -328,23 +380,31 @@ def poly_derive_program(fwd: PolyProgram):
 
 def poly_softcap_fwd(dtype, alpha, x, y, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 2 * n, "poly_softcap_fwd", nm, dtype=dtype)
     _check(lib().poly_softcap_fwd(dtype, float(alpha), _ptr(x), _ptr(y), n, _stream(stream)),
            "poly_softcap_fwd")
 
 
 def poly_softcap_bwd(dtype, alpha, x, dy, dx, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (dy, "dy"), (dx, "dx")):
+        _room(t, 2 * n, "poly_softcap_bwd", nm, dtype=dtype)
     _check(lib().poly_softcap_bwd(dtype, float(alpha), _ptr(x), _ptr(dy), _ptr(dx), n,
                                   _stream(stream)), "poly_softcap_bwd")
 
 
 def poly_exp2(core, x, y, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 4 * n, "poly_exp2", nm, esize=4)
     _check(lib().poly_exp2(core, _ptr(x), _ptr(y), n, _stream(stream)), "poly_exp2")
 
 
 def poly_ctrl_exp2(x, y, n=None, stream=None):
     n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 4 * n, "poly_ctrl_exp2", nm, esize=4)
     _check(lib().poly_ctrl_exp2(_ptr(x), _ptr(y), n, _stream(stream)), "poly_ctrl_exp2")
 
 
@@ -368,6 +428,12 @@ def poly_rope_programs():
 def _rope(fn, name, variant, q, k, q_out, k_out, delta, cos_tab, sin_tab, shape,
           pos_offset, stream):
     batch, seq, hq, hkv, head_dim = shape
+    nq, nk = batch * seq * hq * head_dim, batch * seq * hkv * head_dim
+    for t, nm, cnt in ((q, "q", nq), (k, "k", nk), (q_out, "q_out", nq), (k_out, "k_out", nk),
+                       (cos_tab, "cos_tab", seq * head_dim // 2),
+                       (sin_tab, "sin_tab", seq * head_dim // 2)):
+        _room(t, 2 * cnt, name, nm)
+    _room(delta, 4 * (head_dim // 2), name, "delta", esize=4)
     _check(fn(variant, _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(delta), _ptr(cos_tab),
               _ptr(sin_tab), batch, seq, hq, hkv, head_dim, pos_offset, _stream(stream)), name)
 

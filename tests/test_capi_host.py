@@ -199,6 +199,15 @@ def test_oversized_and_wrapping_arguments_are_rejected(L):
     assert L.poly_last_cuda_error() == 0
 
 
+def test_binding_refuses_pageable_host_tensors():
+    """The binding passes only device or pinned host memory to the library:
+    an ordinary CPU tensor is refused before any call."""
+    import torch
+    x = torch.zeros(16, dtype=torch.float16)
+    with pytest.raises(ValueError, match="pinned"):
+        B.poly_act_fwd(B.POLY_SIGMOID, B.POLY_F16, x, x.clone())
+
+
 def test_empty_calls_are_no_ops(L):
     """n == 0 / rows == 0 return POLY_OK without touching CUDA (no GPU here)."""
     s = None

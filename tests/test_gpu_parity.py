@@ -139,6 +139,30 @@ def test_small_sizes_offsets_and_guards(dt):
             assert guards_intact(buf, n, G, off_y), (n, off_x, off_y)
 
 
+def test_binding_checks_tensor_extents_before_launch():
+    """A tensor too short for the call, a dtype that disagrees with the
+    call's, or pageable host memory is refused by the binding before the
+    library sees the address; the output stays untouched."""
+    dt = B.POLY_F16
+    x = torch.zeros(1000, dtype=torch.float16, device=DEV)
+    dy_short = torch.zeros(999, dtype=torch.float16, device=DEV)
+    y = torch.full((1000,), 0x5A5A, dtype=torch.int16, device=DEV).view(torch.float16)
+    with pytest.raises(ValueError, match="dy"):
+        B.poly_act_bwd(B.POLY_SIGMOID, dt, x, dy_short, y)
+    with pytest.raises(ValueError, match="y"):
+        B.poly_act_fwd(B.POLY_SIGMOID, dt, x, y[1:])
+    with pytest.raises(ValueError, match="dtype"):
+        B.poly_act_fwd(B.POLY_SIGMOID, B.POLY_BF16, x, y)
+    with pytest.raises(ValueError, match="pinned"):
+        B.poly_act_fwd(B.POLY_SIGMOID, dt, x, torch.empty(1000, dtype=torch.float16))
+    g = torch.zeros((8, 64), dtype=torch.bfloat16, device=DEV)
+    u_short = torch.zeros((8, 32), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError, match="u"):
+        B.poly_swiglu_fwd(B.POLY_BF16, g, u_short, torch.empty_like(g), cols=64, ldu=64)
+    torch.cuda.synchronize()
+    assert bool((y.view(torch.int16) == 0x5A5A).all())
+
+
 def test_injected_launch_failures_leave_outputs_and_context_intact():
     """Two injected launch failures (poly_debug_fail_launches): the next two
     launching calls -- an activation and a SwiGLU -- raise POLY_ECUDA with the
