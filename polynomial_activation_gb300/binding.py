@@ -432,7 +432,7 @@ def _rope(fn, name, variant, q, k, q_out, k_out, delta, cos_tab, sin_tab, shape,
     for t, nm, cnt in ((q, "q", nq), (k, "k", nk), (q_out, "q_out", nq), (k_out, "k_out", nk),
                        (cos_tab, "cos_tab", seq * head_dim // 2),
                        (sin_tab, "sin_tab", seq * head_dim // 2)):
-        _room(t, 2 * cnt, name, nm)
+        _room(t, 2 * cnt, name, nm, dtype=POLY_F16)          # the RoPE kernels are FP16
     _room(delta, 4 * (head_dim // 2), name, "delta", esize=4)
     _check(fn(variant, _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(delta), _ptr(cos_tab),
               _ptr(sin_tab), batch, seq, hq, hkv, head_dim, pos_offset, _stream(stream)), name)

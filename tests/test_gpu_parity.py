@@ -155,6 +155,11 @@ def test_binding_checks_tensor_extents_before_launch():
         B.poly_act_fwd(B.POLY_SIGMOID, B.POLY_BF16, x, y)
     with pytest.raises(ValueError, match="pinned"):
         B.poly_act_fwd(B.POLY_SIGMOID, dt, x, torch.empty(1000, dtype=torch.float16))
+    qb = torch.zeros((1, 4, 2, 8), dtype=torch.bfloat16, device=DEV)
+    dlt = torch.from_numpy(B.poly_rope_turn_increments(8).view(np.int32)).to(DEV)
+    with pytest.raises(ValueError, match="dtype"):                    # RoPE is FP16 only
+        B.poly_rope_fwd(B.POLY_ROPE_POLY, qb, None, torch.empty((1, 2, 4, 8), dtype=torch.bfloat16,
+                        device=DEV), None, dlt, hkv=0)
     g = torch.zeros((8, 64), dtype=torch.bfloat16, device=DEV)
     u_short = torch.zeros((8, 32), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(ValueError, match="u"):
