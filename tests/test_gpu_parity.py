@@ -550,6 +550,55 @@ def test_host_memory_operands(dt):
     assert np.array_equal(yh2.view(torch.int16).numpy().view(np.uint16), forward(op, x))
 
 
+def _strided_view(buf, off, rows, cols, ld):
+    return torch.as_strided(buf, (rows, cols), (ld, 1), storage_offset=off)
+
+
+def test_swiglu_random_layouts_every_element():
+    """48 seeded cases: rows 1-40, cols 1-70, a leading dimension and an
+    element offset of its own for every stream (0-13 padding, 0-7 elements
+    of misalignment), both formats, both SwiGLU rules, forward and backward;
+    every element against the oracle, and nothing outside an output's view
+    is written."""
+    from oracle.replay import swiglu_sigmoid_backward, swiglu_sigmoid_forward
+    rng = np.random.default_rng(71)
+    for case in range(48):
+        dt = DTS[case % 2]
+        fmt = FMT[dt]
+        sig_rule = (case // 2) % 2 == 1
+        rows, cols = int(rng.integers(1, 41)), int(rng.integers(1, 71))
+        lds = [cols + int(rng.integers(0, 14)) for _ in range(6)]       # g, u, y, dy, dg, du
+        offs = [int(rng.integers(0, 8)) for _ in range(6)]
+        bufs = [torch.full((o + rows * l + 8,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+                for o, l in zip(offs, lds)]
+        vals = [_rand_bits(rng, rows * cols, fmt).reshape(rows, cols) for _ in range(3)]
+        views = [_strided_view(b, o, rows, cols, l) for b, o, l in zip(bufs, offs, lds)]
+        for v, a in zip((views[0], views[1], views[3]), vals):
+            v.copy_(to_dev(a, dt).view(rows, cols))
+        g, u, dy = vals
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID if sig_rule else B.POLY_SWIGLU_DIRECT)
+        try:
+            B.poly_swiglu_fwd(dt, views[0], views[1], views[2])
+            B.poly_swiglu_bwd(dt, views[0], views[1], views[3], views[4], views[5])
+        finally:
+            B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+        if sig_rule:
+            sig = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+            wy = swiglu_sigmoid_forward(sig, g, u)
+            wdg, wdu = swiglu_sigmoid_backward(sig, g, u, dy)
+        else:
+            s_op, d_op = _swiglu_ops(dt)
+            wy = swiglu_forward(s_op, g, u)
+            wdg, wdu = swiglu_backward(s_op, d_op, g, u, dy)
+        where = (case, rows, cols, lds, offs)
+        for k, want in ((2, wy), (4, wdg), (5, wdu)):
+            assert np.array_equal(from_dev(views[k]).reshape(rows, cols), want), where
+            full = from_dev(bufs[k]).copy()
+            idx = offs[k] + np.arange(rows)[:, None] * lds[k] + np.arange(cols)[None, :]
+            full[idx.reshape(-1)] = 0x5A5A
+            assert np.all(full == 0x5A5A), where
+
+
 @pytest.fixture
 def sigmoid_swiglu():
     B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
