@@ -264,6 +264,24 @@ def _equal_bits(got, want):
     return bool(torch.equal(g[~nan], w[~nan])) and bool(torch.isnan(got.float()[nan]).all())
 
 
+def test_chunk_shape_switch_sizes():
+    """Sizes on both sides of the point where a one-input call changes from
+    one to two 16-byte chunks per thread (four two-chunk blocks per SM), with
+    and without an n mod 8 tail: every element against the oracle's table."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    edge = 4 * sms * 256 * 2 * 8
+    dt = B.POLY_BF16
+    op = oracle_program(B.POLY_GELU, B.POLY_FWD, dt)
+    rng = np.random.default_rng(81)
+    big = _rand_bits(rng, edge + 8192, "bf16")
+    xd = to_dev(big, dt)
+    for n in (edge - 4096 - 3, edge - 8, edge - 1, edge, edge + 5, edge + 8, edge + 4096 + 7):
+        y = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+        B.poly_act_fwd(B.POLY_GELU, dt, xd[:n], y[:n], n)
+        assert _equal_bits(y[:n], _apply_lut(op, xd[:n])), n
+        assert bool((y[n:].view(torch.int16) == 0x5A5A).all()), n
+
+
 @pytest.mark.parametrize("n", [(1 << 31) - 3, (1 << 31) + 13])
 def test_index_width_limits(n):
     """Just below 2^31 elements (the dense kernel's 32-bit indices at their
