@@ -20,10 +20,16 @@ Transcendentals for LLMs", arXiv 2610.00049):
   add, §3.2 step 4) and in real arithmetic (the Table 2 metric).
 * ``fit``       -- the endpoint-constrained least-squares fitter and the
   (Li, Lc) search of §3.2 (eq. 7-8, steps 1-7).
+* ``exp2``      -- 2^x with the FP32 range reduction, packed-FP16 fractional
+  cores and exponent-bit reconstruction of Appendix B.1 (Table 8).
+* ``rope``      -- Q0.32 turn increments, the folded Q15 phase, the paired
+  FP16 sine / cosine programs and the rotation of Appendix B.2.
 
 Every function is pinned in ``tests/test_oracle_*.py`` against something
-other than itself: exact rational arithmetic, mpmath, printed values of the
-paper's Table 2 and Figure 2, closed forms and exact symmetry identities.
+other than itself: exact rational arithmetic and a second exact model in
+scaled integers (ten million random triples per format), mpmath, printed
+values of the paper's Tables 2 and 8 and Figure 2, closed forms and exact
+symmetry identities.
 Parity unpinned: the exact coefficients chosen by ``fit.search`` (the paper
 prints none for these programs; only magnitudes of their errors).
 """
