@@ -16,19 +16,22 @@
  *   throws, aborts or prints.
  * - Ownership: the caller owns every buffer.  The library never allocates,
  *   frees or synchronises device memory.
- * - Device calls (poly_act_*, poly_swiglu_*, poly_ctrl_*) take addresses
- *   the GPU can reach -- device memory, or, on systems with coherent host
- *   access such as GB300's NVLink-C2C, pinned host memory (the kernels then
- *   stream it over the link with no staging copy) -- and a CUDA stream
- *   (poly_stream_t is layout-compatible with cudaStream_t; NULL = the legacy
- *   default stream).  Kernels run on the calling thread's current device.  They validate the
+ * - Device calls (poly_act_*, poly_swiglu_*, poly_softcap_*, poly_exp2,
+ *   poly_rope_*, poly_ctrl_*, poly_diag_packed) take addresses the GPU can
+ *   reach -- device memory, or, on systems with coherent host access such as
+ *   GB300's NVLink-C2C, pinned host memory (the kernels then stream it over
+ *   the link with no staging copy) -- and a CUDA stream (poly_stream_t is
+ *   layout-compatible with cudaStream_t; NULL = the legacy default stream).
+ *   Kernels run on the calling thread's current device.  They validate the
  *   arguments on the host, enqueue one kernel and return without waiting.
  *   A launch failure is reported as POLY_ECUDA (the CUDA error is consumed
  *   and available through poly_last_cuda_error).
  * - Tensors hold 16-bit elements (FP16 or BF16 bit patterns), contiguous
  *   unless leading dimensions are given.  Any 2-byte alignment is accepted:
  *   16-byte-aligned data takes the 128-bit vector path, a scalar head and
- *   tail cover the rest.  Odd addresses -> POLY_EINVAL.
+ *   tail cover the rest.  Odd addresses -> POLY_EINVAL.  Exceptions, stated
+ *   at each call: poly_exp2 works on FP32 (4-byte aligned), the RoPE calls
+ *   on FP16 with 16-byte-aligned tensors.
  * - n == 0 (or rows == 0 / cols == 0) is a valid no-op: POLY_OK, no launch.
  * - Sizes: a tensor extent above 2^46 elements, a leading dimension or size
  *   factor above that, or a tensor whose last byte would wrap the address
