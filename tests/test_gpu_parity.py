@@ -705,6 +705,29 @@ def test_softcap_exhaustive(dt, alpha):
     assert np.array_equal(from_dev(out), softcap_backward(dp, alpha, x, dy))
 
 
+def test_softcap_full_size_every_element():
+    """alpha = 30 on the bench's 268,435,456-element FP16 tensors: the forward
+    through the oracle's exhaustive table of softcap(x); the backward as dy
+    times the tabulated tanh'(x * (1/alpha)), each product rounded once (a
+    product of two FP16 values is exact in FP32)."""
+    from oracle.replay import softcap_backward, softcap_forward
+    dt, alpha = B.POLY_F16, 30.0
+    tp = oracle_program(B.POLY_TANH, B.POLY_FWD, dt)
+    dp = oracle_program(B.POLY_TANH, B.POLY_BWD, dt)
+    x, dy = workloads.isolated_hbm("f16")
+    xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+    del x, dy
+    out = torch.empty_like(xd)
+    idx = (xd.view(torch.int16).to(torch.int32) & 0xFFFF).long()
+    B.poly_softcap_fwd(dt, alpha, xd, out)
+    lut_f = torch.from_numpy(softcap_forward(tp, alpha, X_ALL).view(np.int16)).to(DEV)
+    assert _equal_bits(out, lut_f[idx].view(torch.float16))
+    B.poly_softcap_bwd(dt, alpha, xd, dyd, out)
+    ones = np.full(X_ALL.size, 0x3C00, dtype=np.uint16)          # dy = 1 tabulates the factor
+    lut_d = torch.from_numpy(softcap_backward(dp, alpha, X_ALL, ones).view(np.int16)).to(DEV)
+    assert _equal_bits(out, _rn_mul(dyd, lut_d[idx].view(torch.float16)))
+
+
 @pytest.mark.parametrize("dt", DTS)
 @pytest.mark.parametrize("fn,D", [(B.POLY_TANH, 4), (B.POLY_SIGMOID, 3)])
 def test_derived_program_backward_exhaustive(dt, fn, D):
