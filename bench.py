@@ -716,10 +716,47 @@ def e2e(args, dev, stream, xh, dyh, chunks=8):
 
     steps = max(3, min(20, args.steps // 20))
     ms = _time(step, stream, steps, 4)     # the first passes touch the pinned pages
+    link = link_bound(x, xp, dyf, outs_h[0], stream, copy_stream, h2d=2 * 2 * n, d2h=6 * 2 * n)
+    link["frac"] = link["bound_ms"] / ms
     return {"value": 6 * n / ms / 1e6, "unit": UNIT, "h2d_bytes_per_step": 2 * 2 * n,
-            "d2h_bytes_per_step": 6 * 2 * n, "ms_per_step": ms,
+            "d2h_bytes_per_step": 6 * 2 * n, "ms_per_step": ms, "link": link,
             "method": f"pinned host inputs copied in {len(bounds)} pieces on a second stream; "
                       "kernels write outputs directly to pinned host memory (NVLink-C2C)"}
+
+
+def link_bound(xd, xp, src, out_h, stream, copy_stream, h2d, d2h):
+    """The host link's rates, measured on the step's own buffers: host->device
+    copies alone, kernel stores into pinned host memory alone, and both at
+    once (equal bytes).  A step moving h2d bytes in and d2h >= h2d bytes out
+    cannot beat h2d / r_both + (d2h - h2d) / r_store, where r_both is the
+    per-direction rate while both directions are busy.  The copy fills xd
+    from xp; the kernel reads src (another device buffer) into out_h."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    m = xd.numel()
+    nb = 2 * m
+
+    def copy_in():
+        with torch.cuda.stream(copy_stream):
+            xd.copy_(xp, non_blocking=True)
+        stream.wait_stream(copy_stream)
+
+    def store_out():
+        B.poly_act_fwd(FN["sigmoid"], B.POLY_F16, src, out_h, m, stream=stream)
+
+    def both():
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            xd.copy_(xp, non_blocking=True)
+        B.poly_act_fwd(FN["sigmoid"], B.POLY_F16, src, out_h, m, stream=stream)
+        stream.wait_stream(copy_stream)
+
+    r_in = nb / _time(copy_in, stream, 3) / 1e6
+    r_out = nb / _time(store_out, stream, 3) / 1e6
+    r_both = nb / _time(both, stream, 3) / 1e6          # per direction
+    bound = (h2d / r_both + max(0, d2h - h2d) / r_out) / 1e6
+    return {"h2d_copy_gbs": r_in, "kernel_store_to_host_gbs": r_out,
+            "per_direction_when_both_gbs": r_both, "bound_ms": bound}
 
 
 if __name__ == "__main__":
