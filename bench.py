@@ -60,10 +60,16 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources with comments and blank space removed, so
+    that only a change to the code itself invalidates recorded counters."""
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "polynomial_activation_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "polynomial_activation_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

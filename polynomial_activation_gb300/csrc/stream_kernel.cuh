@@ -11,9 +11,10 @@
 //    replaced as fast as the memory system drains them;
 //  * a dense kernel for the common cases (flat, or ragged rows of a multiple
 //    of 8 columns; every stream 16-byte aligned; fewer than 2^31 elements)
-//    with 32-bit indices and no layout branches,
-//    which cuts the per-thread instruction count that dominates launches of
-//    L2-resident size;
+//    with 32-bit indices and no layout branches, which cuts the per-thread
+//    instruction count that dominates launches of L2-resident size;
+//  * programmatic dependent launch, so that a launch's blocks are scheduled
+//    while the previous kernel on the stream drains;
 //  * a scalar head (up to the first 16-byte boundary) and tail, evaluated
 //    with the same packed instructions on one lane so that every element
 //    gets bit-identical arithmetic; streams whose addresses disagree modulo

@@ -43,3 +43,19 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     c = bench.ClockSampler(0)
     c.start()
     assert c.stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+
+
+def test_kernel_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    """Recorded DRAM counters stay valid across comment edits and become
+    invalid when the code changes."""
+    csrc = tmp_path / "polynomial_activation_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = csrc / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", ["k.cu"])
+    src.write_text("// a kernel\nint f(int x) { return x + 1; }  /* one */\n")
+    h0 = bench.kernel_source_hash()
+    src.write_text("// the kernel, reworded\n\nint f(int x) {\n  return x + 1;  // same code\n}\n")
+    assert bench.kernel_source_hash() == h0
+    src.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_source_hash() != h0
