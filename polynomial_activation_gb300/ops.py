@@ -112,6 +112,29 @@ def swiglu(g, u):
     return PolySwiGLU.apply(g, u)
 
 
+class PolySwiGLURagged(torch.autograd.Function):
+    """Routed-expert SwiGLU over rows [seg_off[0], seg_off[E]) of [cap_rows,
+    cols] gate / up buffers (offsets stay on the device); rows outside the
+    range are left zero in the output and in both gradients."""
+
+    @staticmethod
+    def forward(ctx, g, u, seg_off):
+        g, u = g.contiguous(), u.contiguous()
+        ctx.save_for_backward(g, u, seg_off)
+        return swiglu_fwd_ragged(g, u, seg_off, out=torch.zeros_like(g))
+
+    @staticmethod
+    def backward(ctx, dy):
+        g, u, seg_off = ctx.saved_tensors
+        dg, du = swiglu_bwd_ragged(g, u, dy.contiguous(), seg_off, dg=torch.zeros_like(g),
+                                   du=torch.zeros_like(g))
+        return dg, du, None
+
+
+def swiglu_ragged(g, u, seg_off):
+    return PolySwiGLURagged.apply(g, u, seg_off)
+
+
 class PolySoftcap(torch.autograd.Function):
     """alpha * tanh(x / alpha) (attention-logit softcap)."""
 

@@ -992,6 +992,18 @@ def test_autograd_wrappers_match_direct_calls():
         dg, du = ops.swiglu_bwd(g.detach(), u.detach(), dyy)
         assert torch.equal(g.grad.view(torch.int16), dg.view(torch.int16))
         assert torch.equal(u.grad.view(torch.int16), du.view(torch.int16))
+        # ragged: rows [0, 40) of a 64-row capacity; the rest stay zero
+        seg = torch.tensor([0, 10, 10, 40], dtype=torch.int32, device=DEV)
+        g.grad, u.grad = None, None
+        y = ops.swiglu_ragged(g, u, seg)
+        y.backward(dyy)
+        dg, du = ops.swiglu_bwd(g.detach()[:40], u.detach()[:40], dyy[:40])
+        assert torch.equal(y.detach()[:40].view(torch.int16),
+                           ops.swiglu_fwd(g.detach()[:40], u.detach()[:40]).view(torch.int16))
+        assert torch.equal(g.grad[:40].view(torch.int16), dg.view(torch.int16))
+        assert torch.equal(u.grad[:40].view(torch.int16), du.view(torch.int16))
+        for t in (y.detach(), g.grad, u.grad):
+            assert not bool(t[40:].view(torch.int16).any())
         x.grad = None
         y = ops.softcap(x, 30.0)
         y.backward(dy)
