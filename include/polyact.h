@@ -36,9 +36,11 @@
  * - Sizes: a tensor extent above 2^46 elements, a leading dimension or size
  *   factor above that, or a tensor whose last byte would wrap the address
  *   space -> POLY_EINVAL (no size computation can overflow).
- * - Aliasing: an output may be exactly the same buffer as an input (in
- *   place).  Partial overlap of an output with any other tensor ->
- *   POLY_EINVAL.
+ * - Aliasing: an output may be exactly the same view as an input (in
+ *   place).  An output sharing any byte with another tensor otherwise ->
+ *   POLY_EINVAL.  Views that share no element may interleave: row sets of
+ *   the same leading dimension whose rows fall in each other's gaps (the
+ *   gate and up halves of one [T, 2H] buffer, ld = 2H) are accepted.
  * - Arithmetic: every packed FMA / multiply rounds once to the target format,
  *   to nearest-even, with subnormals kept; a NaN result is 0x7FFF.  Outputs
  *   are bit-exact functions of the inputs and the installed program.

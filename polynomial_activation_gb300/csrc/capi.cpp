@@ -87,33 +87,56 @@ int64_t checked_mul(int64_t a, int64_t b) {
   return r;
 }
 
-// Byte span [lo, hi) of a tensor; ok is false when its extent is too large
-// or its end wraps the address space.
+// Byte span [lo, hi) of a tensor, as rows of `width` bytes whose starts are
+// `pitch` bytes apart (one row for a flat tensor); ok is false when its
+// extent is too large or its end wraps the address space.
 struct Span {
   uintptr_t lo, hi;
   bool ok;
+  uintptr_t pitch, width;
 };
 
 Span span_bytes(const void *p, int64_t bytes) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   uintptr_t hi = 0;
   const bool ok = bytes >= 0 && !__builtin_add_overflow(a, (uintptr_t)bytes, &hi);
-  return {a, hi, ok};
+  return {a, hi, ok, (uintptr_t)bytes, (uintptr_t)bytes};
 }
 
 Span span_flat(const void *p, int64_t n) {
-  if (n < 0 || n > kMaxElems) return {0, 0, false};
+  if (n < 0 || n > kMaxElems) return {0, 0, false, 0, 0};
   return span_bytes(p, n * 2);
 }
 
 // rows x cols with leading dimension ld (all at most kMaxElems, ld >= cols).
 Span span_2d(const void *p, int64_t rows, int64_t cols, int64_t ld) {
   const int64_t body = checked_mul(rows - 1, ld);
-  if (body < 0 || cols > kMaxElems || body + cols > kMaxElems) return {0, 0, false};
-  return span_bytes(p, (body + cols) * 2);
+  if (body < 0 || cols > kMaxElems || body + cols > kMaxElems) return {0, 0, false, 0, 0};
+  Span s = span_bytes(p, (body + cols) * 2);
+  if (rows > 1) {
+    s.pitch = (uintptr_t)ld * 2;
+    s.width = (uintptr_t)cols * 2;
+  }
+  return s;
 }
 
-bool overlaps(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
+// Whether two tensors share a byte.  Extents that intersect can still be
+// disjoint when both are row sets of the same pitch and one's rows fall in
+// the other's gaps (the gate and up halves of one [T, 2H] buffer).
+bool overlaps(const Span &a, const Span &b) {
+  if (!(a.lo < b.hi && b.lo < a.hi)) return false;
+  if (a.pitch == b.pitch && a.pitch > a.width && b.pitch > b.width) {
+    const Span &f = a.lo <= b.lo ? a : b;
+    const Span &g = a.lo <= b.lo ? b : a;
+    const uintptr_t d = (g.lo - f.lo) % f.pitch;
+    if (d >= f.width && d + g.width <= f.pitch) return false;
+  }
+  return true;
+}
+
+bool same_view(const Span &a, const Span &b) {
+  return a.lo == b.lo && a.hi == b.hi && a.pitch == b.pitch && a.width == b.width;
+}
 
 // Every span is valid; outputs may coincide exactly with an input (in
 // place), never partially overlap anything, and never overlap each other.
@@ -125,7 +148,7 @@ bool aliasing_ok(const Span *in, int nin, const Span *out, int nout) {
   for (int o = 0; o < nout; ++o) {
     for (int i = 0; i < nin; ++i) {
       if (!overlaps(out[o], in[i])) continue;
-      if (out[o].lo == in[i].lo && out[o].hi == in[i].hi) continue;
+      if (same_view(out[o], in[i])) continue;
       return false;
     }
     for (int o2 = o + 1; o2 < nout; ++o2)

@@ -177,6 +177,7 @@ def test_oversized_and_wrapping_arguments_are_rejected(L):
     """Extents above 2^46 elements, products that would overflow and spans
     that would wrap the address space fail validation on the host."""
     s = None
+    before = L.poly_last_cuda_error()
     top = 0xFFFFFFFFFFFFF000                    # even; 4,096 FP16 elements wrap past 2^64
     assert L.poly_act_fwd(0, 0, FAKE, FAKE + (1 << 49), 1 << 47, s) == B.POLY_EINVAL
     assert L.poly_act_fwd(0, 0, top, FAKE, 4096, s) == B.POLY_EINVAL
@@ -196,7 +197,30 @@ def test_oversized_and_wrapping_arguments_are_rejected(L):
         assert L.poly_rope_fwd(B.POLY_ROPE_POLY, FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288,
                                FAKE + 16384, None, None, batch, seq, hq, hkv, d, pos,
                                s) == B.POLY_EINVAL
-    assert L.poly_last_cuda_error() == 0
+    assert L.poly_last_cuda_error() == before
+
+
+def test_interleaved_halves_are_disjoint_partial_overlap_is_not(L):
+    """Gate and up (and their gradients) as the two halves of one [T, 2H]
+    buffer with ld = 2H share no element and pass validation -- shown by an
+    injected launch failure, which only a call that reached its launch
+    consumes -- while views whose rows overlap by one chunk are refused."""
+    T, H = 16, 64
+    gu, dgu, dy = FAKE, FAKE + (1 << 20), FAKE + (2 << 20)
+    assert L.poly_debug_fail_launches(777, 1) == 0
+    try:
+        st = L.poly_swiglu_bwd(1, gu, gu + 2 * H, dy, dgu, dgu + 2 * H, T, H, 2 * H, 2 * H, H,
+                               2 * H, 2 * H, None)
+        assert st == B.POLY_ECUDA and L.poly_last_cuda_error() == 777
+        assert L.poly_debug_fail_launches(777, 0) == 0            # consumed by that call
+        # du shifted 8 elements left: its rows overlap the end of dg's rows
+        assert L.poly_swiglu_bwd(1, gu, gu + 2 * H, dy, dgu, dgu + 2 * (H - 8), T, H, 2 * H,
+                                 2 * H, H, 2 * H, 2 * H, None) == B.POLY_EINVAL
+        # output over an input's gap-free region: y on top of gate's rows
+        assert L.poly_swiglu_fwd(1, gu, gu + 2 * H, gu + 16, T, H, 2 * H, 2 * H, 2 * H,
+                                 None) == B.POLY_EINVAL
+    finally:
+        L.poly_debug_fail_launches(777, 0)
 
 
 def test_binding_refuses_pageable_host_tensors():
@@ -211,6 +235,7 @@ def test_binding_refuses_pageable_host_tensors():
 def test_empty_calls_are_no_ops(L):
     """n == 0 / rows == 0 return POLY_OK without touching CUDA (no GPU here)."""
     s = None
+    before = L.poly_last_cuda_error()
     assert L.poly_act_fwd(0, 0, None, None, 0, s) == B.POLY_OK
     assert L.poly_act_bwd(1, 1, None, None, None, 0, s) == B.POLY_OK
     assert L.poly_ctrl_act_fwd(3, 1, None, None, 0, s) == B.POLY_OK
@@ -218,7 +243,7 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_swiglu_bwd(1, None, None, None, None, None, 5, 0, 0, 0, 0, 0, 0, s) == B.POLY_OK
     assert L.poly_swiglu_fwd_ragged(1, None, None, None, FAKE, 4, 0, 16, None, s) == B.POLY_OK
     assert L.poly_diag_packed(0, 0, None, None, None, None, 0, s) == B.POLY_OK
-    assert L.poly_last_cuda_error() == 0
+    assert L.poly_last_cuda_error() == before
 
 
 def test_failure_injection_is_consumed_only_by_launches(L):
@@ -228,10 +253,11 @@ def test_failure_injection_is_consumed_only_by_launches(L):
     assert L.poly_debug_fail_launches(-5, 1) == B.POLY_EINVAL
     assert L.poly_debug_fail_launches(701, -1) == B.POLY_EINVAL
     assert L.poly_debug_fail_launches(701, 2) == 0
+    before = L.poly_last_cuda_error()            # the last POLY_ECUDA's code, per thread
     try:
         assert L.poly_act_fwd(0, 0, FAKE + 1, FAKE + 4096, 8, None) == B.POLY_EINVAL
         assert L.poly_act_fwd(0, 0, None, None, 0, None) == B.POLY_OK
-        assert L.poly_last_cuda_error() == 0
+        assert L.poly_last_cuda_error() == before
     finally:
         assert L.poly_debug_fail_launches(701, 0) == 2       # both still pending; cleared
 

@@ -572,6 +572,29 @@ def _strided_view(buf, off, rows, cols, ld):
     return torch.as_strided(buf, (rows, cols), (ld, 1), storage_offset=off)
 
 
+@pytest.mark.parametrize("H", [72, 21])
+@pytest.mark.parametrize("dt", DTS)
+def test_swiglu_fused_gate_up_halves(dt, H):
+    """Gate and up as the two halves of one [T, 2H] projection output, and
+    dg, du written into the two halves of one [T, 2H] gradient buffer
+    (leading dimension 2H everywhere): every element against the oracle."""
+    fmt = FMT[dt]
+    s_op, d_op = _swiglu_ops(dt)
+    rng = np.random.default_rng(91)
+    T = 37
+    gu = _rand_bits(rng, T * 2 * H, fmt).reshape(T, 2 * H)
+    dy = _rand_bits(rng, T * H, fmt).reshape(T, H)
+    gud = to_dev(gu, dt).view(T, 2 * H)
+    y = torch.empty((T, H), dtype=TDT[dt], device=DEV)
+    B.poly_swiglu_fwd(dt, gud[:, :H], gud[:, H:], y)
+    assert np.array_equal(from_dev(y).reshape(T, H), swiglu_forward(s_op, gu[:, :H], gu[:, H:]))
+    dgu = torch.full((T, 2 * H), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+    B.poly_swiglu_bwd(dt, gud[:, :H], gud[:, H:], to_dev(dy, dt).view(T, H), dgu[:, :H], dgu[:, H:])
+    wdg, wdu = swiglu_backward(s_op, d_op, gu[:, :H], gu[:, H:], dy)
+    got = from_dev(dgu).reshape(T, 2 * H)
+    assert np.array_equal(got[:, :H], wdg) and np.array_equal(got[:, H:], wdu)
+
+
 def test_swiglu_random_layouts_every_element():
     """48 seeded cases: rows 1-40, cols 1-70, a leading dimension and an
     element offset of its own for every stream (0-13 padding, 0-7 elements
