@@ -196,6 +196,16 @@ def _extent(rows, cols, ld):
     return (rows - 1) * ld + cols if rows > 0 and cols > 0 else 0
 
 
+def _rows(t, cols):
+    """Rows of a 2-D row-major view, or of a contiguous tensor of any rank
+    read as [numel / cols, cols] (e.g. [batch, tokens, hidden])."""
+    if t.dim() == 2:
+        return t.shape[0]
+    if t.is_contiguous() and cols > 0:
+        return t.numel() // cols
+    raise ValueError("tensor must be 2-D row-major or contiguous")
+
+
 def _ld(t, cols):
     """Leading dimension (elements) of a 2-D row-major view."""
     if t is None or isinstance(t, int):
@@ -277,8 +287,8 @@ def poly_ctrl_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
 
 
 def _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, name):
-    rows = g.shape[0] if rows is None else rows
     cols = g.shape[-1] if cols is None else cols
+    rows = _rows(g, cols) if rows is None else rows
     ldg = _ld(g, cols) if ldg is None else ldg
     ldu = _ld(u, cols) if ldu is None else ldu
     ldy = _ld(y, cols) if ldy is None else ldy
@@ -301,8 +311,8 @@ def poly_ctrl_swiglu_fwd(dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=Non
 
 
 def _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, lds, stream, name):
-    rows = g.shape[0] if rows is None else rows
     cols = g.shape[-1] if cols is None else cols
+    rows = _rows(g, cols) if rows is None else rows
     ts = (g, u, dy, dg, du)
     lds = [(_ld(t, cols) if l is None else l) for t, l in zip(ts, lds)]
     for t, nm, ld in zip(ts, ("g", "u", "dy", "dg", "du"), lds):
@@ -333,8 +343,8 @@ def _ragged_room(where, dtype, ts, names, seg_off, num_segments, cap_rows, cols,
 def poly_swiglu_fwd_ragged(dtype, g, u, y, seg_off, num_segments=None, cap_rows=None,
                            cols=None, status=None, stream=None):
     num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
-    cap_rows = g.shape[0] if cap_rows is None else cap_rows
     cols = g.shape[-1] if cols is None else cols
+    cap_rows = _rows(g, cols) if cap_rows is None else cap_rows
     _ragged_room("poly_swiglu_fwd_ragged", dtype, (g, u, y), ("g", "u", "y"), seg_off,
                  num_segments, cap_rows, cols, status)
     _check(lib().poly_swiglu_fwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(y), _ptr(seg_off),
@@ -345,8 +355,8 @@ def poly_swiglu_fwd_ragged(dtype, g, u, y, seg_off, num_segments=None, cap_rows=
 def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, cap_rows=None,
                            cols=None, status=None, stream=None):
     num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
-    cap_rows = g.shape[0] if cap_rows is None else cap_rows
     cols = g.shape[-1] if cols is None else cols
+    cap_rows = _rows(g, cols) if cap_rows is None else cap_rows
     _ragged_room("poly_swiglu_bwd_ragged", dtype, (g, u, dy, dg, du), ("g", "u", "dy", "dg", "du"),
                  seg_off, num_segments, cap_rows, cols, status)
     _check(lib().poly_swiglu_bwd_ragged(dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg), _ptr(du),

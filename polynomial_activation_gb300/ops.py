@@ -30,6 +30,12 @@ def act_bwd(fn: str, x: torch.Tensor, dy: torch.Tensor, out=None,
     return dx
 
 
+def _rows(t):
+    """t itself when it is a row-major 2-D view (any leading dimension, e.g.
+    one half of a [T, 2H] gate-up buffer), else a contiguous copy."""
+    return t if t.dim() == 2 and t.stride(1) == 1 else t.contiguous()
+
+
 def swiglu_fwd(g, u, out=None, control: bool = False):
     y = torch.empty(g.shape, dtype=g.dtype, device=g.device) if out is None else out
     (B.poly_ctrl_swiglu_fwd if control else B.poly_swiglu_fwd)(_dt(g), g, u, y)
@@ -98,14 +104,14 @@ class PolySwiGLU(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, g, u):
-        g, u = g.contiguous(), u.contiguous()
+        g, u = _rows(g), _rows(u)
         ctx.save_for_backward(g, u)
         return swiglu_fwd(g, u)
 
     @staticmethod
     def backward(ctx, dy):
         g, u = ctx.saved_tensors
-        return swiglu_bwd(g, u, dy.contiguous())
+        return swiglu_bwd(g, u, _rows(dy))
 
 
 def swiglu(g, u):

@@ -1015,6 +1015,12 @@ def test_autograd_wrappers_match_direct_calls():
         dg, du = ops.swiglu_bwd(g.detach(), u.detach(), dyy)
         assert torch.equal(g.grad.view(torch.int16), dg.view(torch.int16))
         assert torch.equal(u.grad.view(torch.int16), du.view(torch.int16))
+        # a [batch, tokens, hidden] input is read as [batch * tokens, hidden]
+        g3 = g.detach().reshape(4, 16, 256).requires_grad_(True)
+        y3 = ops.swiglu(g3, u.detach().reshape(4, 16, 256))
+        assert y3.shape == (4, 16, 256)
+        assert torch.equal(y3.detach().reshape(64, 256).view(torch.int16),
+                           ops.swiglu_fwd(g.detach(), u.detach()).view(torch.int16))
         # ragged: rows [0, 40) of a 64-row capacity; the rest stay zero
         seg = torch.tensor([0, 10, 10, 40], dtype=torch.int32, device=DEV)
         g.grad, u.grad = None, None
