@@ -171,15 +171,18 @@ def _check(status, where):
 
 def _room(t, nbytes, where, name, esize=2, dtype=None):
     """Check a tensor argument before its address crosses the C ABI (which
-    sees only pointers): device memory or pinned host memory, elements of
-    esize bytes, a declared FP16 / BF16 type that agrees with the call's
-    dtype, and at least nbytes from its first element to the end of its
-    storage.  Raw integer addresses are the caller's responsibility."""
+    sees only pointers): memory of the current device or pinned host memory,
+    elements of esize bytes, a declared FP16 / BF16 type that agrees with the
+    call's dtype, and at least nbytes from its first element to the end of
+    its storage.  Raw integer addresses are the caller's responsibility."""
     if t is None or isinstance(t, int):
         return
     import torch
     if not (t.is_cuda or t.is_pinned()):
         raise ValueError(f"{where}: {name} must be a CUDA tensor or pinned host memory")
+    if t.is_cuda and t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{where}: {name} is on cuda:{t.device.index}, the kernels run on the "
+                         f"current device cuda:{torch.cuda.current_device()}")
     if t.element_size() != esize:
         raise ValueError(f"{where}: {name} has {t.element_size()}-byte elements, expected {esize}")
     if dtype is not None and t.dtype in (torch.float16, torch.bfloat16) and _dtype_of(t) != dtype:
