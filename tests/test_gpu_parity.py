@@ -1050,6 +1050,52 @@ def test_autograd_wrappers_match_direct_calls():
     assert np.array_equal(from_dev(k.grad).reshape(gk.shape), gk)
 
 
+def test_every_degree_every_program_exhaustive():
+    """Programs of every degree D3-D6 (fitted by the library, installed with
+    poly_set_program) for every function, direction and format, over all
+    65,536 inputs against the oracle replay of the same descriptor; then
+    SwiGLU with non-default SiLU / SiLU' degree pairs."""
+    from oracle import fit
+    rng = np.random.default_rng(95)
+    try:
+        for dt in DTS:
+            fmt = FMT[dt]
+            xd = to_dev(X_ALL, dt)
+            dy = _rand_bits(rng, X_ALL.size, fmt)
+            dyd = to_dev(dy, dt)
+            out = torch.empty_like(xd)
+            for fn, d in PROGRAMS:
+                for D in (3, 4, 5, 6):
+                    p = B.poly_fit(fn, d, dt, D)
+                    B.poly_set_program(p)
+                    op = fit.make_program(fn, d, fmt, p.degree, p.li, p.lc, p.coefficients())
+                    if d == B.POLY_FWD:
+                        B.poly_act_fwd(fn, dt, xd, out)
+                        want = forward(op, X_ALL)
+                    else:
+                        B.poly_act_bwd(fn, dt, xd, dyd, out)
+                        want = backward(op, X_ALL, dy)
+                    assert np.array_equal(from_dev(out), want), (fn, d, fmt, D)
+            g = _rand_bits(rng, 48 * 80, fmt).reshape(48, 80)
+            u = _rand_bits(rng, 48 * 80, fmt).reshape(48, 80)
+            gd, ud = to_dev(g, dt).view(48, 80), to_dev(u, dt).view(48, 80)
+            for DS, DD in ((6, 3), (4, 6), (5, 5)):
+                ps, pd = B.poly_fit(B.POLY_SILU, 0, dt, DS), B.poly_fit(B.POLY_SILU, 1, dt, DD)
+                B.poly_set_program(ps)
+                B.poly_set_program(pd)
+                s_op = fit.make_program(B.POLY_SILU, 0, fmt, DS, ps.li, ps.lc, ps.coefficients())
+                d_op = fit.make_program(B.POLY_SILU, 1, fmt, DD, pd.li, pd.lc, pd.coefficients())
+                y, dg, du = (torch.empty_like(gd) for _ in range(3))
+                B.poly_swiglu_fwd(dt, gd, ud, y)
+                B.poly_swiglu_bwd(dt, gd, ud, ud, dg, du)
+                wdg, wdu = swiglu_backward(s_op, d_op, g, u, u)
+                assert np.array_equal(from_dev(y).reshape(48, 80), swiglu_forward(s_op, g, u))
+                assert np.array_equal(from_dev(dg).reshape(48, 80), wdg), (DS, DD)
+                assert np.array_equal(from_dev(du).reshape(48, 80), wdu), (DS, DD)
+    finally:
+        B.poly_reset_programs()
+
+
 def test_must_fail_perturbed_program_on_gpu():
     """The parity check can fail: install a program whose c_2 is one ulp off
     and the GPU output no longer equals the oracle's replay of the fitted
