@@ -1092,7 +1092,23 @@ def test_every_degree_every_program_exhaustive():
                 assert np.array_equal(from_dev(y).reshape(48, 80), swiglu_forward(s_op, g, u))
                 assert np.array_equal(from_dev(dg).reshape(48, 80), wdg), (DS, DD)
                 assert np.array_equal(from_dev(du).reshape(48, 80), wdu), (DS, DD)
+            # the sigmoid rule with sigmoid programs of degree 4-6
+            from oracle.replay import swiglu_sigmoid_backward, swiglu_sigmoid_forward
+            B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
+            for D in (4, 5, 6):
+                p = B.poly_fit(B.POLY_SIGMOID, 0, dt, D)
+                B.poly_set_program(p)
+                sig = fit.make_program(B.POLY_SIGMOID, 0, fmt, D, p.li, p.lc, p.coefficients())
+                y, dg, du = (torch.empty_like(gd) for _ in range(3))
+                B.poly_swiglu_fwd(dt, gd, ud, y)
+                B.poly_swiglu_bwd(dt, gd, ud, ud, dg, du)
+                wdg, wdu = swiglu_sigmoid_backward(sig, g, u, u)
+                assert np.array_equal(from_dev(y).reshape(48, 80), swiglu_sigmoid_forward(sig, g, u))
+                assert np.array_equal(from_dev(dg).reshape(48, 80), wdg), D
+                assert np.array_equal(from_dev(du).reshape(48, 80), wdu), D
+            B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
     finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
         B.poly_reset_programs()
 
 
