@@ -1107,6 +1107,18 @@ def test_every_degree_every_program_exhaustive():
                 assert np.array_equal(from_dev(dg).reshape(48, 80), wdg), D
                 assert np.array_equal(from_dev(du).reshape(48, 80), wdu), D
             B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+            # the softcap with tanh and tanh' programs of degree 3, 5 and 6
+            from oracle.replay import softcap_backward, softcap_forward
+            for D in (3, 5, 6):
+                pf, pb = B.poly_fit(B.POLY_TANH, 0, dt, D), B.poly_fit(B.POLY_TANH, 1, dt, D)
+                B.poly_set_program(pf)
+                B.poly_set_program(pb)
+                tf_op = fit.make_program(B.POLY_TANH, 0, fmt, D, pf.li, pf.lc, pf.coefficients())
+                tb_op = fit.make_program(B.POLY_TANH, 1, fmt, D, pb.li, pb.lc, pb.coefficients())
+                B.poly_softcap_fwd(dt, 30.0, xd, out)
+                assert np.array_equal(from_dev(out), softcap_forward(tf_op, 30.0, X_ALL)), D
+                B.poly_softcap_bwd(dt, 30.0, xd, dyd, out)
+                assert np.array_equal(from_dev(out), softcap_backward(tb_op, 30.0, X_ALL, dy)), D
     finally:
         B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
         B.poly_reset_programs()
