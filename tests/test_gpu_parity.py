@@ -1076,6 +1076,12 @@ def test_every_degree_every_program_exhaustive():
                         B.poly_act_bwd(fn, dt, xd, dyd, out)
                         want = backward(op, X_ALL, dy)
                     assert np.array_equal(from_dev(out), want), (fn, d, fmt, D)
+                    # one element off the 16-byte grid: the general kernel's head / body / tail
+                    if d == B.POLY_FWD:
+                        B.poly_act_fwd(fn, dt, xd[1:], out[1:])
+                    else:
+                        B.poly_act_bwd(fn, dt, xd[1:], dyd[1:], out[1:])
+                    assert np.array_equal(from_dev(out[1:]), want[1:]), (fn, d, fmt, D, "offset")
             g = _rand_bits(rng, 48 * 80, fmt).reshape(48, 80)
             u = _rand_bits(rng, 48 * 80, fmt).reshape(48, 80)
             gd, ud = to_dev(g, dt).view(48, 80), to_dev(u, dt).view(48, 80)
