@@ -169,6 +169,19 @@ def _check(status, where):
         raise PolyError(status, where)
 
 
+_TORCH = None
+_NDEV = None
+
+
+def _torch():
+    global _TORCH, _NDEV
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+        _NDEV = torch.cuda.device_count() if torch.cuda.is_available() else 0
+    return _TORCH
+
+
 def _room(t, nbytes, where, name, esize=2, dtype=None):
     """Check a tensor argument before its address crosses the C ABI (which
     sees only pointers): memory of the current device or pinned host memory,
@@ -177,17 +190,20 @@ def _room(t, nbytes, where, name, esize=2, dtype=None):
     its storage.  Raw integer addresses are the caller's responsibility."""
     if t is None or isinstance(t, int):
         return
-    import torch
-    if not (t.is_cuda or t.is_pinned()):
+    torch = _torch()
+    if t.is_cuda:
+        if _NDEV > 1 and t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{where}: {name} is on cuda:{t.device.index}, the kernels run on "
+                             f"the current device cuda:{torch.cuda.current_device()}")
+    elif not t.is_pinned():
         raise ValueError(f"{where}: {name} must be a CUDA tensor or pinned host memory")
-    if t.is_cuda and t.device.index != torch.cuda.current_device():
-        raise ValueError(f"{where}: {name} is on cuda:{t.device.index}, the kernels run on the "
-                         f"current device cuda:{torch.cuda.current_device()}")
     if t.element_size() != esize:
         raise ValueError(f"{where}: {name} has {t.element_size()}-byte elements, expected {esize}")
     if dtype is not None and t.dtype in (torch.float16, torch.bfloat16) and _dtype_of(t) != dtype:
         raise ValueError(f"{where}: {name} is {t.dtype}, which is not the call's dtype")
-    if nbytes > 0:
+    if nbytes > 0 and not (t.is_contiguous() and t.numel() * esize >= nbytes):
+        # views: judge by the storage from the first element on (an expanded,
+        # stride-0 tensor is judged by what it owns, not by its shape)
         avail = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
         if avail < nbytes:
             raise ValueError(f"{where}: {name} has {avail} bytes from its first element; the "

@@ -75,6 +75,7 @@ __host__ __device__ constexpr int chunks_per_thread() {
   return Op::NIN == 1 ? 2 : 1;
 }
 constexpr int kMinBlocksPerSm = 4;
+constexpr int64_t kRowsTwoOutMax = int64_t(1) << 19;
 
 template <class Op>
 __device__ __forceinline__ void apply_chunk(const uint4 (&in)[Op::NIN], uint4 (&out)[Op::NOUT],
@@ -190,37 +191,68 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
   }
 }
 
-// Dense: the flat layout when every stream starts on a 16-byte boundary and
-// n < 2^31 -- the common case -- with 32-bit indices, no layout branches and
-// no loop: the grid covers the body exactly once, and the last block also
-// evaluates the n mod 8 tail elements.  With RAGGED the range is the rows
-// read from the device offsets (cols % 8 == 0 and cap_rows * cols < 2^31, so
-// every row starts on a 16-byte boundary and there is no tail); the grid
-// covers cap_rows and blocks past the last row only return.
-struct DenseRagged {
-  const int32_t *seg;
-  int32_t nseg;
-  int32_t cap_rows;
-  uint32_t cols;
+// Dense: the common layouts with 32-bit indices, no layout branches and no
+// loop (the grid covers the body exactly once).
+//   kDenseFlat    n < 2^31 contiguous elements, every stream on a 16-byte
+//                 boundary; the last block also evaluates the n mod 8 tail.
+//   kDenseRagged  the rows read from the device offsets (cols % 8 == 0 and
+//                 cap_rows * cols < 2^31, so every row starts on a 16-byte
+//                 boundary and there is no tail); the grid covers cap_rows and
+//                 blocks past the last row only return.
+//   kDenseRows    rows x cols with a leading dimension per stream, every row
+//                 start on a 16-byte boundary and every extent below 2^31
+//                 elements (e.g. the gate and up halves of one [T, 2H]
+//                 buffer); the row of a chunk comes from a multiply and a
+//                 shift instead of a division.
+enum DenseMode { kDenseFlat = 0, kDenseRagged = 1, kDenseRows = 2 };
+
+struct DenseArgs {
+  uint32_t nvec, ntail;            // chunks of 8 elements; flat tail elements
+  const int32_t *seg;              // ragged: device offsets, their count,
+  int32_t nseg, cap_rows;          //   the row capacity and the status word
   int32_t *status;
+  uint32_t cols;                   // ragged / rows: elements per row
+  uint32_t cpr, mul, shift;        // rows: chunks per row and floor(c / cpr) =
+                                   //   (c * mul) >> shift for every c < 2^31
+  uint32_t ld_in[3], ld_out[2];    // rows: leading dimensions in elements
 };
 
-template <class Op, bool RAGGED, int U>
-__global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nvec,
-                                                         uint32_t ntail, DenseRagged g,
+// Division constants for numerators below 2^31 (the round-up reciprocal:
+// with l = ceil(log2 d) and m = ceil(2^(31+l) / d), m * d lies in
+// [2^(31+l), 2^(31+l) + 2^l), which makes floor(n m / 2^(31+l)) = floor(n / d)).
+inline void row_divisor(uint32_t d, uint32_t &mul, uint32_t &shift) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  mul = (uint32_t)(((uint64_t(1) << (31 + l)) + d - 1) / d);
+  shift = 31 + l;
+}
+
+template <int MODE>
+__device__ __forceinline__ uint32_t chunk_offset(uint32_t i, const DenseArgs &a, uint32_t ld) {
+  if constexpr (MODE == kDenseRows) {
+    const uint32_t row = (uint32_t)(((uint64_t)i * a.mul) >> a.shift);
+    return row * ld + (i - row * a.cpr) * 8;
+  } else {
+    return i * 8;
+  }
+}
+
+template <class Op, int MODE, int U>
+__global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, DenseArgs a,
                                                          typename Op::Params p) {
   pdl_enter();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
-  if constexpr (RAGGED) {
+  uint32_t nvec = a.nvec;
+  if constexpr (MODE == kDenseRagged) {
     int64_t lo, hi;
-    ragged_rows(g.seg, g.nseg, g.cap_rows, g.status, lo, hi);
-    const size_t off = (size_t)lo * g.cols;
+    ragged_rows(a.seg, a.nseg, a.cap_rows, a.status, lo, hi);
+    const size_t off = (size_t)lo * a.cols;
 #pragma unroll
     for (int k = 0; k < Op::NIN; ++k) src[k] += off;
 #pragma unroll
     for (int k = 0; k < Op::NOUT; ++k) dst[k] += off;
-    nvec = (uint32_t)(((uint64_t)(hi - lo) * g.cols) >> 3);
+    nvec = (uint32_t)(((uint64_t)(hi - lo) * a.cols) >> 3);
   }
   const uint32_t base = blockIdx.x * (uint32_t)(kThreads * U) + threadIdx.x;
   uint4 r[U][Op::NIN];
@@ -229,7 +261,8 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nve
     const uint32_t i = base + u * kThreads;
     if (i < nvec) {
 #pragma unroll
-      for (int k = 0; k < Op::NIN; ++k) r[u][k] = ld_stream(src[k] + (size_t)i * 8);
+      for (int k = 0; k < Op::NIN; ++k)
+        r[u][k] = ld_stream(src[k] + chunk_offset<MODE>(i, a, a.ld_in[k]));
     }
   }
 #pragma unroll
@@ -239,10 +272,12 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, uint32_t nve
       uint4 o[Op::NOUT];
       apply_chunk<Op>(r[u], o, p);
 #pragma unroll
-      for (int k = 0; k < Op::NOUT; ++k) st_stream(dst[k] + (size_t)i * 8, o[k]);
+      for (int k = 0; k < Op::NOUT; ++k)
+        st_stream(dst[k] + chunk_offset<MODE>(i, a, a.ld_out[k]), o[k]);
     }
   }
-  if (!RAGGED && ntail != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x < ntail) {
+  if (MODE == kDenseFlat && a.ntail != 0 && blockIdx.x == gridDim.x - 1 &&
+      threadIdx.x < a.ntail) {
     const uint16_t *in[Op::NIN];
     uint16_t *out[Op::NOUT];
 #pragma unroll
@@ -331,36 +366,58 @@ inline bool aligned16(const Streams &s) {
 template <class Op>
 cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Params &p,
                       cudaStream_t stream) {
+  constexpr int U = chunks_per_thread<Op>();
+  const int64_t per_block = (int64_t)kThreads * 8 * U;
+  const int64_t lim = int64_t(1) << 31;
   if constexpr (Op::TWO_D) {
     if (l.mode == kStrided) {
+      // two-output operations (the SwiGLU backward) keep the strided kernel
+      // above 2^19 chunks: measured 3-8 % faster there on GB300, while the
+      // rows mode wins below and for every single-output operation
+      bool fast = l.vec && l.rows * (l.cols >> 3) < (Op::NOUT == 1 ? lim : kRowsTwoOutMax);
+      for (int k = 0; k < 3; ++k) fast &= (l.rows - 1) * l.ld_in[k] + l.cols < lim;
+      for (int k = 0; k < 2; ++k) fast &= (l.rows - 1) * l.ld_out[k] + l.cols < lim;
+      if (fast) {
+        DenseArgs a{};
+        a.cpr = (uint32_t)(l.cols >> 3);
+        a.nvec = (uint32_t)(l.rows * a.cpr);
+        row_divisor(a.cpr, a.mul, a.shift);
+        for (int k = 0; k < 3; ++k) a.ld_in[k] = (uint32_t)l.ld_in[k];
+        for (int k = 0; k < 2; ++k) a.ld_out[k] = (uint32_t)l.ld_out[k];
+        int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
+        if (blocks < 1) blocks = 1;
+        return launch_pdl(dense_kernel<Op, kDenseRows, U>, blocks, kThreads, stream, s, a, p);
+      }
       const int64_t blocks = grid_for(l, l.vec ? 8 : 1);
       return launch_pdl(strided_kernel<Op>, blocks, kThreads, stream, s, l, p);
     }
   }
   if (l.mode == kStrided) return cudaErrorInvalidValue;
-  constexpr int U = chunks_per_thread<Op>();
-  const int64_t per_block = (int64_t)kThreads * 8 * U;
-  if (l.mode == kFlat && l.n < (int64_t(1) << 31) && aligned16(s)) {
-    const int64_t nvec = l.n >> 3;
-    int64_t blocks = (nvec * 8 + per_block - 1) / per_block;
+  if (l.mode == kFlat && l.n < lim && aligned16(s)) {
+    DenseArgs a{};
+    a.nvec = (uint32_t)(l.n >> 3);
+    a.ntail = (uint32_t)(l.n & 7);
+    int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
     if constexpr (U > 1) {
       if (blocks < (int64_t)kMinBlocksPerSm * sm_count()) {
-        blocks = (nvec + kThreads - 1) / kThreads;
+        blocks = ((int64_t)a.nvec + kThreads - 1) / kThreads;
         if (blocks < 1) blocks = 1;
-        return launch_pdl(dense_kernel<Op, false, 1>, blocks, kThreads, stream, s,
-                          (uint32_t)nvec, (uint32_t)(l.n & 7), DenseRagged{}, p);
+        return launch_pdl(dense_kernel<Op, kDenseFlat, 1>, blocks, kThreads, stream, s, a, p);
       }
     }
-    return launch_pdl(dense_kernel<Op, false, U>, blocks, kThreads, stream, s, (uint32_t)nvec,
-                      (uint32_t)(l.n & 7), DenseRagged{}, p);
+    return launch_pdl(dense_kernel<Op, kDenseFlat, U>, blocks, kThreads, stream, s, a, p);
   }
-  if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < (int64_t(1) << 31) &&
-      aligned16(s)) {
-    const DenseRagged g{l.seg, l.nseg, (int32_t)l.cap_rows, (uint32_t)l.cols, l.status};
+  if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < lim && aligned16(s)) {
+    DenseArgs a{};
+    a.seg = l.seg;
+    a.nseg = l.nseg;
+    a.cap_rows = (int32_t)l.cap_rows;
+    a.status = l.status;
+    a.cols = (uint32_t)l.cols;
     int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(dense_kernel<Op, true, U>, blocks, kThreads, stream, s, 0u, 0u, g, p);
+    return launch_pdl(dense_kernel<Op, kDenseRagged, U>, blocks, kThreads, stream, s, a, p);
   }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);

@@ -155,6 +155,8 @@ def test_binding_checks_tensor_extents_before_launch():
         B.poly_act_fwd(B.POLY_SIGMOID, B.POLY_BF16, x, y)
     with pytest.raises(ValueError, match="pinned"):
         B.poly_act_fwd(B.POLY_SIGMOID, dt, x, torch.empty(1000, dtype=torch.float16))
+    with pytest.raises(ValueError, match="x"):                        # owns 2 bytes, shows 1000
+        B.poly_act_fwd(B.POLY_SIGMOID, dt, torch.zeros(1, dtype=torch.float16, device=DEV).expand(1000), y)
     qb = torch.zeros((1, 4, 2, 8), dtype=torch.bfloat16, device=DEV)
     dlt = torch.from_numpy(B.poly_rope_turn_increments(8).view(np.int32)).to(DEV)
     with pytest.raises(ValueError, match="dtype"):                    # RoPE is FP16 only
@@ -593,6 +595,29 @@ def test_swiglu_fused_gate_up_halves(dt, H):
     wdg, wdu = swiglu_backward(s_op, d_op, gu[:, :H], gu[:, H:], dy)
     got = from_dev(dgu).reshape(T, 2 * H)
     assert np.array_equal(got[:, :H], wdg) and np.array_equal(got[:, H:], wdu)
+
+
+def test_swiglu_fused_halves_large_every_element():
+    """Gate / up and dg / du as halves of [T, 2H] buffers above the size at
+    which the backward changes kernel (T = 2100, H = 2048: 537,600 chunks of
+    8), every element through the oracle's exhaustive tables, products
+    rounded once."""
+    dt = B.POLY_BF16
+    s_op, d_op = _swiglu_ops(dt)
+    T, H = 2100, 2048
+    rng = np.random.default_rng(97)
+    gu = to_dev(_rand_bits(rng, T * 2 * H, "bf16"), dt).view(T, 2 * H)
+    dyd = to_dev(_rand_bits(rng, T * H, "bf16"), dt).view(T, H)
+    g, u = gu[:, :H], gu[:, H:]
+    y = torch.empty((T, H), dtype=TDT[dt], device=DEV)
+    B.poly_swiglu_fwd(dt, g, u, y)
+    dgu = torch.empty_like(gu)
+    B.poly_swiglu_bwd(dt, g, u, dyd, dgu[:, :H], dgu[:, H:])
+    gc, uc = g.contiguous(), u.contiguous()
+    sg, sdg = _apply_lut(s_op, gc), _apply_lut(d_op, gc)
+    assert _equal_bits(y, _rn_mul(sg, uc))
+    assert _equal_bits(dgu[:, :H].contiguous(), _rn_mul(_rn_mul(dyd, uc), sdg))
+    assert _equal_bits(dgu[:, H:].contiguous(), _rn_mul(dyd, sg))
 
 
 def test_swiglu_random_layouts_every_element():
