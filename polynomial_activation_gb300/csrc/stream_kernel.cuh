@@ -227,13 +227,14 @@ inline void row_divisor(uint32_t d, uint32_t &mul, uint32_t &shift) {
   shift = 31 + l;
 }
 
+// Element offset of chunk i (the flat form stays one wide multiply-add).
 template <int MODE>
-__device__ __forceinline__ uint32_t chunk_offset(uint32_t i, const DenseArgs &a, uint32_t ld) {
+__device__ __forceinline__ size_t chunk_offset(uint32_t i, const DenseArgs &a, uint32_t ld) {
   if constexpr (MODE == kDenseRows) {
     const uint32_t row = (uint32_t)(((uint64_t)i * a.mul) >> a.shift);
-    return row * ld + (i - row * a.cpr) * 8;
+    return (size_t)(row * ld + (i - row * a.cpr) * 8);
   } else {
-    return i * 8;
+    return (size_t)i * 8;
   }
 }
 
