@@ -1155,6 +1155,62 @@ def test_every_degree_every_program_exhaustive():
         B.poly_reset_programs()
 
 
+def _random_program(rng, fn, d, dt, D):
+    """A descriptor the library accepts with arbitrary coefficient bits:
+    ordinary, subnormal, huge, infinite and NaN patterns mixed in."""
+    fmt = FMT[dt]
+    p = B.PolyProgram()
+    p.fn, p.dir, p.dtype, p.degree = fn, d, dt, D
+    p.form = B.lib().poly_form_of(fn, d)
+    coef = _rand_bits(rng, D + 1, fmt)
+    sp = np.array([0x0001, 0x8003, 0x7BFF, 0xFC00, 0x7E01] if fmt == "f16" else
+                  [0x0001, 0x8003, 0x7F7F, 0xFF80, 0x7FC1], dtype=np.uint16)
+    pick = rng.random(D + 1) < 0.25
+    coef[pick] = sp[rng.integers(0, sp.size, int(pick.sum()))]
+    if p.form != B.POLY_FORM_E:
+        coef[0] = 0                                  # c0 = f(0) = 0 for these forms
+    for j in range(D + 1):
+        p.coef[j] = int(coef[j])
+    lc = float(rng.uniform(0.25, 20.0))
+    p.lc_bits = int(tf.from_f64(lc, fmt))
+    p.lc = float(tf.decode(np.uint16(p.lc_bits), fmt))
+    p.li = p.lc
+    p.version = 1
+    return p
+
+
+def test_random_descriptors_exhaustive():
+    """Any descriptor the library accepts -- here random coefficient bits,
+    specials included, with a random clamp -- is evaluated bit-exactly: every
+    form and degree D3-D6, both formats, all 65,536 inputs, three descriptors
+    each."""
+    from oracle import fit
+    rng = np.random.default_rng(99)
+    try:
+        for dt in DTS:
+            fmt = FMT[dt]
+            xd = to_dev(X_ALL, dt)
+            dy = _rand_bits(rng, X_ALL.size, fmt)
+            dyd = to_dev(dy, dt)
+            out = torch.empty_like(xd)
+            for fn, d in PROGRAMS:
+                for D in (3, 4, 5, 6):
+                    for _ in range(3):
+                        p = _random_program(rng, fn, d, dt, D)
+                        B.poly_set_program(p)
+                        op = fit.make_program(fn, d, fmt, D, p.li, p.lc, p.coefficients())
+                        assert op.lc_bits == p.lc_bits
+                        if d == B.POLY_FWD:
+                            B.poly_act_fwd(fn, dt, xd, out)
+                            want = forward(op, X_ALL)
+                        else:
+                            B.poly_act_bwd(fn, dt, xd, dyd, out)
+                            want = backward(op, X_ALL, dy)
+                        assert np.array_equal(from_dev(out), want), (fn, d, fmt, D, p.coefficients())
+    finally:
+        B.poly_reset_programs()
+
+
 def test_must_fail_perturbed_program_on_gpu():
     """The parity check can fail: install a program whose c_2 is one ulp off
     and the GPU output no longer equals the oracle's replay of the fitted
