@@ -1207,7 +1207,46 @@ def test_random_descriptors_exhaustive():
                             B.poly_act_bwd(fn, dt, xd, dyd, out)
                             want = backward(op, X_ALL, dy)
                         assert np.array_equal(from_dev(out), want), (fn, d, fmt, D, p.coefficients())
+            # the fused kernels with random descriptors: SwiGLU (both rules), softcap
+            from oracle.replay import (softcap_backward, softcap_forward,
+                                       swiglu_sigmoid_backward, swiglu_sigmoid_forward)
+            g = _rand_bits(rng, 32 * 64, fmt).reshape(32, 64)
+            u = _rand_bits(rng, 32 * 64, fmt).reshape(32, 64)
+            gd, ud = to_dev(g, dt).view(32, 64), to_dev(u, dt).view(32, 64)
+            mk = lambda q: fit.make_program(q.fn, q.dir, fmt, q.degree, q.li, q.lc, q.coefficients())
+            for D in (3, 5, 6):
+                ps = _random_program(rng, B.POLY_SILU, 0, dt, D)
+                pd = _random_program(rng, B.POLY_SILU, 1, dt, 9 - D)
+                psig = _random_program(rng, B.POLY_SIGMOID, 0, dt, D)
+                for q in (ps, pd, psig):
+                    B.poly_set_program(q)
+                y, dg, du = (torch.empty_like(gd) for _ in range(3))
+                B.poly_swiglu_fwd(dt, gd, ud, y)
+                B.poly_swiglu_bwd(dt, gd, ud, ud, dg, du)
+                wdg, wdu = swiglu_backward(mk(ps), mk(pd), g, u, u)
+                assert np.array_equal(from_dev(y).reshape(32, 64), swiglu_forward(mk(ps), g, u))
+                assert np.array_equal(from_dev(dg).reshape(32, 64), wdg)
+                assert np.array_equal(from_dev(du).reshape(32, 64), wdu)
+                B.poly_set_swiglu_variant(B.POLY_SWIGLU_SIGMOID)
+                try:
+                    B.poly_swiglu_fwd(dt, gd, ud, y)
+                    B.poly_swiglu_bwd(dt, gd, ud, ud, dg, du)
+                finally:
+                    B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+                wdg, wdu = swiglu_sigmoid_backward(mk(psig), g, u, u)
+                assert np.array_equal(from_dev(y).reshape(32, 64),
+                                      swiglu_sigmoid_forward(mk(psig), g, u))
+                assert np.array_equal(from_dev(dg).reshape(32, 64), wdg)
+                assert np.array_equal(from_dev(du).reshape(32, 64), wdu)
+                pt, ptd = (_random_program(rng, B.POLY_TANH, dd, dt, D) for dd in (0, 1))
+                B.poly_set_program(pt)
+                B.poly_set_program(ptd)
+                B.poly_softcap_fwd(dt, 30.0, xd, out)
+                assert np.array_equal(from_dev(out), softcap_forward(mk(pt), 30.0, X_ALL))
+                B.poly_softcap_bwd(dt, 30.0, xd, dyd, out)
+                assert np.array_equal(from_dev(out), softcap_backward(mk(ptd), 30.0, X_ALL, dy))
     finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
         B.poly_reset_programs()
 
 
