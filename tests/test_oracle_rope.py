@@ -4,7 +4,6 @@ endpoint-constrained sine/cosine fits, the packed-FP16 programs over every
 Q15 coordinate, the rotation in exact rationals, identity at position 0 and
 the FP64 complex-multiplication reference."""
 import math
-from fractions import Fraction
 
 import numpy as np
 import pytest
