@@ -804,6 +804,35 @@ def test_derived_program_backward_exhaustive(dt, fn, D):
         B.poly_reset_programs()
 
 
+def test_derived_programs_every_degree():
+    """Forward programs of degree 3-6 (sigmoid centred-odd, tanh odd) in both
+    formats, differentiated by the library and by the oracle into even
+    programs of degree 2-5: equal coefficients, and the backward kernel
+    equals the oracle over every input."""
+    from oracle import fit
+    from oracle.replay import derive
+    rng = np.random.default_rng(33)
+    try:
+        for dt in DTS:
+            fmt = FMT[dt]
+            xd = to_dev(X_ALL, dt)
+            dy = _rand_bits(rng, X_ALL.size, fmt)
+            dyd = to_dev(dy, dt)
+            out = torch.empty_like(xd)
+            for fn in (B.POLY_SIGMOID, B.POLY_TANH):
+                for D in (3, 4, 5, 6):
+                    fwd = B.poly_fit(fn, B.POLY_FWD, dt, D)
+                    d = B.poly_derive_program(fwd)
+                    od = derive(fit.make_program(fn, B.POLY_FWD, fmt, D, fwd.li, fwd.lc,
+                                                 fwd.coefficients()))
+                    assert d.degree == D - 1 and d.coefficients() == list(od.coef), (fn, D)
+                    B.poly_set_program(d)
+                    B.poly_act_bwd(fn, dt, xd, dyd, out)
+                    assert np.array_equal(from_dev(out), backward(od, X_ALL, dy)), (fn, fmt, D)
+    finally:
+        B.poly_reset_programs()
+
+
 # ------------------------------------------------------------------- exp2
 
 def _exp2_inputs():
