@@ -941,6 +941,47 @@ def test_rope_poly_bit_exact(shape, pos):
     assert torch.equal(ko2.view(torch.int16), ko.view(torch.int16))
 
 
+def test_rope_random_shapes():
+    """24 seeded random shapes -- batch 1-3, sequence 1-70, Hq 0-19, Hkv 0-9
+    (so eight-head chunks straddle the Q / K boundary), head dimension 8-256,
+    random position offsets -- forward and backward bit for bit, and the
+    table variant fed the oracle's tables."""
+    from oracle import rope
+    rng = np.random.default_rng(123)
+    for case in range(24):
+        b, s = int(rng.integers(1, 4)), int(rng.integers(1, 71))
+        hq, hkv = int(rng.integers(0, 20)), int(rng.integers(0, 10))
+        if hq + hkv == 0:
+            hq = 1
+        d = 8 * int(rng.integers(1, 33))
+        pos = int(rng.integers(0, (1 << 32) - s))
+        q, k = _rope_case(rng, b, s, hq, hkv, d)
+        delta = rope.turn_increments(d)
+        dd = torch.from_numpy(delta.view(np.int32)).to(DEV)
+        qd, kd = to_dev(q, 0), to_dev(k, 0)
+        qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=DEV)
+        ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=DEV)
+        dims = dict(batch=b, seq=s, hq=hq, hkv=hkv, head_dim=d, pos_offset=pos)
+        B.poly_rope_fwd(B.POLY_ROPE_POLY, qd, kd, qo, ko, dd, **dims)
+        wq, wk = rope.rope_forward(q, k, delta, pos)
+        where = (case, b, s, hq, hkv, d, pos)
+        assert np.array_equal(from_dev(qo).reshape(wq.shape), wq), where
+        assert np.array_equal(from_dev(ko).reshape(wk.shape), wk), where
+        gq = torch.empty((b, s, hq, d), dtype=torch.float16, device=DEV)
+        gk = torch.empty((b, s, hkv, d), dtype=torch.float16, device=DEV)
+        B.poly_rope_bwd(B.POLY_ROPE_POLY, qo, ko, gq, gk, dd, **dims)
+        bq, bk = rope.rope_backward(wq, wk, delta, pos)
+        assert np.array_equal(from_dev(gq).reshape(bq.shape), bq), where
+        assert np.array_equal(from_dev(gk).reshape(bk.shape), bk), where
+        cs, sn = rope.tables(s, delta, pos)
+        qo2, ko2 = torch.empty_like(qo), torch.empty_like(ko)
+        B.poly_rope_fwd(B.POLY_ROPE_TABLE, qd, kd, qo2, ko2, None,
+                        torch.from_numpy(cs.view(np.int16)).to(DEV),
+                        torch.from_numpy(sn.view(np.int16)).to(DEV), **dims)
+        assert torch.equal(qo2.view(torch.int16), qo.view(torch.int16)), where
+        assert torch.equal(ko2.view(torch.int16), ko.view(torch.int16)), where
+
+
 def test_rope_mufu_variant_accuracy():
     from oracle import rope
     b, s, hq, hkv, d = 1, 512, 4, 2, 128
