@@ -123,3 +123,39 @@ def fit_rows(path: str, rows, opts=None):
         have.add(tuple(row))
         save(progs, path)
     return progs
+
+
+def _parse_row(text: str):
+    """'sigmoid:fwd:bf16:3' -> (fn, dir, dtype, degree)."""
+    fn, d, dt, deg = text.split(":")
+    return (B.FN[fn], B.POLY_BWD if d == "bwd" else B.POLY_FWD, _DTYPE_IDS[dt], int(deg))
+
+
+def main(argv=None) -> int:
+    """Command line: fit rows into a file (resumable), show or verify one."""
+    import argparse
+    ap = argparse.ArgumentParser(prog="python -m polynomial_activation_gb300.programs")
+    sub = ap.add_subparsers(dest="cmd", required=True)
+    f = sub.add_parser("fit", help="fit the missing rows into FILE (rows: fn:dir:dtype:degree)")
+    f.add_argument("file")
+    f.add_argument("rows", nargs="+")
+    for name in ("show", "verify"):
+        sub.add_parser(name).add_argument("file")
+    a = ap.parse_args(argv)
+    if a.cmd == "fit":
+        progs = fit_rows(a.file, [_parse_row(r) for r in a.rows])
+        print(f"{a.file}: {len(progs)} programs")
+        return 0
+    progs = load(a.file)                               # verifies every hash
+    if a.cmd == "show":
+        for p in progs:
+            r = to_record(p)
+            print(f"{r['fn']}.{r['dir']}.{r['dtype']}.D{r['degree']}  Li={r['li']:g} "
+                  f"Lc={r['lc']:g}  bound={r['stated_max_abs_err']:.4e}  {r['sha256'][:12]}")
+    else:
+        print(f"{a.file}: {len(progs)} programs, every hash verified")
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

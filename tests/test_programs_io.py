@@ -85,3 +85,19 @@ def test_fit_rows_resumes(tmp_path, monkeypatch):
     progs = P.fit_rows(path, rows)                 # only the missing row is fitted
     assert calls[2:] == [rows[2]]
     assert [(p.fn, p.dir, p.dtype, p.degree) for p in progs] == rows
+
+
+def test_command_line_fit_show_verify(tmp_path, capsys):
+    path = str(tmp_path / "cli.json")
+    assert P.main(["fit", path, "tanh:fwd:bf16:4", "sigmoid:bwd:f16:4"]) == 0
+    assert P.main(["fit", path, "tanh:fwd:bf16:4", "gelu:fwd:bf16:5"]) == 0   # resumes
+    assert len(P.load(path)) == 3
+    assert P.main(["show", path]) == 0
+    out = capsys.readouterr().out
+    assert "tanh.fwd.bf16.D4" in out and "gelu.fwd.bf16.D5" in out
+    assert P.main(["verify", path]) == 0
+    doc = json.load(open(path))
+    doc["programs"][0]["coef"][1] = "0x0000"
+    json.dump(doc, open(path, "w"))
+    with pytest.raises(ValueError):
+        P.main(["verify", path])
