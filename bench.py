@@ -219,12 +219,15 @@ def oracle_sample_time(n_sample):
     from oracle.replay import backward, forward
     x, dy = workloads.isolated_hbm("f16", n=n_sample)
     progs = oracle_programs()
+    piece = 1 << 22                 # bounds the replay's FP64 temporaries
     t0 = time.perf_counter()
-    for p, (name, d, D) in zip(progs, SIX):
-        if d == 0:
-            forward(p, x)
-        else:
-            backward(p, x, dy)
+    for lo in range(0, n_sample, piece):
+        xs, dys = x[lo:lo + piece], dy[lo:lo + piece]
+        for p, (name, d, D) in zip(progs, SIX):
+            if d == 0:
+                forward(p, xs)
+            else:
+                backward(p, xs, dys)
     return time.perf_counter() - t0, 6 * n_sample
 
 
@@ -273,7 +276,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="only the timed step")
-    ap.add_argument("--cpu-sample", type=int, default=1 << 20,
+    ap.add_argument("--cpu-sample", type=int, default=1 << 24,
                     help="elements per program for the CPU oracle baseline (0 = skip)")
     ap.add_argument("--elements", type=int, default=workloads.N_HBM,
                     help="tensor size (a smaller case for profiling runs)")
