@@ -411,6 +411,7 @@ def main():
         result["rope"] = rope_extras(dev, stream, peak)
         result["swiglu"] = swiglu_extras(args, dev, stream, peak)
         result["l2_resident"] = l2_extras(dev, stream)
+        result["host_us_per_call"] = host_cost_extras(dev)
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
@@ -682,6 +683,48 @@ def l2_extras(dev, stream):
         tc = _time_graph(lambda: out[:m].copy_(big[:m]), 200)
         curve[str(m)] = {"poly_us": tp * 1e3, "copy_us": tc * 1e3, "poly_gbs": 4 * m / tp / 1e6}
     res["size_curve_sigmoid_fwd"] = curve
+    return res
+
+
+def host_cost_extras(dev, reps=5000):
+    """Host time per eager call (microseconds) for a decode-sized tensor, the
+    library's calls beside torch's own: the binding with a preallocated
+    output, the allocating wrappers without and with an autograd node, and
+    the fused SwiGLU against torch's two kernels.  The loop is host-bound
+    (the kernels take ~2 us), so wall time per call is the host cost."""
+    import torch
+    from polynomial_activation_gb300 import binding as B, ops
+    F = torch.nn.functional
+    x = torch.randn(14336, device=dev).half()
+    dy, y = torch.randn_like(x), torch.empty_like(x)
+    xr = x.clone().requires_grad_(True)
+    g = torch.randn(8, 1792, device=dev).bfloat16()
+    u = torch.randn_like(g)
+    cases = {
+        "binding_act_fwd_preallocated": lambda: B.poly_act_fwd(B.POLY_SIGMOID, B.POLY_F16, x, y),
+        "torch_sigmoid_out": lambda: torch.sigmoid(x, out=y),
+        "binding_act_bwd_preallocated": lambda: B.poly_act_bwd(B.POLY_SIGMOID, B.POLY_F16, x, dy, y),
+        "torch_sigmoid_backward": lambda: torch.ops.aten.sigmoid_backward(dy, x),
+        "ops_sigmoid": lambda: ops.sigmoid(x),
+        "torch_sigmoid": lambda: torch.sigmoid(x),
+        "ops_sigmoid_recorded": lambda: ops.sigmoid(xr),
+        "torch_sigmoid_recorded": lambda: torch.sigmoid(xr),
+        "ops_swiglu_8x1792": lambda: ops.swiglu(g, u),
+        "torch_silu_mul_8x1792": lambda: F.silu(g) * u,
+    }
+    res = {}
+    for k, f in cases.items():
+        for _ in range(200):
+            f()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            f()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        res[k] = (t1 - t0) / reps * 1e6
+    res["config"] = (f"FP16 x of 14,336 elements (BF16 8 x 1,792 for SwiGLU), mean host time "
+                     f"per call over {reps} eager calls, microseconds")
     return res
 
 

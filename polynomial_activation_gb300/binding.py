@@ -150,18 +150,31 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_CURRENT_STREAM = None
+
+
+def _current_stream_fn():
+    """A function returning the current device's current CUDA stream handle.
+    torch's raw-stream query skips building a torch.cuda.Stream object (about
+    2 us per call); where this torch lacks it, the public API is used."""
+    global _CURRENT_STREAM
+    torch = _torch()
+    C = torch._C
+    if hasattr(C, "_cuda_getCurrentRawStream") and hasattr(C, "_cuda_getDevice"):
+        torch.cuda.init()
+        raw, device = C._cuda_getCurrentRawStream, C._cuda_getDevice
+        _CURRENT_STREAM = lambda: raw(device())
+    else:
+        _CURRENT_STREAM = lambda: torch.cuda.current_stream().cuda_stream
+    return _CURRENT_STREAM
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return (_CURRENT_STREAM or _current_stream_fn())()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
-
-
-def _dtype_of(t):
-    import torch
-    return {torch.float16: POLY_F16, torch.bfloat16: POLY_BF16}[t.dtype]
 
 
 def _check(status, where):
@@ -171,14 +184,16 @@ def _check(status, where):
 
 _TORCH = None
 _NDEV = None
+_HALF_IDS = {}              # torch half dtypes -> POLY_F16 / POLY_BF16
 
 
 def _torch():
     global _TORCH, _NDEV
     if _TORCH is None:
         import torch
-        _TORCH = torch
+        _HALF_IDS.update({torch.float16: POLY_F16, torch.bfloat16: POLY_BF16})
         _NDEV = torch.cuda.device_count() if torch.cuda.is_available() else 0
+        _TORCH = torch
     return _TORCH
 
 
@@ -197,10 +212,15 @@ def _room(t, nbytes, where, name, esize=2, dtype=None):
                              f"the current device cuda:{torch.cuda.current_device()}")
     elif not t.is_pinned():
         raise ValueError(f"{where}: {name} must be a CUDA tensor or pinned host memory")
-    if t.element_size() != esize:
+    tdt = t.dtype
+    declared = _HALF_IDS.get(tdt)
+    if declared is not None:
+        if esize != 2:
+            raise ValueError(f"{where}: {name} has 2-byte elements, expected {esize}")
+        if dtype is not None and declared != dtype:
+            raise ValueError(f"{where}: {name} is {tdt}, which is not the call's dtype")
+    elif t.element_size() != esize:
         raise ValueError(f"{where}: {name} has {t.element_size()}-byte elements, expected {esize}")
-    if dtype is not None and t.dtype in (torch.float16, torch.bfloat16) and _dtype_of(t) != dtype:
-        raise ValueError(f"{where}: {name} is {t.dtype}, which is not the call's dtype")
     if nbytes > 0 and not (t.is_contiguous() and t.numel() * esize >= nbytes):
         # views: judge by the storage from the first element on (an expanded,
         # stride-0 tensor is judged by what it owns, not by its shape)

@@ -7,16 +7,26 @@ import torch
 from . import binding as B
 
 
+_IDS = {torch.float16: B.POLY_F16, torch.bfloat16: B.POLY_BF16}
+
+
 def _dt(t):
-    if t.dtype not in (torch.float16, torch.bfloat16):
+    dt = _IDS.get(t.dtype)
+    if dt is None:
         raise TypeError("FP16 or BF16 tensors only")
     if not t.is_cuda:
         raise ValueError("CUDA tensors only: the library has no CPU path")
-    return B.POLY_F16 if t.dtype == torch.float16 else B.POLY_BF16
+    return dt
+
+
+def _dense(t):
+    """t, or a contiguous copy of it (the check is cheaper than a no-op
+    .contiguous() call, which goes through the dispatcher)."""
+    return t if t.is_contiguous() else t.contiguous()
 
 
 def act_fwd(fn: str, x: torch.Tensor, out=None, control: bool = False) -> torch.Tensor:
-    x = x.contiguous()
+    x = _dense(x)
     y = torch.empty_like(x) if out is None else out
     (B.poly_ctrl_act_fwd if control else B.poly_act_fwd)(B.FN[fn], _dt(x), x, y)
     return y
@@ -24,7 +34,7 @@ def act_fwd(fn: str, x: torch.Tensor, out=None, control: bool = False) -> torch.
 
 def act_bwd(fn: str, x: torch.Tensor, dy: torch.Tensor, out=None,
             control: bool = False) -> torch.Tensor:
-    x, dy = x.contiguous(), dy.contiguous()
+    x, dy = _dense(x), _dense(dy)
     dx = torch.empty_like(x) if out is None else out
     (B.poly_ctrl_act_bwd if control else B.poly_act_bwd)(B.FN[fn], _dt(x), x, dy, dx)
     return dx
@@ -72,7 +82,7 @@ class PolyActivation(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, fn: str):
-        x = x.contiguous()
+        x = _dense(x)
         ctx.save_for_backward(x)
         ctx.fn = fn
         return act_fwd(fn, x)
@@ -80,23 +90,33 @@ class PolyActivation(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         (x,) = ctx.saved_tensors
-        return act_bwd(ctx.fn, x, dy.contiguous()), None
+        return act_bwd(ctx.fn, x, _dense(dy)), None
+
+
+def _grad(*ts):
+    """True when autograd has to record the call; otherwise the wrappers below
+    call the kernels directly (the autograd node costs ~10 us of host time)."""
+    return torch.is_grad_enabled() and any(t.requires_grad for t in ts)
+
+
+def _act(x, fn):
+    return PolyActivation.apply(x, fn) if _grad(x) else act_fwd(fn, x)
 
 
 def sigmoid(x):
-    return PolyActivation.apply(x, "sigmoid")
+    return _act(x, "sigmoid")
 
 
 def tanh(x):
-    return PolyActivation.apply(x, "tanh")
+    return _act(x, "tanh")
 
 
 def silu(x):
-    return PolyActivation.apply(x, "silu")
+    return _act(x, "silu")
 
 
 def gelu(x):
-    return PolyActivation.apply(x, "gelu")
+    return _act(x, "gelu")
 
 
 class PolySwiGLU(torch.autograd.Function):
@@ -115,7 +135,7 @@ class PolySwiGLU(torch.autograd.Function):
 
 
 def swiglu(g, u):
-    return PolySwiGLU.apply(g, u)
+    return PolySwiGLU.apply(g, u) if _grad(g, u) else swiglu_fwd(_rows(g), _rows(u))
 
 
 class PolySwiGLURagged(torch.autograd.Function):
@@ -125,20 +145,26 @@ class PolySwiGLURagged(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, g, u, seg_off):
-        g, u = g.contiguous(), u.contiguous()
+        g, u = _dense(g), _dense(u)
         ctx.save_for_backward(g, u, seg_off)
-        return swiglu_fwd_ragged(g, u, seg_off, out=torch.zeros_like(g))
+        return _ragged_fwd(g, u, seg_off)
 
     @staticmethod
     def backward(ctx, dy):
         g, u, seg_off = ctx.saved_tensors
-        dg, du = swiglu_bwd_ragged(g, u, dy.contiguous(), seg_off, dg=torch.zeros_like(g),
+        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off, dg=torch.zeros_like(g),
                                    du=torch.zeros_like(g))
         return dg, du, None
 
 
+def _ragged_fwd(g, u, seg_off):
+    return swiglu_fwd_ragged(g, u, seg_off, out=torch.zeros_like(g))
+
+
 def swiglu_ragged(g, u, seg_off):
-    return PolySwiGLURagged.apply(g, u, seg_off)
+    if _grad(g, u):
+        return PolySwiGLURagged.apply(g, u, seg_off)
+    return _ragged_fwd(_dense(g), _dense(u), seg_off)
 
 
 class PolySoftcap(torch.autograd.Function):
@@ -146,23 +172,27 @@ class PolySoftcap(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, alpha: float):
-        x = x.contiguous()
+        x = _dense(x)
         ctx.save_for_backward(x)
         ctx.alpha = alpha
-        y = torch.empty_like(x)
-        B.poly_softcap_fwd(_dt(x), alpha, x, y)
-        return y
+        return _softcap_fwd(x, alpha)
 
     @staticmethod
     def backward(ctx, dy):
         (x,) = ctx.saved_tensors
         dx = torch.empty_like(x)
-        B.poly_softcap_bwd(_dt(x), ctx.alpha, x, dy.contiguous(), dx)
+        B.poly_softcap_bwd(_dt(x), ctx.alpha, x, _dense(dy), dx)
         return dx, None
 
 
+def _softcap_fwd(x, alpha):
+    y = torch.empty_like(x)
+    B.poly_softcap_fwd(_dt(x), alpha, x, y)
+    return y
+
+
 def softcap(x, alpha: float):
-    return PolySoftcap.apply(x, alpha)
+    return PolySoftcap.apply(x, alpha) if _grad(x) else _softcap_fwd(_dense(x), alpha)
 
 
 class PolyRoPE(torch.autograd.Function):
@@ -171,14 +201,9 @@ class PolyRoPE(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, delta, pos_offset: int):
-        q, k = q.contiguous(), k.contiguous()
-        b, s, hq, d = q.shape
-        hkv = k.shape[2]
-        qo = torch.empty((b, hq, s, d), dtype=q.dtype, device=q.device)
-        ko = torch.empty((b, hkv, s, d), dtype=k.dtype, device=k.device)
-        B.poly_rope_fwd(B.POLY_ROPE_POLY, q, k, qo, ko, delta, pos_offset=pos_offset)
+        qo, ko = _rope_fwd(q, k, delta, pos_offset)
         ctx.save_for_backward(delta)
-        ctx.meta = (b, s, hq, hkv, d, pos_offset)
+        ctx.meta = (q.shape[0], q.shape[1], q.shape[2], k.shape[2], q.shape[3], pos_offset)
         return qo, ko
 
     @staticmethod
@@ -186,16 +211,28 @@ class PolyRoPE(torch.autograd.Function):
         (delta,) = ctx.saved_tensors
         b, s, hq, hkv, d, pos = ctx.meta
         dqo = torch.zeros((b, hq, s, d), dtype=torch.float16, device=delta.device) \
-            if dqo is None else dqo.contiguous()
+            if dqo is None else _dense(dqo)
         dko = torch.zeros((b, hkv, s, d), dtype=torch.float16, device=delta.device) \
-            if dko is None else dko.contiguous()
+            if dko is None else _dense(dko)
         dq = torch.empty((b, s, hq, d), dtype=dqo.dtype, device=dqo.device)
         dk = torch.empty((b, s, hkv, d), dtype=dko.dtype, device=dko.device)
         B.poly_rope_bwd(B.POLY_ROPE_POLY, dqo, dko, dq, dk, delta, pos_offset=pos)
         return dq, dk, None, None
 
 
+def _rope_fwd(q, k, delta, pos_offset):
+    q, k = _dense(q), _dense(k)
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    qo = torch.empty((b, hq, s, d), dtype=q.dtype, device=q.device)
+    ko = torch.empty((b, hkv, s, d), dtype=k.dtype, device=k.device)
+    B.poly_rope_fwd(B.POLY_ROPE_POLY, q, k, qo, ko, delta, pos_offset=pos_offset)
+    return qo, ko
+
+
 def rope(q, k, delta, pos_offset: int = 0):
     """delta: device uint32/int32 tensor of D/2 turn increments
     (``binding.poly_rope_turn_increments``)."""
-    return PolyRoPE.apply(q, k, delta, pos_offset)
+    if _grad(q, k):
+        return PolyRoPE.apply(q, k, delta, pos_offset)
+    return _rope_fwd(q, k, delta, pos_offset)

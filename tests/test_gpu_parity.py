@@ -1145,6 +1145,69 @@ def test_autograd_wrappers_match_direct_calls():
     assert np.array_equal(from_dev(k.grad).reshape(gk.shape), gk)
 
 
+def test_wrappers_without_autograd_match_recorded_calls():
+    """With no gradient to record (inputs without requires_grad, or under
+    torch.no_grad / inference_mode) the wrappers call the kernels directly:
+    same bits as the recorded path, no autograd node, ragged rows outside the
+    range still zero."""
+    from polynomial_activation_gb300 import ops
+    from oracle import rope
+    rng = np.random.default_rng(78)
+    for dt in DTS:
+        x = to_dev(_rand_bits(rng, 10_001, FMT[dt]), dt)
+        g = to_dev(_rand_bits(rng, 64 * 256, FMT[dt]), dt).view(64, 256)
+        u = to_dev(_rand_bits(rng, 64 * 256, FMT[dt]), dt).view(64, 256)
+        seg = torch.tensor([0, 10, 10, 40], dtype=torch.int32, device=DEV)
+        calls = [lambda a: ops.sigmoid(a), lambda a: ops.tanh(a), lambda a: ops.silu(a),
+                 lambda a: ops.gelu(a), lambda a: ops.softcap(a, 30.0)]
+        for f in calls:
+            want = f(x.clone().requires_grad_(True))
+            assert want.grad_fn is not None
+            for mode in ("plain", "no_grad", "inference"):
+                if mode == "plain":
+                    got = f(x)
+                elif mode == "no_grad":
+                    with torch.no_grad():
+                        got = f(x.clone().requires_grad_(True))
+                else:
+                    with torch.inference_mode():
+                        got = f(x)
+                assert got.grad_fn is None and not got.requires_grad
+                assert torch.equal(got.view(torch.int16), want.detach().view(torch.int16)), mode
+        want = ops.swiglu(g.clone().requires_grad_(True), u)
+        got = ops.swiglu(g, u)
+        assert got.grad_fn is None
+        assert torch.equal(got.view(torch.int16), want.detach().view(torch.int16))
+        with torch.no_grad():
+            got3 = ops.swiglu(g.reshape(4, 16, 256), u.reshape(4, 16, 256))
+        assert got3.shape == (4, 16, 256)
+        assert torch.equal(got3.reshape(64, 256).view(torch.int16), got.view(torch.int16))
+        want = ops.swiglu_ragged(g.clone().requires_grad_(True), u, seg)
+        got = ops.swiglu_ragged(g, u, seg)
+        assert got.grad_fn is None
+        assert torch.equal(got.view(torch.int16), want.detach().view(torch.int16))
+        assert not bool(got[40:].view(torch.int16).any())
+    q = torch.randn(2, 16, 4, 64, device=DEV).half()
+    k = torch.randn(2, 16, 2, 64, device=DEV).half()
+    delta = torch.from_numpy(rope.turn_increments(64).view(np.int32)).to(DEV)
+    wq, wk = ops.rope(q.clone().requires_grad_(True), k, delta, 7)
+    gq, gk = ops.rope(q, k, delta, 7)
+    assert gq.grad_fn is None and gk.grad_fn is None
+    assert torch.equal(gq.view(torch.int16), wq.detach().view(torch.int16))
+    assert torch.equal(gk.view(torch.int16), wk.detach().view(torch.int16))
+
+
+def test_calls_use_the_current_stream():
+    """With no stream argument the binding launches on the current stream of
+    the current device, inside and outside a torch.cuda.stream context."""
+    side = torch.cuda.Stream()
+    assert B._stream(None) == torch.cuda.current_stream().cuda_stream
+    with torch.cuda.stream(side):
+        assert B._stream(None) == side.cuda_stream
+        assert B._stream(None) == torch.cuda.current_stream().cuda_stream
+    assert B._stream(None) == torch.cuda.current_stream().cuda_stream
+
+
 def test_every_degree_every_program_exhaustive():
     """Programs of every degree D3-D6 (fitted by the library, installed with
     poly_set_program) for every function, direction and format, over all

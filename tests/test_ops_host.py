@@ -1,0 +1,34 @@
+"""The tensor wrappers refuse what the kernels cannot take, on any machine:
+host tensors (the library has no CPU path) and types other than FP16 / BF16."""
+import pytest
+import torch
+
+from polynomial_activation_gb300 import ops
+
+
+@pytest.mark.parametrize("f", [ops.sigmoid, ops.tanh, ops.silu, ops.gelu,
+                               lambda t: ops.softcap(t, 30.0)])
+def test_host_tensor_is_refused(f):
+    x = torch.zeros(64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="no CPU path"):
+        f(x)
+    with pytest.raises(ValueError, match="no CPU path"):
+        f(x.clone().requires_grad_(True))          # the recorded path refuses it too
+
+
+def test_other_types_are_refused():
+    with pytest.raises(TypeError):
+        ops.silu(torch.zeros(64, dtype=torch.float32))
+    with pytest.raises(TypeError):
+        ops.swiglu(torch.zeros(4, 8, dtype=torch.float32), torch.zeros(4, 8, dtype=torch.float32))
+
+
+def test_grad_decision():
+    x = torch.zeros(4, dtype=torch.float16)
+    assert not ops._grad(x)
+    xr = x.clone().requires_grad_(True)
+    assert ops._grad(xr) and ops._grad(x, xr)
+    with torch.no_grad():
+        assert not ops._grad(xr)
+    with torch.inference_mode():
+        assert not ops._grad(xr)
