@@ -357,6 +357,8 @@ def main():
               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
               "dtype": "f16", "data": "synthetic",
               "config": {"workload": WORKLOAD, "elements": n, "programs": [f"{a}.{'bwd' if d else 'fwd'}.D{D}" for a, d, D in SIX],
+                         "inputs": "x ~ N(0, 3^2) with 1 % uniform in [-40, 40] (PCG64 seed 0), "
+                                   "dy ~ N(0, 1) (seed 1), generated on the host, resident in HBM",
                          "l2": "inputs (512 MiB per tensor) larger than L2; no flush",
                          "parallelism": f"replicas x{world}, no collective"},
               "gpu_launches": len(SIX) * args.steps,
