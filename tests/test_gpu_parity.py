@@ -1085,6 +1085,50 @@ def test_concurrent_streams():
     assert np.array_equal(from_dev(yb), forward(oracle_program(B.POLY_SILU, B.POLY_FWD, dt), xb))
 
 
+def test_host_threads_launch_concurrently():
+    """Four host threads, each on its own stream with its own program, launch
+    at the same time (the C calls overlap: ctypes releases the GIL); every
+    output is the oracle's."""
+    import threading
+    dt, fmt = B.POLY_F16, "f16"
+    n = 1_000_003
+    rng = np.random.default_rng(63)
+    jobs = []
+    for fn, d in ((B.POLY_SIGMOID, 0), (B.POLY_TANH, 0), (B.POLY_GELU, 0), (B.POLY_SILU, 1)):
+        x, dy = _rand_bits(rng, n, fmt), _rand_bits(rng, n, fmt)
+        B.poly_get_program(fn, d, dt)
+        jobs.append((fn, d, x, dy, to_dev(x, dt), to_dev(dy, dt)))
+    outs = [torch.empty_like(j[4]) for j in jobs]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(i):
+        try:
+            fn, d, _, _, xd, dyd = jobs[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(50):
+                    if d == 0:
+                        B.poly_act_fwd(fn, dt, xd, outs[i])
+                    else:
+                        B.poly_act_bwd(fn, dt, xd, dyd, outs[i])
+            st.synchronize()
+        except BaseException as e:
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for (fn, d, x, dy, _, _), o in zip(jobs, outs):
+        op = oracle_program(fn, d, dt)
+        want = forward(op, x) if d == 0 else backward(op, x, dy)
+        assert np.array_equal(from_dev(o), want), (fn, d)
+
+
 # ------------------------------------------------------------------ autograd
 
 def test_autograd_wrappers_match_direct_calls():
