@@ -408,6 +408,7 @@ def main():
 
     # ---- extras: SwiGLU and the L2-resident sweep
     if not args.no_extras:
+        result["programs_bf16"] = bf16_extras(x, dy, n, stream, peak)
         result["softcap"] = softcap_extras(x, dy, outs[0], n, stream, peak)
         result["exp2"] = exp2_extras(dev, stream, peak)
         result["rope"] = rope_extras(dev, stream, peak)
@@ -477,6 +478,34 @@ def softcap_extras(x, dy, y, n, stream, peak, alpha=30.0):
     return res
 
 
+def bf16_extras(x, dy, n, stream, peak, reps=30):
+    """The six programs and their MUFU controls on BF16 copies of the step's
+    tensors (same shapes and distribution; converted on the device)."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    bf = B.POLY_BF16
+    xb, dyb = x.to(torch.bfloat16), dy.to(torch.bfloat16)
+    y = torch.empty_like(xb)
+    res = {}
+    for name, d, D in SIX:
+        prog = B.poly_get_program(FN[name], d, bf)
+        if d == 0:
+            fp = lambda: B.poly_act_fwd(FN[name], bf, xb, y, n)
+            fc = lambda: B.poly_ctrl_act_fwd(FN[name], bf, xb, y, n)
+        else:
+            fp = lambda: B.poly_act_bwd(FN[name], bf, xb, dyb, y, n)
+            fc = lambda: B.poly_ctrl_act_bwd(FN[name], bf, xb, dyb, y, n)
+        tp, tc = _time(fp, stream, reps), _time(fc, stream, reps)
+        gb = BYTES[d] * n / 1e9
+        res[f"{name}.{'bwd' if d else 'fwd'}.D{prog.degree}"] = {
+            "poly_ms": tp, "poly_gbs": gb / tp * 1e3, "poly_frac": gb / tp * 1e3 / peak,
+            "ctrl_ms": tc, "speedup_vs_ctrl": tc / tp}
+    res["config"] = ("268,435,456 BF16 elements: the step's FP16 x and dy converted on the device; "
+                     f"mean of {reps} launches each")
+    return res
+
+
+_COPY_MS = {}
 _COPY_MS = {}
 
 

@@ -310,12 +310,14 @@ def test_index_width_limits(n):
     del x, y
 
 
-def test_hbm_resident_sweep_full_size():
-    """268,435,456 FP16 elements (512 MiB per tensor), 1 % outliers in
-    [-40, 40].  Forward: every element equals the oracle's exhaustive table
-    at its input.  Backward: 2^21 sampled elements plus both ends."""
-    dt = B.POLY_F16
-    x, dy = workloads.isolated_hbm("f16")
+@pytest.mark.parametrize("dt", DTS)
+def test_hbm_resident_sweep_full_size(dt):
+    """268,435,456 elements (512 MiB per tensor), 1 % outliers in [-40, 40],
+    FP16 (the bench's step) and BF16.  Forward: every element equals the
+    oracle's exhaustive table at its input.  Backward: 2^21 sampled elements
+    plus both ends through the oracle, and every element as dy times the
+    tabulated program, one rounding."""
+    x, dy = workloads.isolated_hbm(FMT[dt])
     n = x.size
     xd, dyd = to_dev(x, dt), to_dev(dy, dt)
     out = torch.empty_like(xd)
