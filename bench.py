@@ -413,6 +413,7 @@ def main():
         result["exp2"] = exp2_extras(dev, stream, peak)
         result["rope"] = rope_extras(dev, stream, peak)
         result["swiglu"] = swiglu_extras(args, dev, stream, peak)
+        result["components"] = component_extras(dev, stream, peak)
         result["l2_resident"] = l2_extras(dev, stream)
         result["host_us_per_call"] = host_cost_extras(dev)
 
@@ -505,6 +506,82 @@ def bf16_extras(x, dy, n, stream, peak, reps=30):
     return res
 
 
+def component_extras(dev, stream, peak, rounds=5, reps=100):
+    """The paper's two component workloads (its B1 unary SiLU probe, 58,720,256
+    BF16 values, and its B4 one-kernel expert SwiGLU activation, 24,576 rows x
+    1,280), with its component protocol: 25 warm-up calls, then `rounds`
+    alternating rounds of `reps` back-to-back calls per implementation, the
+    median of the per-round means.  Polynomial kernel vs the MUFU control vs
+    PyTorch eager (forward F.silu / F.silu(g) * u; backward aten.silu_backward
+    / the two-output autograd formula)."""
+    import torch
+    from polynomial_activation_gb300 import binding as B
+    F = torch.nn.functional
+    bf = B.POLY_BF16
+    gen = torch.Generator(device=dev).manual_seed(5)
+    res = {}
+
+    def run(impls, nbytes):
+        for f in impls.values():
+            for _ in range(25):
+                f()
+        per = {k: [] for k in impls}
+        order = list(impls)
+        for r in range(rounds):
+            for k in (order if r % 2 == 0 else order[::-1]):
+                per[k].append(_time(impls[k], stream, reps, warm=0))
+        out = {}
+        for k, v in per.items():
+            ms = statistics.median(v)
+            out[f"{k}_us"] = ms * 1e3
+            out[f"{k}_gbs"] = nbytes / ms / 1e6
+        out["poly_frac"] = out["poly_gbs"] / peak
+        out["speedup_vs_ctrl"] = out["ctrl_us"] / out["poly_us"]
+        out["speedup_vs_torch"] = out["torch_us"] / out["poly_us"]
+        return out
+
+    n = 58_720_256
+    x = (torch.randn(n, device=dev, generator=gen) * 3).bfloat16()
+    dy = torch.randn(n, device=dev, generator=gen).bfloat16()
+    y = torch.empty_like(x)
+    silu = FN["silu"]
+    res["silu_probe_fwd"] = run({
+        "poly": lambda: B.poly_act_fwd(silu, bf, x, y, n),
+        "ctrl": lambda: B.poly_ctrl_act_fwd(silu, bf, x, y, n),
+        "torch": lambda: F.silu(x)}, 4 * n)
+    res["silu_probe_bwd"] = run({
+        "poly": lambda: B.poly_act_bwd(silu, bf, x, dy, y, n),
+        "ctrl": lambda: B.poly_ctrl_act_bwd(silu, bf, x, dy, y, n),
+        "torch": lambda: torch.ops.aten.silu_backward(dy, x)}, 6 * n)
+    del x, dy, y
+    rows, cols = 24_576, 1_280
+    g = (torch.randn(rows, cols, device=dev, generator=gen) * 1.5).bfloat16()
+    u = (torch.randn(rows, cols, device=dev, generator=gen) * 1.5).bfloat16()
+    dy = torch.randn(rows, cols, device=dev, generator=gen).bfloat16()
+    y, dg, du = torch.empty_like(g), torch.empty_like(g), torch.empty_like(g)
+    m = rows * cols
+
+    def torch_swiglu_bwd():
+        du_ = dy * F.silu(g)
+        dg_ = torch.ops.aten.silu_backward(dy * u, g)
+        return dg_, du_
+
+    res["expert_swiglu_fwd"] = run({
+        "poly": lambda: B.poly_swiglu_fwd(bf, g, u, y),
+        "ctrl": lambda: B.poly_ctrl_swiglu_fwd(bf, g, u, y),
+        "torch": lambda: F.silu(g) * u}, 6 * m)
+    res["expert_swiglu_bwd"] = run({
+        "poly": lambda: B.poly_swiglu_bwd(bf, g, u, dy, dg, du),
+        "ctrl": lambda: B.poly_ctrl_swiglu_bwd(bf, g, u, dy, dg, du),
+        "torch": torch_swiglu_bwd}, 10 * m)
+    res["config"] = ("BF16; SiLU probe 58,720,256 values, x ~ N(0, 3^2), dy ~ N(0, 1); expert "
+                     "SwiGLU 24,576 x 1,280, g, u ~ N(0, 1.5^2), dy ~ N(0, 1); inputs drawn on the "
+                     f"device (seed 5); {rounds} alternating rounds of {reps} calls, median; "
+                     "no L2 flush (the paper's component protocol); GB/s = algorithmic bytes")
+    return res
+
+
+_COPY_MS = {}
 _COPY_MS = {}
 _COPY_MS = {}
 
