@@ -424,6 +424,49 @@ def test_dense_swiglu_full_size_sampled():
     assert _equal_bits(du, _rn_mul(dyd, sg))
 
 
+def test_component_workloads_every_element():
+    """The bench's component shapes, in the launch configuration it times:
+    the SiLU probe (58,720,256 BF16 values) forward and backward, and the
+    expert SwiGLU activation (24,576 x 1,280 BF16) forward and backward,
+    every element through the oracle's exhaustive tables, plus a sample
+    through the oracle's replay."""
+    dt, fmt = B.POLY_BF16, "bf16"
+    s_op, d_op = _swiglu_ops(dt)
+    rng = np.random.default_rng(51)
+    n = 58_720_256
+    x = workloads.normal(n, 51, 3.0, fmt)
+    dy = workloads.normal(n, 52, 1.0, fmt)
+    xd, dyd = to_dev(x, dt), to_dev(dy, dt)
+    out = torch.empty_like(xd)
+    B.poly_act_fwd(B.POLY_SILU, dt, xd, out, n)
+    assert _equal_bits(out, _apply_lut(s_op, xd))
+    B.poly_act_bwd(B.POLY_SILU, dt, xd, dyd, out, n)
+    assert _equal_bits(out, _rn_mul(dyd, _apply_lut(d_op, xd)))
+    smp = np.unique(np.concatenate([rng.integers(0, n, 1 << 18), np.arange(n - 64, n)]))
+    assert np.array_equal(from_dev(out[torch.from_numpy(smp).to(DEV)]),
+                          backward(d_op, x[smp], dy[smp]))
+    del x, dy, xd, dyd, out
+    rows, cols = 24_576, 1_280
+    m = rows * cols
+    g = workloads.normal(m, 53, 1.5, fmt)
+    u = workloads.normal(m, 54, 1.5, fmt)
+    dy = workloads.normal(m, 55, 1.0, fmt)
+    gd, ud, dyd = (to_dev(a, dt).view(rows, cols) for a in (g, u, dy))
+    y, dg, du = torch.empty_like(gd), torch.empty_like(gd), torch.empty_like(gd)
+    B.poly_swiglu_fwd(dt, gd, ud, y)
+    B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+    sg, sdg = _apply_lut(s_op, gd), _apply_lut(d_op, gd)
+    assert _equal_bits(y, _rn_mul(sg, ud))
+    assert _equal_bits(dg, _rn_mul(_rn_mul(dyd, ud), sdg))
+    assert _equal_bits(du, _rn_mul(dyd, sg))
+    smp = np.unique(np.concatenate([rng.integers(0, m, 1 << 18), np.arange(m - cols, m)]))
+    sd = torch.from_numpy(smp).to(DEV)
+    assert np.array_equal(from_dev(y.view(-1)[sd]), swiglu_forward(s_op, g[smp], u[smp]))
+    wdg, wdu = swiglu_backward(s_op, d_op, g[smp], u[smp], dy[smp])
+    assert np.array_equal(from_dev(dg.view(-1)[sd]), wdg)
+    assert np.array_equal(from_dev(du.view(-1)[sd]), wdu)
+
+
 def test_ragged_swiglu_full_size_sampled():
     """16,384 tokens x top-8 over 64 experts: Zipf(1.1) segments summing to
     131,072 rows of 2048; the offsets stay on the device.  Rows past the last
