@@ -139,6 +139,116 @@ def test_small_sizes_offsets_and_guards(dt):
             assert guards_intact(buf, n, G, off_y), (n, off_x, off_y)
 
 
+def _at(bits, off, dt):
+    """bits on the device, starting `off` elements past an aligned address."""
+    return to_dev(np.concatenate([np.zeros(off, np.uint16), bits]), dt)[off:]
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_guard_bands_other_kernel_families(dt):
+    """Softcap, the MUFU controls and dense SwiGLU (polynomial and control)
+    write into sentinel-filled buffers at every 16-byte misalignment, small
+    and odd sizes: each result is checked (the oracle; for the controls, the
+    same call on aligned buffers) and nothing outside the output changes."""
+    from oracle.replay import softcap_backward, softcap_forward
+    fmt = FMT[dt]
+    rng = np.random.default_rng(97)
+    G = 64
+    tp = oracle_program(B.POLY_TANH, B.POLY_FWD, dt)
+    tdp = oracle_program(B.POLY_TANH, B.POLY_BWD, dt)
+    s_op, d_op = _swiglu_ops(dt)
+    for n in (1, 2, 7, 8, 9, 15, 17, 33, 67, 1031):
+        for off in range(8):
+            oo = (off + 3 * (n % 2)) % 8                   # output misaligned differently at odd n
+            x, dy = _rand_bits(rng, n, fmt), _rand_bits(rng, n, fmt)
+            xd, dyd = _at(x, off, dt), _at(dy, off, dt)
+            xa, dya = to_dev(x, dt), to_dev(dy, dt)
+            buf, y = sentinel_buffer(n, G, dt, oo)
+            B.poly_softcap_fwd(dt, 30.0, xd, y, n)
+            assert np.array_equal(from_dev(y), softcap_forward(tp, 30.0, x)), (n, off)
+            assert guards_intact(buf, n, G, oo)
+            buf, y = sentinel_buffer(n, G, dt, oo)
+            B.poly_softcap_bwd(dt, 30.0, xd, dyd, y, n)
+            assert np.array_equal(from_dev(y), softcap_backward(tdp, 30.0, x, dy)), (n, off)
+            assert guards_intact(buf, n, G, oo)
+            for fn, d in ((B.POLY_SIGMOID, 0), (B.POLY_GELU, 0), (B.POLY_TANH, 1), (B.POLY_SILU, 1)):
+                ref = torch.empty_like(xa)
+                buf, y = sentinel_buffer(n, G, dt, oo)
+                if d == 0:
+                    B.poly_ctrl_act_fwd(fn, dt, xa, ref, n)
+                    B.poly_ctrl_act_fwd(fn, dt, xd, y, n)
+                else:
+                    B.poly_ctrl_act_bwd(fn, dt, xa, dya, ref, n)
+                    B.poly_ctrl_act_bwd(fn, dt, xd, dyd, y, n)
+                assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (fn, d, n, off)
+                assert guards_intact(buf, n, G, oo)
+    for rows, cols in ((1, 1), (3, 13), (2, 8), (5, 17), (4, 64)):
+        m = rows * cols
+        for off in range(8):
+            oo = (off + 5) % 8
+            g, u, dy = (_rand_bits(rng, m, fmt) for _ in range(3))
+            gd, ud, dyd = (_at(a, off, dt).view(rows, cols) for a in (g, u, dy))
+            gr, ur, dyr = g.reshape(rows, cols), u.reshape(rows, cols), dy.reshape(rows, cols)
+            for ctrl in (False, True):
+                bufs = [sentinel_buffer(m, G, dt, oo) for _ in range(3)]
+                y, dg, du = (b[1].view(rows, cols) for b in bufs)
+                if ctrl:
+                    B.poly_ctrl_swiglu_fwd(dt, gd, ud, y)
+                    B.poly_ctrl_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+                    ga, ua, dya = (to_dev(a, dt).view(rows, cols) for a in (g, u, dy))
+                    ry, rdg, rdu = torch.empty_like(ga), torch.empty_like(ga), torch.empty_like(ga)
+                    B.poly_ctrl_swiglu_fwd(dt, ga, ua, ry)
+                    B.poly_ctrl_swiglu_bwd(dt, ga, ua, dya, rdg, rdu)
+                    want = (from_dev(ry), from_dev(rdg), from_dev(rdu))
+                else:
+                    B.poly_swiglu_fwd(dt, gd, ud, y)
+                    B.poly_swiglu_bwd(dt, gd, ud, dyd, dg, du)
+                    want = (swiglu_forward(s_op, gr, ur),) + tuple(swiglu_backward(s_op, d_op, gr, ur, dyr))
+                for (b, _), got, w in zip(bufs, (y, dg, du), want):
+                    assert np.array_equal(from_dev(got).reshape(rows, cols), np.reshape(w, (rows, cols))), \
+                        (rows, cols, off, ctrl)
+                    assert guards_intact(b, m, G, oo)
+
+
+def test_guard_bands_exp2_and_rope():
+    """exp2 (FP32, every 4-byte offset within 16 bytes) and fused RoPE
+    (outputs inside sentinel buffers) write exactly their outputs."""
+    from oracle import exp2 as e2, rope
+    rng = np.random.default_rng(98)
+    G = 32
+    for n in (1, 3, 4, 5, 31, 67, 1029):
+        for off in range(4):
+            oo = (off + 1) % 4
+            x = rng.uniform(-60, 10, n).astype(np.float32)
+            xd = torch.from_numpy(np.concatenate([np.zeros(off, np.float32), x])).to(DEV)[off:]
+            buf = torch.full((2 * G + oo + n,), 0x5A5A5A5A, dtype=torch.int32, device=DEV)
+            y = buf[G + oo: G + oo + n].view(torch.float32)
+            B.poly_exp2(B.POLY_EXP2_D2, xd, y, n)
+            assert np.array_equal(y.cpu().numpy().view(np.uint32), e2.exp2_replay("D2", x)), (n, off)
+            assert bool((buf[:G + oo] == 0x5A5A5A5A).all() and (buf[G + oo + n:] == 0x5A5A5A5A).all())
+    for b, s, hq, hkv, d in ((1, 5, 3, 1, 8), (2, 9, 2, 3, 16), (1, 1, 1, 0, 64)):
+        q, k = _rope_case(rng, b, s, hq, hkv, d)
+        delta = rope.turn_increments(d)
+        dd = torch.from_numpy(delta.view(np.int32)).to(DEV)
+        qd, kd = to_dev(q, 0), to_dev(k, 0)
+        nq, nk = b * hq * s * d, b * hkv * s * d
+        Gh = 8 * 16                                           # a 16-byte multiple of FP16 elements
+        bq = torch.full((2 * Gh + nq,), 0x5A5A, dtype=torch.int16, device=DEV)
+        bk = torch.full((2 * Gh + nk,), 0x5A5A, dtype=torch.int16, device=DEV)
+        qo = bq[Gh:Gh + nq].view(torch.float16).view(b, hq, s, d)
+        ko = bk[Gh:Gh + nk].view(torch.float16).view(b, hkv, s, d)
+        B.poly_rope_fwd(B.POLY_ROPE_POLY, qd, kd if hkv else None, qo, ko if hkv else None, dd,
+                        batch=b, seq=s, hq=hq, hkv=hkv, head_dim=d, pos_offset=11)
+        wq, wk = rope.rope_forward(q, k, delta, 11)
+        assert np.array_equal(from_dev(qo).reshape(wq.shape), wq)
+        if hkv:
+            assert np.array_equal(from_dev(ko).reshape(wk.shape), wk)
+        for t, m in ((bq, nq), (bk, nk)):
+            assert bool((t[:Gh] == 0x5A5A).all() and (t[Gh + m:] == 0x5A5A).all())
+        if not hkv:
+            assert bool((bk == 0x5A5A).all())
+
+
 def test_binding_checks_tensor_extents_before_launch():
     """A tensor too short for the call, a dtype that disagrees with the
     call's, or pageable host memory is refused by the binding before the
