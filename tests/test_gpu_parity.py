@@ -420,6 +420,71 @@ def test_index_width_limits(n):
     del x, y
 
 
+def test_swiglu_above_2_31_elements():
+    """SwiGLU forward and backward, dense and ragged, over 2^31 + 2,048
+    elements (1,048,577 rows of 2,048): the general kernel's 64-bit path for
+    two- and three-input operations.  The gate cycles through all 65,536 BF16
+    patterns (the up and dy streams through shifted copies), so every element
+    is checked against the oracle's exhaustive tables, in slices of 2^28;
+    ragged rows past the last offset stay untouched."""
+    dt = B.POLY_BF16
+    s_op, d_op = _swiglu_ops(dt)
+    ls, ld = _lut(s_op), _lut(d_op)
+    rows, cols = 1_048_577, 2048
+    n = rows * cols
+    assert n > 1 << 31
+    cap = rows + 7
+    pat = torch.from_numpy(X_ALL.view(np.int16)).to(DEV)
+
+    def cyclic(shift):
+        t = torch.empty(cap * cols, dtype=torch.int16, device=DEV)
+        p = torch.roll(pat, shift)
+        full = t.numel() // 65536
+        t[:full * 65536].view(full, 65536).copy_(p.expand(full, 65536))
+        t[full * 65536:] = p[:t.numel() - full * 65536]
+        return t.view(torch.bfloat16)
+
+    g, u, dy = cyclic(0), cyclic(12_345), cyclic(40_000)
+
+    def check(y, dg, du):
+        step = 1 << 28
+        for lo in range(0, n, step):
+            hi = min(n, lo + step)
+            gi = (g[lo:hi].view(torch.int16).to(torch.int32) & 0xFFFF).long()
+            sg, sdg = ls[gi].view(torch.bfloat16), ld[gi].view(torch.bfloat16)
+            us, dys = u[lo:hi], dy[lo:hi]
+            if y is not None:
+                assert _equal_bits(y[lo:hi], _rn_mul(sg, us)), lo
+            if dg is not None:
+                assert _equal_bits(dg[lo:hi], _rn_mul(_rn_mul(dys, us), sdg)), lo
+                assert _equal_bits(du[lo:hi], _rn_mul(dys, sg)), lo
+            del gi, sg, sdg
+
+    gv, uv, dyv = (t[:n].view(rows, cols) for t in (g, u, dy))
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=DEV)
+    B.poly_swiglu_fwd(dt, gv, uv, y)
+    check(y.view(-1), None, None)
+    dg, du = torch.empty_like(y), torch.empty_like(y)
+    B.poly_swiglu_bwd(dt, gv, uv, dyv, dg, du)
+    check(None, dg.view(-1), du.view(-1))
+    del y, dg, du
+    seg = torch.tensor([0, 500_000, 500_000, rows], dtype=torch.int32, device=DEV)
+    gc, uc, dyc = (t.view(cap, cols) for t in (g, u, dy))
+    fill = lambda: torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    y = fill()
+    B.poly_swiglu_fwd_ragged(dt, gc, uc, y, seg)
+    check(y.view(-1), None, None)
+    assert bool((y[rows:].view(torch.int16) == 0x5A5A).all())
+    del y
+    dg, du = fill(), fill()
+    B.poly_swiglu_bwd_ragged(dt, gc, uc, dyc, dg, du, seg)
+    check(None, dg.view(-1), du.view(-1))
+    assert bool((dg[rows:].view(torch.int16) == 0x5A5A).all())
+    assert bool((du[rows:].view(torch.int16) == 0x5A5A).all())
+    del dg, du, g, u, dy
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("dt", DTS)
 def test_hbm_resident_sweep_full_size(dt):
     """268,435,456 elements (512 MiB per tensor), 1 % outliers in [-40, 40],
