@@ -1107,6 +1107,31 @@ def test_exp2_full_size_sampled(core):
     assert bad.size == 0, [(float(x[idx[i]]), hex(got[i]), hex(want[i])) for i in bad[:6]]
 
 
+def test_exp2_above_2_31_elements():
+    """2^31 + 4,099 FP32 elements cycling through 65,536 values of
+    U[-60, 10]: every element equals the oracle's value for its input
+    (checked in slices of 2^28), tail included."""
+    from oracle import exp2 as e2
+    n = (1 << 31) + 4099
+    pat = np.random.default_rng(17).uniform(-60, 10, 65536).astype(np.float32)
+    want = torch.from_numpy(e2.exp2_replay("D2", pat).view(np.int32)).to(DEV)
+    pd = torch.from_numpy(pat).to(DEV)
+    x = torch.empty(n, dtype=torch.float32, device=DEV)
+    full = n // 65536
+    x[:full * 65536].view(full, 65536).copy_(pd.expand(full, 65536))
+    x[full * 65536:] = pd[:n - full * 65536]
+    y = torch.empty_like(x)
+    B.poly_exp2(B.POLY_EXP2_D2, x, y)
+    yi = y.view(torch.int32)
+    rows = 1 << 12
+    for r0 in range(0, full, rows):
+        r1 = min(full, r0 + rows)
+        assert bool((yi[r0 * 65536:r1 * 65536].view(r1 - r0, 65536) == want[None, :]).all()), r0
+    assert torch.equal(yi[full * 65536:], want[:n - full * 65536])
+    del x, y, yi
+    torch.cuda.empty_cache()
+
+
 def test_exp2_mufu_control_accuracy():
     x = np.random.default_rng(43).uniform(-120, 120, 1 << 20).astype(np.float32)
     xd = torch.from_numpy(x).to(DEV)
@@ -1245,6 +1270,41 @@ def test_rope_full_size_sampled():
         assert np.array_equal(from_dev(qo[bb, :, ss, :]), want)
         xk = from_dev(kd[bb, ss])
         assert np.array_equal(from_dev(ko[bb, :, ss, :]), rope.rotate(xk, cs[ss][None, :], sn[ss][None, :]))
+
+
+def test_rope_above_2_31_elements():
+    """q of 2^31 + 2^25 elements (B = 1, S = 65,792, Hq = 256, D = 128, plus
+    Hkv = 4), forward and backward: 64-bit element offsets in both layouts;
+    sampled positions (the last ones included) against the oracle, a late
+    position offset making the phases wrap."""
+    from oracle import rope
+    b, s, hq, hkv, d = 1, 65_792, 256, 4, 128
+    assert b * s * hq * d > 1 << 31
+    pos0 = 3_000_000_000
+    rng = np.random.default_rng(12)
+    gen = torch.Generator(device=DEV).manual_seed(3)
+    qd = torch.randn((b, s, hq, d), generator=gen, device=DEV, dtype=torch.float32).to(torch.float16)
+    kd = torch.randn((b, s, hkv, d), generator=gen, device=DEV, dtype=torch.float32).to(torch.float16)
+    delta = rope.turn_increments(d)
+    dd = torch.from_numpy(delta.view(np.int32)).to(DEV)
+    qo = torch.empty((b, hq, s, d), dtype=torch.float16, device=DEV)
+    ko = torch.empty((b, hkv, s, d), dtype=torch.float16, device=DEV)
+    B.poly_rope_fwd(B.POLY_ROPE_POLY, qd, kd, qo, ko, dd, pos_offset=pos0)
+    picks = sorted(set(int(v) for v in rng.integers(0, s, 24)) | {0, s - 1})
+    for ss in picks:
+        cs, sn = rope.tables(1, delta, pos0 + ss)
+        assert np.array_equal(from_dev(qo[0, :, ss, :]), rope.rotate(from_dev(qd[0, ss]), cs, sn)), ss
+        assert np.array_equal(from_dev(ko[0, :, ss, :]), rope.rotate(from_dev(kd[0, ss]), cs, sn)), ss
+    gq = torch.empty_like(qd)
+    gk = torch.empty_like(kd)
+    B.poly_rope_bwd(B.POLY_ROPE_POLY, qo, ko, gq, gk, dd, pos_offset=pos0)
+    for ss in picks:
+        wq, wk = rope.rope_backward(from_dev(qo[:, :, ss:ss + 1, :]), from_dev(ko[:, :, ss:ss + 1, :]),
+                                    delta, pos0 + ss)
+        assert np.array_equal(from_dev(gq[:, ss:ss + 1]), wq), ss
+        assert np.array_equal(from_dev(gk[:, ss:ss + 1]), wk), ss
+    del qd, kd, qo, ko, gq, gk
+    torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------- graphs and streams
