@@ -24,6 +24,8 @@
  *   layout-compatible with cudaStream_t; NULL = the legacy default stream).
  *   Kernels run on the calling thread's current device.  They validate the
  *   arguments on the host, enqueue one kernel and return without waiting.
+ *   Several host threads may call them at once (each launch carries its
+ *   program as a kernel parameter; nothing is shared between launches).
  *   A launch failure is reported as POLY_ECUDA (the CUDA error is consumed
  *   and available through poly_last_cuda_error).
  * - Tensors hold 16-bit elements (FP16 or BF16 bit patterns), contiguous
@@ -147,7 +149,9 @@ int poly_fit_defaults(poly_fit_opts *opts);
  * monotone real-arithmetic replay for functions monotone on t >= 0); the
  * candidates (top_k of them if top_k > 0) are re-scored in the deployed fused
  * order and gated again, and the one with the smallest deployed-order error
- * (ties: better split rank, then the smaller clamp offset) is written to *out.  opts NULL = defaults.  Deterministic.  Host memory only.
+ * (exact ties: the smaller Table 2 metric, then the smaller Li, then the
+ * smaller Lc) is written to *out.  opts NULL = defaults.  Deterministic.
+ * Host memory only.  Thread-safe (concurrent calls give what lone calls give).
  * Returns POLY_EINVAL (bad enum, degree outside [3, 6], bad opts, out NULL)
  * or POLY_ENOFIT (no candidate passed). */
 int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
