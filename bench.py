@@ -13,9 +13,11 @@ same six programs through the MUFU-native control kernels, torch's native
 ops, the SwiGLU kernels (dense [8192 x 14336] and ragged 131,072 x 2048 BF16)
 and the L2-resident 4,194,304-element sweep as extras, an end-to-end figure
 through the public API with host buffers, SM clocks sampled during the timed
-region, and the CPU replay oracle's throughput on a bounded sample.
+region, and the CPU replay oracle's throughput on a bounded sample, run on
+every host core (one spawned worker process per core).
 
-``--impl reference`` times the CPU replay oracle itself as the reference arm.
+``--impl reference`` times the CPU replay oracle itself as the reference arm,
+on every host core in the same way.
 Multi-GPU: one process per GPU (torchrun); every rank runs the same
 per-GPU workload with no collective on the data path (weak scaling).
 """
@@ -213,45 +215,107 @@ def oracle_programs():
     return out
 
 
-def oracle_sample_time(n_sample):
-    """Time the CPU replay oracle on the first n_sample elements of the
-    workload for each of the six programs; returns (seconds, elements)."""
+_PROGS = None
+
+
+def _replay_six(x, dy):
+    """The oracle's six programs over one piece of the sample (in pieces of
+    2^22 elements, which bounds the replay's FP64 temporaries); returns the
+    seconds it took."""
+    global _PROGS
     from oracle.replay import backward, forward
-    x, dy = workloads.isolated_hbm("f16", n=n_sample)
-    progs = oracle_programs()
-    piece = 1 << 22                 # bounds the replay's FP64 temporaries
+    if _PROGS is None:
+        _PROGS = oracle_programs()
+    piece = 1 << 22
     t0 = time.perf_counter()
-    for lo in range(0, n_sample, piece):
+    for lo in range(0, x.size, piece):
         xs, dys = x[lo:lo + piece], dy[lo:lo + piece]
-        for p, (name, d, D) in zip(progs, SIX):
+        for p, (name, d, D) in zip(_PROGS, SIX):
             if d == 0:
                 forward(p, xs)
             else:
                 backward(p, xs, dys)
-    return time.perf_counter() - t0, 6 * n_sample
+    return time.perf_counter() - t0
+
+
+def _warm_worker(_):
+    time.sleep(0.2)                     # one task per worker: every worker imports the oracle
+    _replay_six(np.zeros(8, np.uint16), np.zeros(8, np.uint16))
+    return os.getpid()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """The CPU replay oracle, unchanged, on every host core: a sample is cut
+    into one contiguous piece per worker process.  Workers are spawned (no
+    CUDA state is inherited) and import the oracle before any timing."""
+
+    def __init__(self, workers):
+        self.workers = max(1, int(workers))
+        self.pool = None
+        if self.workers > 1:
+            import multiprocessing as mp
+            self.pool = mp.get_context("spawn").Pool(self.workers)
+            self.pool.map(_warm_worker, range(self.workers), chunksize=1)
+
+    def run(self, x, dy):
+        """(wall seconds, [seconds per piece], [elements per piece])."""
+        if self.pool is None:
+            t = _replay_six(x, dy)
+            return t, [t], [x.size]
+        b = np.linspace(0, x.size, self.workers + 1).astype(np.int64)
+        args = [(x[b[i]:b[i + 1]], dy[b[i]:b[i + 1]]) for i in range(self.workers)]
+        t0 = time.perf_counter()
+        per = self.pool.starmap(_replay_six, args, chunksize=1)
+        return time.perf_counter() - t0, per, [int(b[i + 1] - b[i]) for i in range(self.workers)]
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+
+
+def oracle_sample_time(n_sample, workers=1):
+    """Time the CPU replay oracle on the first n_sample elements of the
+    workload through each of the six programs, on `workers` processes.
+    Returns (wall seconds, elements x programs, CPU seconds, per-core
+    Gelem/s)."""
+    x, dy = workloads.isolated_hbm("f16", n=n_sample)
+    pool = OraclePool(workers)
+    try:
+        wall, per, sizes = pool.run(x, dy)
+    finally:
+        pool.close()
+    per_core = statistics.mean(6 * m / t / 1e9 for m, t in zip(sizes, per) if t > 0)
+    return wall, 6 * n_sample, sum(per), per_core
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    per_step = int(np.clip(2 ** 23 // max(1, args.steps + args.warmup), 2 ** 12, 2 ** 20))
-    from oracle.replay import backward, forward
+    cores = host_cores()
+    per_step = int(np.clip(2 ** 27 // max(1, args.steps + args.warmup), 2 ** 16, 2 ** 22))
     x, dy = workloads.isolated_hbm("f16", n=per_step)
-    progs = oracle_programs()
-
-    def step():
-        for p, (name, d, D) in zip(progs, SIX):
-            forward(p, x) if d == 0 else backward(p, x, dy)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+    pool = OraclePool(cores)
+    try:
+        for _ in range(args.warmup):
+            pool.run(x, dy)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pool.run(x, dy)
+        dt = time.perf_counter() - t0
+    finally:
+        pool.close()
     value = 6 * per_step * args.steps / dt / 1e9
-    sample = f"first {per_step} elements of x and dy per program per step (CPU replay oracle, numpy)"
+    sample = (f"first {per_step} elements of x and dy per program per step, cut into {cores} "
+              f"pieces on {cores} host cores (CPU replay oracle, numpy)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -259,7 +323,7 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "elements_per_program": per_step,
                        "note": "bounded sample of the workload; the oracle is a deliberately "
                                "plain CPU replay"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -423,12 +487,14 @@ def main():
 
     # ---- CPU oracle on a bounded sample
     if rank == 0 and args.cpu_sample > 0:
-        secs, elems = oracle_sample_time(args.cpu_sample)
-        result["cpu_baseline"] = {"value": elems / secs / 1e9, "unit": UNIT, "cores": 1,
-                                  "kind": "oracle",
+        cores = host_cores()
+        wall, elems, cpu_s, per_core = oracle_sample_time(args.cpu_sample, cores)
+        result["cpu_baseline"] = {"value": elems / wall / 1e9, "unit": UNIT, "cores": cores,
+                                  "kind": "oracle", "per_core_value": per_core,
                                   "sample": f"first {args.cpu_sample} elements of the workload "
-                                            f"through each of the six programs (numpy replay, "
-                                            f"{secs:.1f} s)"}
+                                            f"through each of the six programs, one contiguous "
+                                            f"piece per core (numpy replay, {wall:.1f} s wall, "
+                                            f"{cpu_s:.1f} s of CPU work)"}
     if rank == 0:
         if args.elements != workloads.N_HBM:
             result["config"]["workload"] = f"profiling case: {args.elements} elements"

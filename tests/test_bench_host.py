@@ -59,3 +59,18 @@ def test_kernel_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     src.write_text("int f(int x) { return x + 2; }\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_oracle_pool_covers_the_sample():
+    """The CPU baseline's worker pool (spawned processes) replays every
+    element of the sample once, in one contiguous piece per worker."""
+    import bench
+    import workloads
+    x, dy = workloads.isolated_hbm("f16", n=10_007)
+    pool = bench.OraclePool(3)
+    try:
+        wall, per, sizes = pool.run(x, dy)
+    finally:
+        pool.close()
+    assert sum(sizes) == x.size and len(per) == len(sizes) == 3
+    assert wall > 0 and all(t > 0 for t in per)
