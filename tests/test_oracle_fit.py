@@ -195,3 +195,31 @@ def test_search_gates_hold_on_golden_programs():
         if rng:
             assert y.min() >= rng[0] and y.max() <= rng[1], k
         assert p.lc <= p.li + 1
+
+
+def _gate(fn, d, fmt, coef, lc):
+    """The search's gates for one candidate (split-order replay on the score
+    grid, as the search applies them)."""
+    x = fit.score_grid(fmt)
+    cb = np.asarray(tf.from_f64(np.asarray(coef, dtype=np.float64), fmt))
+    lc_bits = tf.from_f64(lc, fmt)
+    y = evaluate(ref.form_of(fn, d), tuple(int(b) for b in cb), lc_bits, x, fmt, fused=False)
+    return bool(fit._gates(fn, d, y, fmt, cb, lc, x))
+
+
+def test_gates_reject_each_violation():
+    """§3.2 rejects shape or boundary violations: each gate alone turns away
+    a candidate built to break only it, and the accepted program passes."""
+    S, T, F = ref.SIGMOID, ref.TANH, ref.FWD
+    g = gp.load()["sigmoid.fwd.bf16.D3"]
+    assert _gate(S, F, "bf16", tf.decode(np.array(g.coef, np.uint16), "bf16"), g.lc)
+    # range: y = 1/2 + t/2 reaches 1.25 at Lc = 1.5 (monotone, finite, P(0) exact)
+    assert not _gate(S, F, "bf16", [0.0, 0.5, 0.0, 0.0], 1.5)
+    assert _gate(S, F, "bf16", [0.0, 0.25, 0.0, 0.0], 1.5)      # 1/2 + t/4 <= 0.875: passes
+    # shape: 1/2 + 0.25 t - 0.2 t^2 rises then falls, inside [0, 1] up to Lc = 1.5
+    assert not _gate(S, F, "bf16", [0.0, 0.25, -0.2, 0.0], 1.5)
+    # boundary: sigma' with P(0) = 0.3 instead of 1/4
+    assert not _gate(S, ref.BWD, "bf16", [0.3, 0.0, -0.01, 0.0, 0.0], 4.0)
+    assert _gate(S, ref.BWD, "bf16", [0.25, 0.0, -0.01, 0.0, 0.0], 4.0)
+    # finite: an FP16 tanh whose Horner chain overflows near the clamp
+    assert not _gate(T, F, "f16", [0.0, 1.0, 0.0, 0.0, 60000.0], 2.0)
