@@ -218,8 +218,18 @@ def test_gates_reject_each_violation():
     assert _gate(S, F, "bf16", [0.0, 0.25, 0.0, 0.0], 1.5)      # 1/2 + t/4 <= 0.875: passes
     # shape: 1/2 + 0.25 t - 0.2 t^2 rises then falls, inside [0, 1] up to Lc = 1.5
     assert not _gate(S, F, "bf16", [0.0, 0.25, -0.2, 0.0], 1.5)
-    # boundary: sigma' with P(0) = 0.3 instead of 1/4
-    assert not _gate(S, ref.BWD, "bf16", [0.3, 0.0, -0.01, 0.0, 0.0], 4.0)
+    # boundary: sigma' with P(0) = 0.2 instead of 1/4 (inside [0, 1/4], decreasing)
+    assert not _gate(S, ref.BWD, "bf16", [0.2, 0.0, -0.01, 0.0, 0.0], 4.0)
     assert _gate(S, ref.BWD, "bf16", [0.25, 0.0, -0.01, 0.0, 0.0], 4.0)
-    # finite: an FP16 tanh whose Horner chain overflows near the clamp
-    assert not _gate(T, F, "f16", [0.0, 1.0, 0.0, 0.0, 60000.0], 2.0)
+    # finite: an FP16 SiLU' (no exact range, not monotone, so no other gate
+    # applies) whose Horner chain overflows before the clamp
+    assert not _gate(ref.SILU, ref.BWD, "f16", [0.0, 0.0, 0.0, 60000.0], 4.0)
+    assert _gate(ref.SILU, ref.BWD, "f16", [0.0, 0.0, 0.0, 0.01], 4.0)
+
+
+@pytest.mark.parametrize("fn,D,li", [(ref.SIGMOID, 3, 1.0), (ref.SILU, 3, 2.0)])
+def test_clamp_bound_is_enforced(fn, D, li):
+    """Lc <= Li + 1 (§3.2): with a single short fit interval the best clamp
+    would lie beyond the bound, so the search must stop exactly at it."""
+    p = fit.search(fn, ref.FWD, "bf16", D, li_grid=[li])
+    assert p.lc == li + 1.0
