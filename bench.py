@@ -467,7 +467,7 @@ def main():
                           "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                           "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                           "algorithmic_bytes_per_launch": BYTES[d] * n,
-                          "traffic": recorded_traffic(kkey),
+                          "traffic": recorded_traffic(kkey) if n == workloads.N_HBM else None,
                           "share_of_step": per_ms[dom] / sum(per_ms)}
 
     # ---- extras: SwiGLU and the L2-resident sweep

@@ -1728,3 +1728,38 @@ def test_must_fail_perturbed_program_on_gpu():
         assert np.array_equal(got, forward(perturbed, X_ALL))
     finally:
         B.poly_reset_programs()
+
+
+def test_bench_line_keeps_its_contract():
+    """bench.py on a small case prints one JSON line with every key its
+    readers rely on, with consistent values."""
+    import json as _json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--elements", str(1 << 22),
+                        "--steps", "5", "--warmup", "3", "--no-extras", "--cpu-sample", "65536"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = _json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches", "env"):
+        assert k in d, k
+    assert d["steps"] == 5 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["value"] > 0
+    assert d["gpu_launches"] == 6 * 5 and d["higher_is_better"] is True
+    assert abs(d["value"] - 6 * (1 << 22) / (d["ms_per_step"] * 1e-3) / 1e9) < 1e-6 * d["value"]
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["traffic"] is None                      # recorded only for the full-size step
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["unit"] == d["unit"]
+    e = d["e2e"]
+    assert e["value"] > 0 and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 2 * 2 * (1 << 22) and e["d2h_bytes_per_step"] == 6 * 2 * (1 << 22)
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    assert "workload" in d["config"]
