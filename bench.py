@@ -757,7 +757,28 @@ def swiglu_extras(args, dev, stream, peak):
                           "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
     finally:
         B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
-    del gd, ud, dyd, y, dg, du
+    del y, dg, du
+    # training step of the activation through autograd on a fused gate-up
+    # buffer [8192, 2 x 14336]: forward + backward, gradient into one buffer
+    from polynomial_activation_gb300 import ops
+    h = gd.shape[1]
+    gu = torch.cat([gd, ud], dim=1).requires_grad_(True)
+    del gd, ud
+
+    def autograd_step(f):
+        def step():
+            gu.grad = None
+            f(gu).backward(dyd)
+        return step
+
+    for label, f in [
+        ("packed_autograd_fwd_bwd", ops.swiglu_packed),
+        ("sliced_autograd_fwd_bwd", lambda a: ops.swiglu(a[:, :h], a[:, h:])),
+        ("torch_autograd_fwd_bwd", lambda a: torch.nn.functional.silu(a[:, :h]) * a[:, h:]),
+    ]:
+        ms = min(_time(autograd_step(f), stream, reps, warm=6) for _ in range(3))
+        out[label] = {"ms": ms, "gbs": 16 * n / ms / 1e6, "frac": 16 * n / ms / 1e6 / peak}
+    del gu, dyd
     g, u, dy, seg = workloads.ragged_swiglu("bf16")
     gd, ud, dyd = t(g), t(u), t(dy)
     del g, u, dy
@@ -773,6 +794,9 @@ def swiglu_extras(args, dev, stream, peak):
                       "frac": nbytes * n / ms / 1e6 / peak,
                       "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
     out["config"] = {"dense": "BF16 [8192 x 14336], gate/up 2 N(0,1), dy N(0,1)",
+                     "autograd": "forward + backward through torch.autograd on one [8192, "
+                                 "28672] gate-up buffer; GB/s counts 16 bytes per element "
+                                 "(fwd 6, bwd 10); best of 3 rounds of 20 steps",
                      "ragged": "BF16 131,072 x 2048 rows from 64 Zipf(1.1) segments, N(0,1.5^2)"}
     return out
 

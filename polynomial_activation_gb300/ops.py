@@ -138,6 +138,49 @@ def swiglu(g, u):
     return PolySwiGLU.apply(g, u) if _grad(g, u) else swiglu_fwd(_rows(g), _rows(u))
 
 
+def _halves(gu):
+    """[rows, 2H] row-major view of a fused gate-up buffer and its two halves."""
+    two_h = gu.shape[-1]
+    if two_h % 2:
+        raise ValueError("the last dimension of a fused gate-up buffer must be even")
+    gu2 = gu if gu.dim() == 2 and gu.stride(1) == 1 else _dense(gu).view(-1, two_h)
+    h = two_h // 2
+    return gu2, gu2[:, :h], gu2[:, h:]
+
+
+def _packed_fwd(gu):
+    gu2, g, u = _halves(gu)
+    y = torch.empty((gu2.shape[0], g.shape[1]), dtype=gu.dtype, device=gu.device)
+    B.poly_swiglu_fwd(_dt(gu), g, u, y)
+    return y.view(*gu.shape[:-1], g.shape[1])
+
+
+class PolySwiGLUPacked(torch.autograd.Function):
+    """y = SiLU(gu[..., :H]) * gu[..., H:] for a fused gate-up buffer
+    [..., 2H] (one projection producing both halves).  The backward writes
+    dgate and dup straight into the two halves of one [..., 2H] gradient, so
+    no slice gradients are assembled afterwards."""
+
+    @staticmethod
+    def forward(ctx, gu):
+        ctx.save_for_backward(gu)
+        return _packed_fwd(gu)
+
+    @staticmethod
+    def backward(ctx, dy):
+        (gu,) = ctx.saved_tensors
+        gu2, g, u = _halves(gu)
+        h = g.shape[1]
+        dgu = torch.empty((gu2.shape[0], 2 * h), dtype=gu.dtype, device=gu.device)
+        B.poly_swiglu_bwd(_dt(gu), g, u, _dense(dy).view(-1, h), dgu[:, :h], dgu[:, h:])
+        return dgu.view(gu.shape)
+
+
+def swiglu_packed(gu):
+    """SwiGLU of a fused gate-up buffer [..., 2H] -> [..., H]."""
+    return PolySwiGLUPacked.apply(gu) if _grad(gu) else _packed_fwd(gu)
+
+
 class PolySwiGLURagged(torch.autograd.Function):
     """Routed-expert SwiGLU over rows [seg_off[0], seg_off[E]) of [cap_rows,
     cols] gate / up buffers (offsets stay on the device); rows outside the

@@ -1521,6 +1521,33 @@ def test_wrappers_without_autograd_match_recorded_calls():
     assert torch.equal(gk.view(torch.int16), wk.detach().view(torch.int16))
 
 
+def test_swiglu_packed_gate_up_buffer():
+    """ops.swiglu_packed on a fused [.., 2H] gate-up buffer: the same bits as
+    the separate-tensor SwiGLU, forward and backward, with the gradient
+    written as one [.., 2H] tensor; 2-D and 3-D, recorded and not."""
+    from polynomial_activation_gb300 import ops
+    rng = np.random.default_rng(79)
+    for dt in DTS:
+        for shape in ((64, 2 * 200), (3, 7, 2 * 48)):
+            m = int(np.prod(shape))
+            gu = to_dev(_rand_bits(rng, m, FMT[dt]), dt).view(*shape)
+            dy = to_dev(_rand_bits(rng, m // 2, FMT[dt]), dt).view(*shape[:-1], shape[-1] // 2)
+            h = shape[-1] // 2
+            g, u = gu[..., :h].contiguous(), gu[..., h:].contiguous()
+            want = ops.swiglu_fwd(g.reshape(-1, h), u.reshape(-1, h)).view(*shape[:-1], h)
+            got = ops.swiglu_packed(gu)
+            assert got.shape == want.shape and got.grad_fn is None
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+            gur = gu.clone().requires_grad_(True)
+            y = ops.swiglu_packed(gur)
+            assert torch.equal(y.detach().view(torch.int16), want.view(torch.int16))
+            y.backward(dy)
+            dg, du = ops.swiglu_bwd(g.reshape(-1, h), u.reshape(-1, h), dy.reshape(-1, h))
+            assert gur.grad.shape == gu.shape
+            assert torch.equal(gur.grad[..., :h].reshape(-1, h).view(torch.int16), dg.view(torch.int16))
+            assert torch.equal(gur.grad[..., h:].reshape(-1, h).view(torch.int16), du.view(torch.int16))
+
+
 def test_calls_use_the_current_stream():
     """With no stream argument the binding launches on the current stream of
     the current device, inside and outside a torch.cuda.stream context."""
