@@ -793,6 +793,16 @@ def swiglu_extras(args, dev, stream, peak):
         out[label] = {"ms": ms, "gelem_s": n / ms / 1e6, "gbs": nbytes * n / ms / 1e6,
                       "frac": nbytes * n / ms / 1e6 / peak,
                       "vs_same_bytes_copy": same_bytes_copy_ms(nbytes * n, dev, stream) / ms}
+    # autograd forward + backward over the ragged rows (the offsets cover every row)
+    from polynomial_activation_gb300 import ops
+    gr = gd.requires_grad_(True)
+    for label, pf in [("ragged_autograd_fwd_bwd", False),
+                      ("ragged_autograd_fwd_bwd_padding_free", True)]:
+        def step(pf=pf):
+            gr.grad = None
+            ops.swiglu_ragged(gr, ud, segd, padding_free=pf).backward(dyd)
+        ms = min(_time(step, stream, reps, warm=6) for _ in range(3))
+        out[label] = {"ms": ms, "gbs": 16 * n / ms / 1e6, "frac": 16 * n / ms / 1e6 / peak}
     out["config"] = {"dense": "BF16 [8192 x 14336], gate/up 2 N(0,1), dy N(0,1)",
                      "autograd": "forward + backward through torch.autograd on one [8192, "
                                  "28672] gate-up buffer; GB/s counts 16 bytes per element "

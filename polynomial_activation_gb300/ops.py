@@ -184,30 +184,39 @@ def swiglu_packed(gu):
 class PolySwiGLURagged(torch.autograd.Function):
     """Routed-expert SwiGLU over rows [seg_off[0], seg_off[E]) of [cap_rows,
     cols] gate / up buffers (offsets stay on the device); rows outside the
-    range are left zero in the output and in both gradients."""
+    range are left zero in the output and in both gradients.  With
+    padding_free the caller guarantees seg_off[0] = 0 and seg_off[E] =
+    cap_rows, so every row is written by the kernel and no buffer is zeroed
+    first."""
 
     @staticmethod
-    def forward(ctx, g, u, seg_off):
+    def forward(ctx, g, u, seg_off, padding_free):
         g, u = _dense(g), _dense(u)
         ctx.save_for_backward(g, u, seg_off)
-        return _ragged_fwd(g, u, seg_off)
+        ctx.padding_free = padding_free
+        return _ragged_fwd(g, u, seg_off, padding_free)
 
     @staticmethod
     def backward(ctx, dy):
         g, u, seg_off = ctx.saved_tensors
-        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off, dg=torch.zeros_like(g),
-                                   du=torch.zeros_like(g))
-        return dg, du, None
+        alloc = torch.empty_like if ctx.padding_free else torch.zeros_like
+        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off, dg=alloc(g), du=alloc(g))
+        return dg, du, None, None
 
 
-def _ragged_fwd(g, u, seg_off):
-    return swiglu_fwd_ragged(g, u, seg_off, out=torch.zeros_like(g))
+def _ragged_fwd(g, u, seg_off, padding_free=False):
+    out = torch.empty_like(g) if padding_free else torch.zeros_like(g)
+    return swiglu_fwd_ragged(g, u, seg_off, out=out)
 
 
-def swiglu_ragged(g, u, seg_off):
+def swiglu_ragged(g, u, seg_off, padding_free: bool = False):
+    """padding_free=True: seg_off[0] = 0 and seg_off[E] = g.shape[0] (every
+    row belongs to a segment); the outputs are then not zero-filled first.
+    Rows outside the range would be left uninitialised, so pass it only when
+    that holds."""
     if _grad(g, u):
-        return PolySwiGLURagged.apply(g, u, seg_off)
-    return _ragged_fwd(_dense(g), _dense(u), seg_off)
+        return PolySwiGLURagged.apply(g, u, seg_off, padding_free)
+    return _ragged_fwd(_dense(g), _dense(u), seg_off, padding_free)
 
 
 class PolySoftcap(torch.autograd.Function):

@@ -1548,6 +1548,34 @@ def test_swiglu_packed_gate_up_buffer():
             assert torch.equal(gur.grad[..., h:].reshape(-1, h).view(torch.int16), du.view(torch.int16))
 
 
+def test_swiglu_ragged_padding_free():
+    """With padding_free (the offsets cover every row) the ragged wrapper
+    skips the zero fill and gives the same bits, recorded and not."""
+    from polynomial_activation_gb300 import ops
+    rng = np.random.default_rng(80)
+    for dt in DTS:
+        rows, cols = 96, 136
+        g = to_dev(_rand_bits(rng, rows * cols, FMT[dt]), dt).view(rows, cols)
+        u = to_dev(_rand_bits(rng, rows * cols, FMT[dt]), dt).view(rows, cols)
+        dy = to_dev(_rand_bits(rng, rows * cols, FMT[dt]), dt).view(rows, cols)
+        seg = torch.tensor([0, 30, 30, 77, rows], dtype=torch.int32, device=DEV)
+        want = ops.swiglu_ragged(g, u, seg)
+        got = ops.swiglu_ragged(g, u, seg, padding_free=True)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        assert torch.equal(want.view(torch.int16), ops.swiglu_fwd(g, u).view(torch.int16))
+        grads = []
+        for pf in (False, True):
+            gr, ur = g.clone().requires_grad_(True), u.clone().requires_grad_(True)
+            y = ops.swiglu_ragged(gr, ur, seg, padding_free=pf)
+            y.backward(dy)
+            grads.append((y.detach(), gr.grad, ur.grad))
+        for a, b in zip(*grads):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        dg, du = ops.swiglu_bwd(g, u, dy)
+        assert torch.equal(grads[1][1].view(torch.int16), dg.view(torch.int16))
+        assert torch.equal(grads[1][2].view(torch.int16), du.view(torch.int16))
+
+
 def test_calls_use_the_current_stream():
     """With no stream argument the binding launches on the current stream of
     the current device, inside and outside a torch.cuda.stream context."""
