@@ -7,7 +7,9 @@ from polynomial_activation_gb300 import ops
 
 
 @pytest.mark.parametrize("f", [ops.sigmoid, ops.tanh, ops.silu, ops.gelu,
-                               lambda t: ops.softcap(t, 30.0)])
+                               lambda t: ops.softcap(t, 30.0),
+                               lambda t: ops.swiglu_packed(t.view(8, 8)),
+                               lambda t: ops.swiglu(t.view(8, 8), t.view(8, 8))])
 def test_host_tensor_is_refused(f):
     x = torch.zeros(64, dtype=torch.float16)
     with pytest.raises(ValueError, match="no CPU path"):
@@ -32,3 +34,8 @@ def test_grad_decision():
         assert not ops._grad(xr)
     with torch.inference_mode():
         assert not ops._grad(xr)
+
+
+def test_packed_buffer_needs_an_even_last_dimension():
+    with pytest.raises(ValueError, match="even"):
+        ops.swiglu_packed(torch.zeros(4, 7, dtype=torch.float16))
