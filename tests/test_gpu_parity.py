@@ -1521,12 +1521,22 @@ def test_wrappers_without_autograd_match_recorded_calls():
     assert torch.equal(gk.view(torch.int16), wk.detach().view(torch.int16))
 
 
-def test_swiglu_packed_gate_up_buffer():
+@pytest.mark.parametrize("variant", [B.POLY_SWIGLU_DIRECT, B.POLY_SWIGLU_SIGMOID])
+def test_swiglu_packed_gate_up_buffer(variant):
     """ops.swiglu_packed on a fused [.., 2H] gate-up buffer: the same bits as
     the separate-tensor SwiGLU, forward and backward, with the gradient
-    written as one [.., 2H] tensor; 2-D and 3-D, recorded and not."""
+    written as one [.., 2H] tensor; 2-D and 3-D, recorded and not; under
+    both SwiGLU rules."""
     from polynomial_activation_gb300 import ops
     rng = np.random.default_rng(79)
+    B.poly_set_swiglu_variant(variant)
+    try:
+        _packed_cases(ops, rng)
+    finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
+
+
+def _packed_cases(ops, rng):
     for dt in DTS:
         for shape in ((64, 2 * 200), (3, 7, 2 * 48)):
             m = int(np.prod(shape))
