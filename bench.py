@@ -773,7 +773,8 @@ def swiglu_extras(args, dev, stream, peak):
 
     for label, f in [
         ("packed_autograd_fwd_bwd", ops.swiglu_packed),
-        ("sliced_autograd_fwd_bwd", lambda a: ops.swiglu(a[:, :h], a[:, h:])),
+        ("chunked_autograd_fwd_bwd", lambda a: ops.swiglu(*a.chunk(2, dim=-1))),
+        ("slice_gradients_autograd_fwd_bwd", lambda a: ops.PolySwiGLU.apply(a[:, :h], a[:, h:])),
         ("torch_autograd_fwd_bwd", lambda a: torch.nn.functional.silu(a[:, :h]) * a[:, h:]),
     ]:
         ms = min(_time(autograd_step(f), stream, reps, warm=6) for _ in range(3))

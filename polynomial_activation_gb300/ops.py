@@ -134,8 +134,42 @@ class PolySwiGLU(torch.autograd.Function):
         return swiglu_bwd(g, u, _rows(dy))
 
 
+def _fused_base(g, u):
+    """The contiguous [..., 2H] buffer whose two halves g and u are (as from
+    gu.chunk(2, dim=-1), possibly through a reshape of gu), or None."""
+    b = g._base
+    if b is None or u._base is not b or not b.is_contiguous() or g.dim() == 0:
+        return None
+    # differentiable views of a buffer that is itself in the graph
+    if not (b.requires_grad and g.grad_fn is not None and u.grad_fn is not None):
+        return None
+    h = g.shape[-1]
+    if g.shape != u.shape or b.shape[-1] != 2 * h or b.numel() != 2 * g.numel():
+        return None
+    es = g.element_size()
+    if g.data_ptr() != b.data_ptr() or u.data_ptr() != b.data_ptr() + h * es:
+        return None
+    # g and u must be rows of h elements, one every 2h, in row-major order
+    want = 2 * h
+    for d in range(g.dim() - 2, -1, -1):
+        if g.stride(d) != want and g.shape[d] != 1:
+            return None
+        want *= g.shape[d]
+    if g.stride(-1) != 1 or g.stride() != u.stride():
+        return None
+    return b
+
+
 def swiglu(g, u):
-    return PolySwiGLU.apply(g, u) if _grad(g, u) else swiglu_fwd(_rows(g), _rows(u))
+    """SiLU(g) * u.  When g and u are the two halves of one fused gate-up
+    buffer (gu.chunk(2, dim=-1)), the recorded path runs on that buffer so
+    that the backward writes one [..., 2H] gradient (see swiglu_packed)."""
+    if not _grad(g, u):
+        return swiglu_fwd(_rows(g), _rows(u))
+    b = _fused_base(g, u)
+    if b is not None:
+        return PolySwiGLUPacked.apply(b).view(g.shape)
+    return PolySwiGLU.apply(g, u)
 
 
 def _halves(gu):

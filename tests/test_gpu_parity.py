@@ -1558,6 +1558,51 @@ def _packed_cases(ops, rng):
             assert torch.equal(gur.grad[..., h:].reshape(-1, h).view(torch.int16), du.view(torch.int16))
 
 
+def test_swiglu_on_chunked_halves_takes_the_fused_path():
+    """ops.swiglu(*gu.chunk(2, -1)) with a gate-up buffer in the graph runs on
+    the buffer itself (one gradient buffer): the same bits as separate
+    leaves, also through a reshape of the buffer and with the gate used
+    elsewhere in the graph too."""
+    from polynomial_activation_gb300 import ops
+    rng = np.random.default_rng(81)
+    for dt in DTS:
+        rows, h = 48, 96
+        gu0 = to_dev(_rand_bits(rng, rows * 2 * h, FMT[dt]), dt).view(rows, 2 * h)
+        dy = to_dev(_rand_bits(rng, rows * h, FMT[dt]), dt).view(rows, h)
+        g0, u0 = gu0[:, :h].contiguous(), gu0[:, h:].contiguous()
+        want_y = ops.swiglu_fwd(g0, u0)
+        want_dg, want_du = ops.swiglu_bwd(g0, u0, dy)
+        # a leaf buffer, chunked
+        gu = gu0.clone().requires_grad_(True)
+        g, u = gu.chunk(2, dim=-1)
+        assert ops._fused_base(g, u) is gu
+        y = ops.swiglu(g, u)
+        assert torch.equal(y.detach().view(torch.int16), want_y.view(torch.int16))
+        y.backward(dy)
+        assert torch.equal(gu.grad[:, :h].view(torch.int16), want_dg.view(torch.int16))
+        assert torch.equal(gu.grad[:, h:].view(torch.int16), want_du.view(torch.int16))
+        # a non-leaf buffer reshaped to [4, 12, 2H] before chunking; the gate
+        # also feeds a second term of the loss (finite normal inputs: the
+        # gradients from the two paths are summed by autograd)
+        gu1 = to_dev(workloads.normal(rows * 2 * h, 82, 1.0, FMT[dt]), dt).view(rows, 2 * h)
+        dy1 = to_dev(workloads.normal(rows * h, 83, 1.0, FMT[dt]), dt).view(rows, h)
+        src = gu1.float().requires_grad_(True)
+        x = src.to(TDT[dt]).view(4, rows // 4, 2 * h)
+        g, u = x.chunk(2, dim=-1)
+        assert ops._fused_base(g, u) is not None
+        y = ops.swiglu(g, u)
+        assert y.shape == (4, rows // 4, h)
+        ((y * dy1.view(4, rows // 4, h)).float().sum() + g.float().sum()).backward()
+        # reference with separate leaves
+        gl = gu1[:, :h].contiguous().requires_grad_(True)
+        ul = gu1[:, h:].contiguous().requires_grad_(True)
+        yl = ops.swiglu(gl, ul)
+        ((yl * dy1).float().sum() + gl.float().sum()).backward()
+        got = src.grad.to(TDT[dt])
+        assert torch.equal(got[:, :h].view(torch.int16), gl.grad.view(torch.int16))
+        assert torch.equal(got[:, h:].view(torch.int16), ul.grad.view(torch.int16))
+
+
 def test_swiglu_ragged_padding_free():
     """With padding_free (the offsets cover every row) the ragged wrapper
     skips the zero fill and gives the same bits, recorded and not."""
