@@ -39,3 +39,26 @@ def test_grad_decision():
 def test_packed_buffer_needs_an_even_last_dimension():
     with pytest.raises(ValueError, match="even"):
         ops.swiglu_packed(torch.zeros(4, 7, dtype=torch.float16))
+
+
+def test_fused_base_detection():
+    """ops.swiglu routes the two halves of one gate-up buffer in the graph to
+    the fused-buffer path, and only those."""
+    gu = torch.zeros(6, 10, dtype=torch.float16, requires_grad=True)
+    g, u = gu.chunk(2, dim=-1)
+    assert ops._fused_base(g, u) is gu
+    assert ops._fused_base(u, g) is None                        # halves swapped
+    root = torch.zeros(12, 10, requires_grad=True).half()       # a non-leaf buffer
+    g, u = root.view(3, 4, 10).chunk(2, dim=-1)                 # through a reshape
+    assert ops._fused_base(g, u) is root
+    wide = torch.zeros(6, 15, requires_grad=True).half()
+    assert ops._fused_base(wide[:, :5], wide[:, 5:10]) is None  # not the whole buffer
+    other = torch.zeros(6, 5, dtype=torch.float16, requires_grad=True)
+    assert ops._fused_base(gu[:, :5], other) is None            # u from another buffer
+    plain = torch.zeros(6, 10, dtype=torch.float16)
+    assert ops._fused_base(*plain.chunk(2, dim=-1)) is None     # no graph to route
+    with torch.no_grad():
+        g, u = gu.chunk(2, dim=-1)
+    assert ops._fused_base(g, u) is None                        # views made without grad
+    t = torch.zeros(10, 6, dtype=torch.float16, requires_grad=True).t()
+    assert ops._fused_base(*t.chunk(2, dim=-1)) is None         # buffer not row-major
