@@ -247,6 +247,20 @@ int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u,
                            int64_t cap_rows, int64_t cols, int32_t *status,
                            poly_stream_t stream);
 
+/* Zero the rows of a [cap_rows, cols] buffer of 16-bit elements (any format:
+ * +0 is all-zero bits) that the ragged calls above leave untouched: rows
+ * outside [max(seg_off[0], 0), min(seg_off[num_segments], cap_rows)), the
+ * range read on the device as those calls read it (empty when the offsets
+ * cross or start past the buffer: every row is zeroed then).  Paired with a ragged
+ * call on the same stream (in either order) it gives an output or gradient
+ * that reads as zero outside the segments, writing each row once instead of
+ * filling the whole buffer first; when the segments cover every row it
+ * writes nothing.  out: device (or pinned host) memory, 2-byte aligned.
+ * POLY_EINVAL if seg_off or out is NULL (with work to do), num_segments,
+ * cap_rows or cols is negative, or the extent is too large (Sizes rule). */
+int poly_ragged_zero_outside(void *out, const int32_t *seg_off, int num_segments,
+                             int64_t cap_rows, int64_t cols, poly_stream_t stream);
+
 /* ---- tanh softcap (§2.3 eq. 1; §3.3 eq. 12) -------------------------------
  * softcap_alpha(x) = alpha tanh(x / alpha), the attention-logit softcap.
  * Forward:   z = x * A_inv,  y = A * tanh_program(z)

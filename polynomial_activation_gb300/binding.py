@@ -24,7 +24,7 @@ FN = {"sigmoid": POLY_SIGMOID, "tanh": POLY_TANH, "silu": POLY_SILU, "gelu": POL
 FN_NAMES = {v: k for k, v in FN.items()}
 
 # version of include/polyact.h this binding marshals for (poly_abi_version)
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 # every function declared in include/polyact.h
 EXPORTS = [
@@ -32,6 +32,7 @@ EXPORTS = [
     "poly_default_degree", "poly_fit_defaults", "poly_fit", "poly_set_program",
     "poly_get_program", "poly_reset_programs", "poly_act_fwd", "poly_act_bwd",
     "poly_swiglu_fwd", "poly_swiglu_bwd", "poly_swiglu_fwd_ragged", "poly_swiglu_bwd_ragged",
+    "poly_ragged_zero_outside",
     "poly_ctrl_act_fwd", "poly_ctrl_act_bwd", "poly_ctrl_swiglu_fwd", "poly_ctrl_swiglu_bwd",
     "poly_diag_packed", "poly_set_swiglu_variant", "poly_get_swiglu_variant",
     "poly_debug_fail_launches",
@@ -127,6 +128,7 @@ def lib():
                                      _i64, _i64, _p]
     L.poly_swiglu_fwd_ragged.argtypes = [_i, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
     L.poly_swiglu_bwd_ragged.argtypes = [_i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
+    L.poly_ragged_zero_outside.argtypes = [_p, _p, _i, _i64, _i64, _p]
     L.poly_diag_packed.argtypes = [_i, _i, _p, _p, _p, _p, _i64, _p]
     L.poly_debug_fail_launches.argtypes = [_i, _i]
     for name in EXPORTS:
@@ -402,6 +404,18 @@ def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, 
                                         _ptr(seg_off), num_segments, cap_rows, cols,
                                         _ptr(status), _stream(stream)),
            "poly_swiglu_bwd_ragged")
+
+
+def poly_ragged_zero_outside(out, seg_off, num_segments=None, cap_rows=None, cols=None,
+                             stream=None):
+    """Zero the rows of out [cap_rows, cols] outside [seg_off[0], seg_off[E])."""
+    num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
+    cap_rows = out.shape[0] if cap_rows is None else cap_rows
+    cols = out.shape[1] if cols is None else cols
+    _room(out, 2 * cap_rows * cols, "poly_ragged_zero_outside", "out")
+    _room(seg_off, 4 * (num_segments + 1), "poly_ragged_zero_outside", "seg_off", esize=4)
+    _check(lib().poly_ragged_zero_outside(_ptr(out), _ptr(seg_off), num_segments, cap_rows, cols,
+                                          _stream(stream)), "poly_ragged_zero_outside")
 
 
 def poly_diag_packed(op, dtype, a, b, c, out, n=None, stream=None):

@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpolyact.so")
-SOURCES = ["kern_act.cu", "kern_swiglu.cu", "kern_ctrl.cu", "kern_common.cu", "kern_softcap.cu", "kern_exp2.cu", "kern_rope.cu",
+SOURCES = ["kern_act.cu", "kern_swiglu.cu", "kern_ctrl.cu", "kern_common.cu", "kern_softcap.cu", "kern_exp2.cu", "kern_rope.cu", "kern_fill.cu",
            "capi.cpp", "fit.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # host code: no floating-point contraction, so the fitter's FP64 arithmetic is

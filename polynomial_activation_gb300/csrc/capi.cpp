@@ -301,7 +301,7 @@ const char *poly_status_str(int status) {
 
 int poly_last_cuda_error(void) { return t_last_cuda_error; }
 
-int poly_abi_version(void) { return 2; }
+int poly_abi_version(void) { return 3; }
 
 int poly_debug_fail_launches(int cuda_error, int count) {
   if (cuda_error <= 0 || count < 0) return POLY_EINVAL;
@@ -528,6 +528,18 @@ int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u, const void *
                            int64_t cols, int32_t *status, poly_stream_t stream) {
   return ragged_call(true, dtype, g, u, dy, dg, du, seg_off, num_segments, cap_rows, cols,
                      status, stream);
+}
+
+int poly_ragged_zero_outside(void *out, const int32_t *seg_off, int num_segments,
+                             int64_t cap_rows, int64_t cols, poly_stream_t stream) {
+  if (seg_off == nullptr || num_segments < 0 || cap_rows < 0 || cols < 0) return POLY_EINVAL;
+  if (cap_rows == 0 || cols == 0) return POLY_OK;
+  const int64_t n = checked_mul(cap_rows, cols);
+  if (n < 0 || out == nullptr || !even_address(out) || !span_flat(out, n).ok) return POLY_EINVAL;
+  return launch_status([&] {
+    return launch_zero_outside(static_cast<uint16_t *>(out), seg_off, num_segments, cap_rows,
+                               cols, reinterpret_cast<cudaStream_t>(stream));
+  });
 }
 
 // Shared part of the softcap calls: alpha must give finite, non-zero

@@ -81,6 +81,11 @@ struct RopeConsts {
 cudaError_t launch_rope(int variant, int inv, const RopeArgs &a, const RopeConsts &k,
                         cudaStream_t stream);
 
+// Zero the rows of a [cap_rows, cols] 16-bit buffer outside [seg[0], seg[nseg])
+// (clamped to [0, cap_rows] on the device, as the ragged kernels do).
+cudaError_t launch_zero_outside(uint16_t *out, const int32_t *seg, int32_t nseg,
+                                int64_t cap_rows, int64_t cols, cudaStream_t stream);
+
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
                         cudaStream_t stream);

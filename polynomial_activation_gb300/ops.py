@@ -218,10 +218,10 @@ def swiglu_packed(gu):
 class PolySwiGLURagged(torch.autograd.Function):
     """Routed-expert SwiGLU over rows [seg_off[0], seg_off[E]) of [cap_rows,
     cols] gate / up buffers (offsets stay on the device); rows outside the
-    range are left zero in the output and in both gradients.  With
-    padding_free the caller guarantees seg_off[0] = 0 and seg_off[E] =
-    cap_rows, so every row is written by the kernel and no buffer is zeroed
-    first."""
+    range are zero in the output and in both gradients (written once, by
+    poly_ragged_zero_outside).  With padding_free the caller guarantees
+    seg_off[0] = 0 and seg_off[E] = cap_rows, so the kernel writes every row
+    and the zeroing launch is skipped."""
 
     @staticmethod
     def forward(ctx, g, u, seg_off, padding_free):
@@ -233,21 +233,26 @@ class PolySwiGLURagged(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         g, u, seg_off = ctx.saved_tensors
-        alloc = torch.empty_like if ctx.padding_free else torch.zeros_like
-        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off, dg=alloc(g), du=alloc(g))
+        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off)
+        if not ctx.padding_free:
+            B.poly_ragged_zero_outside(dg, seg_off)
+            B.poly_ragged_zero_outside(du, seg_off)
         return dg, du, None, None
 
 
 def _ragged_fwd(g, u, seg_off, padding_free=False):
-    out = torch.empty_like(g) if padding_free else torch.zeros_like(g)
-    return swiglu_fwd_ragged(g, u, seg_off, out=out)
+    y = swiglu_fwd_ragged(g, u, seg_off)
+    if not padding_free:
+        B.poly_ragged_zero_outside(y, seg_off)
+    return y
 
 
 def swiglu_ragged(g, u, seg_off, padding_free: bool = False):
-    """padding_free=True: seg_off[0] = 0 and seg_off[E] = g.shape[0] (every
-    row belongs to a segment); the outputs are then not zero-filled first.
-    Rows outside the range would be left uninitialised, so pass it only when
-    that holds."""
+    """Rows outside [seg_off[0], seg_off[E]) of the output (and of the
+    gradients) are zero: one extra launch zeroes them on the device, writing
+    nothing when the segments cover every row.  padding_free=True (seg_off[0]
+    = 0 and seg_off[E] = g.shape[0]) skips that launch; rows outside the range
+    would then be left uninitialised, so pass it only when that holds."""
     if _grad(g, u):
         return PolySwiGLURagged.apply(g, u, seg_off, padding_free)
     return _ragged_fwd(_dense(g), _dense(u), seg_off, padding_free)

@@ -117,7 +117,7 @@ def test_fit_argument_errors(L):
         o = B.poly_fit_defaults()
         setattr(o, field, value)
         assert L.poly_fit(0, 0, 0, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_EINVAL
-    assert L.poly_abi_version() == B.ABI_VERSION == 2
+    assert L.poly_abi_version() == B.ABI_VERSION == 3
     # no admissible clamp at all: Lc starts above Li + 1
     o = B.poly_fit_defaults()
     o.li_max, o.lc_min = 2.0, 5.0
@@ -164,6 +164,13 @@ def test_device_calls_reject_bad_arguments_on_host(L):
     # ragged: null offsets, negative segments
     assert L.poly_swiglu_fwd_ragged(1, FAKE, FAKE + 8192, FAKE + 16384, None, 4, 4, 16, None, s) == B.POLY_EINVAL
     assert L.poly_swiglu_fwd_ragged(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 30000, -1, 4, 16, None, s) == B.POLY_EINVAL
+    # zero fill outside the segments: null / odd buffer, null offsets, negative sizes
+    assert L.poly_ragged_zero_outside(None, FAKE, 4, 4, 16, s) == B.POLY_EINVAL
+    assert L.poly_ragged_zero_outside(FAKE + 1, FAKE + 30000, 4, 4, 16, s) == B.POLY_EINVAL
+    assert L.poly_ragged_zero_outside(FAKE, None, 4, 4, 16, s) == B.POLY_EINVAL
+    assert L.poly_ragged_zero_outside(FAKE, FAKE + 30000, -1, 4, 16, s) == B.POLY_EINVAL
+    assert L.poly_ragged_zero_outside(FAKE, FAKE + 30000, 4, -4, 16, s) == B.POLY_EINVAL
+    assert L.poly_ragged_zero_outside(FAKE, FAKE + 30000, 4, 1 << 40, 1 << 40, s) == B.POLY_EINVAL
     # controls share the validation
     assert L.poly_ctrl_act_fwd(0, 0, FAKE + 1, FAKE + 4096, 8, s) == B.POLY_EINVAL
     assert L.poly_ctrl_swiglu_bwd(1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576, FAKE + 24578,
@@ -242,6 +249,8 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_swiglu_fwd(1, None, None, None, 0, 16, 16, 16, 16, s) == B.POLY_OK
     assert L.poly_swiglu_bwd(1, None, None, None, None, None, 5, 0, 0, 0, 0, 0, 0, s) == B.POLY_OK
     assert L.poly_swiglu_fwd_ragged(1, None, None, None, FAKE, 4, 0, 16, None, s) == B.POLY_OK
+    assert L.poly_ragged_zero_outside(None, FAKE, 4, 0, 16, s) == B.POLY_OK
+    assert L.poly_ragged_zero_outside(None, FAKE, 4, 8, 0, s) == B.POLY_OK
     assert L.poly_diag_packed(0, 0, None, None, None, None, 0, s) == B.POLY_OK
     assert L.poly_last_cuda_error() == before
 

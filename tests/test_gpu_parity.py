@@ -1631,6 +1631,40 @@ def test_swiglu_ragged_padding_free():
         assert torch.equal(grads[1][2].view(torch.int16), du.view(torch.int16))
 
 
+def test_ragged_zero_outside():
+    """poly_ragged_zero_outside zeroes exactly the rows outside the clamped
+    range [max(seg[0], 0), min(seg[E], cap)) (empty when the offsets cross),
+    leaves the range and the guard bands untouched, for row widths that are
+    and are not multiples of 8 and for buffers on and off the 16-byte grid."""
+    G = 64
+    cases = [[0, 10, 30], [5, 10, 30], [0, 37], [10, 5], [-3, 50], [7], [0, 0, 36], [36, 37],
+             [50], [40, 45], [-9, -2]]
+    for cols in (8, 21, 2048, 3):
+        cap = 37
+        n = cap * cols
+        for seg in cases:
+            for off in (0, 1, 5):
+                buf = torch.full((2 * G + off + n,), 0x5A5A, dtype=torch.int16, device=DEV)
+                out = buf[G + off:G + off + n].view(cap, cols)
+                segd = torch.tensor(seg, dtype=torch.int32, device=DEV)
+                B.poly_ragged_zero_outside(out, segd)
+                lo = min(max(seg[0], 0), cap)
+                hi = max(min(seg[-1], cap), lo)
+                got = from_dev(out).reshape(cap, cols)
+                assert not got[:lo].any() and not got[hi:].any(), (cols, seg, off)
+                assert (got[lo:hi] == 0x5A5A).all(), (cols, seg, off)
+                b = from_dev(buf)
+                assert (b[:G + off] == 0x5A5A).all() and (b[G + off + n:] == 0x5A5A).all()
+    # full size: the ragged workload inside a capacity of 3,000 more rows
+    g, u, dy, seg = workloads.ragged_swiglu("bf16")
+    rows, cols = g.shape
+    cap = rows + 3000
+    y = torch.full((cap, cols), 0x5A5A, dtype=torch.int16, device=DEV)
+    B.poly_ragged_zero_outside(y, torch.from_numpy(seg).to(DEV))
+    assert bool((y[:rows] == 0x5A5A).all()) and not bool(y[rows:].any())
+    del y
+
+
 def test_calls_use_the_current_stream():
     """With no stream argument the binding launches on the current stream of
     the current device, inside and outside a torch.cuda.stream context."""
