@@ -16,9 +16,10 @@
  *   throws, aborts or prints.
  * - Ownership: the caller owns every buffer.  The library never allocates,
  *   frees or synchronises device memory.
- * - Device calls (poly_act_*, poly_swiglu_*, poly_softcap_*, poly_exp2,
- *   poly_rope_*, poly_ctrl_*, poly_diag_packed) take addresses the GPU can
- *   reach -- device memory, or, on systems with coherent host access such as
+ * - Device calls (poly_act_*, poly_swiglu_*, poly_ragged_zero_outside,
+ *   poly_softcap_*, poly_exp2, poly_rope_*, poly_ctrl_*, poly_diag_packed)
+ *   take addresses the GPU can reach -- device memory, or, on systems with
+ *   coherent host access such as
  *   GB300's NVLink-C2C, pinned host memory (the kernels then stream it over
  *   the link with no staging copy) -- and a CUDA stream (poly_stream_t is
  *   layout-compatible with cudaStream_t; NULL = the legacy default stream).
