@@ -252,7 +252,10 @@ def swiglu_ragged(g, u, seg_off, padding_free: bool = False):
     gradients) are zero: one extra launch zeroes them on the device, writing
     nothing when the segments cover every row.  padding_free=True (seg_off[0]
     = 0 and seg_off[E] = g.shape[0]) skips that launch; rows outside the range
-    would then be left uninitialised, so pass it only when that holds."""
+    would then be left uninitialised, so pass it only when that holds.  (A
+    padding-free call covers every row, so it computes exactly what swiglu
+    does; for gate and up halves of one fused [rows, 2H] buffer, which the
+    ragged calls do not take, use swiglu or swiglu_packed.)"""
     if _grad(g, u):
         return PolySwiGLURagged.apply(g, u, seg_off, padding_free)
     return _ragged_fwd(_dense(g), _dense(u), seg_off, padding_free)
