@@ -129,7 +129,8 @@ typedef struct poly_fit_opts {
 const char *poly_status_str(int status);
 /* The CUDA error code behind the last POLY_ECUDA on this thread (0 if none). */
 int poly_last_cuda_error(void);
-/* Library ABI version (bumped when a signature or struct changes). */
+/* Library ABI version (bumped when an entry point, signature or struct
+ * changes or is added). */
 int poly_abi_version(void);
 /* Form of (fn, dir) or POLY_EINVAL. */
 int poly_form_of(int fn, int dir);
