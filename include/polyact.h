@@ -17,7 +17,8 @@
  * - Ownership: the caller owns every buffer.  The library never allocates,
  *   frees or synchronises device memory.
  * - Device calls (poly_act_*, poly_swiglu_*, poly_ragged_zero_outside,
- *   poly_softcap_*, poly_exp2, poly_rope_*, poly_ctrl_*, poly_diag_packed)
+ *   poly_softcap_*, poly_exp2, poly_rope_*, poly_ctrl_*, poly_diag_packed,
+ *   poly_diag_stream_peak)
  *   take addresses the GPU can reach -- device memory, or, on systems with
  *   coherent host access such as
  *   GB300's NVLink-C2C, pinned host memory (the kernels then stream it over
@@ -162,8 +163,10 @@ int poly_fit(int fn, int dir, int dtype, int degree, const poly_fit_opts *opts,
 /* ---- program registry ---------------------------------------------------- */
 
 /* Install *p as the program used for (p->fn, p->dir, p->dtype) by later
- * calls.  Validates enums, form, degree, version and that c_0 matches the
- * form.  POLY_ENOPROG if inconsistent.  Thread-safe. */
+ * calls.  Validates enums, form, degree, version, that c_0 matches the form,
+ * and the clamp: lc_bits must decode to a finite positive value equal to lc,
+ * with Lc <= Li + 1 (li finite and positive).  POLY_ENOPROG if inconsistent.
+ * Thread-safe. */
 int poly_set_program(const poly_program *p);
 
 /* Copy the installed program for (fn, dir, dtype) into *out.  If none is
@@ -202,7 +205,8 @@ int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx,
                  int64_t n, poly_stream_t stream);
 
 /* ---- SwiGLU gate (§3.4, §5.2.4 eq. 15) ------------------------------------
- * Two rules, chosen process-wide by poly_set_swiglu_variant:
+ * Two rules, chosen per call by the _v entry points (variant argument), or
+ * process-wide for the plain entry points by poly_set_swiglu_variant:
  * POLY_SWIGLU_DIRECT (default): s = installed SiLU forward program (HX form),
  *   s' = installed SiLU backward program (CO form, the centred SiLU
  *   derivative of eq. 9).
@@ -217,8 +221,10 @@ int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx,
  * Dense: row-major [rows, cols] with leading dimensions (elements, >= cols).
  */
 enum { POLY_SWIGLU_DIRECT = 0, POLY_SWIGLU_SIGMOID = 1 };
-/* Select the SwiGLU rule for later calls (thread-safe, process-wide).
- * POLY_EINVAL for an unknown variant. */
+/* Select the SwiGLU rule used by later calls of the plain (non-_v) SwiGLU
+ * entry points (thread-safe, process-wide; callers on different streams that
+ * want different rules use the _v entry points instead).  POLY_EINVAL for an
+ * unknown variant. */
 int poly_set_swiglu_variant(int variant);
 /* The current SwiGLU rule. */
 int poly_get_swiglu_variant(void);
@@ -230,6 +236,16 @@ int poly_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy,
                     void *dg, void *du, int64_t rows, int64_t cols, int64_t ldg,
                     int64_t ldu, int64_t lddy, int64_t lddg, int64_t lddu,
                     poly_stream_t stream);
+/* The same calls with the rule as an argument (POLY_SWIGLU_DIRECT or
+ * POLY_SWIGLU_SIGMOID; anything else -> POLY_EINVAL).  Nothing process-wide
+ * is read, so concurrent callers may use different rules. */
+int poly_swiglu_fwd_v(int variant, int dtype, const void *g, const void *u, void *y,
+                      int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
+                      poly_stream_t stream);
+int poly_swiglu_bwd_v(int variant, int dtype, const void *g, const void *u, const void *dy,
+                      void *dg, void *du, int64_t rows, int64_t cols, int64_t ldg,
+                      int64_t ldu, int64_t lddy, int64_t lddg, int64_t lddu,
+                      poly_stream_t stream);
 
 /* Ragged routed-expert SwiGLU: the rows of all experts are packed without
  * padding into [cap_rows, cols] tensors (leading dimension cols); expert e
@@ -248,6 +264,14 @@ int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u,
                            const int32_t *seg_off, int num_segments,
                            int64_t cap_rows, int64_t cols, int32_t *status,
                            poly_stream_t stream);
+/* The ragged calls with the rule as an argument, as poly_swiglu_fwd_v. */
+int poly_swiglu_fwd_ragged_v(int variant, int dtype, const void *g, const void *u, void *y,
+                             const int32_t *seg_off, int num_segments, int64_t cap_rows,
+                             int64_t cols, int32_t *status, poly_stream_t stream);
+int poly_swiglu_bwd_ragged_v(int variant, int dtype, const void *g, const void *u,
+                             const void *dy, void *dg, void *du, const int32_t *seg_off,
+                             int num_segments, int64_t cap_rows, int64_t cols,
+                             int32_t *status, poly_stream_t stream);
 
 /* Zero the rows of a [cap_rows, cols] buffer of 16-bit elements (any format:
  * +0 is all-zero bits) that the ragged calls above leave untouched: rows
@@ -341,14 +365,33 @@ int poly_rope_turn_increments(int head_dim, double base, uint32_t *out);
 int poly_rope_programs(uint16_t *sin_coef, uint16_t *cos_coef);
 
 /* ---- MUFU-native controls (same signatures and memory schedule) ----------
- * FP32 math on the special-function unit: sigmoid = rcp.approx(1 +
- * ex2.approx(-x log2 e)); tanh = tanh.approx; SiLU = the overflow-safe form
- * e = 2^(-|x| log2 e), y = (x >= 0 ? x : x e) * rcp.approx(1 + e); exact GELU
- * = x/2 (1 + erff(x / sqrt 2)) (no special-function erf exists; erff is a
- * CUDA-core polynomial).  Backward: sigma (1 - sigma), 1 - tanh^2,
- * sigma (1 + x (1 - sigma)), Phi + x phi, all recomputed from x.  Results
- * are rounded once to the target format; they are approximations of the
- * true function, not of the polynomial programs. */
+ * The comparators of §4.2 / Table 3: the same functions on the
+ * special-function unit instead of polynomial programs.  Two variants:
+ *
+ * POLY_CTRL_FP32 (the plain poly_ctrl_* calls): each element widened to
+ * FP32: sigmoid = rcp.approx(1 + ex2.approx(-x log2 e)); tanh = tanh.approx;
+ * SiLU = the overflow-safe form e = 2^(-|x| log2 e),
+ * y = (x >= 0 ? x : x e) * rcp.approx(1 + e); exact GELU = x/2 (1 + erff(x /
+ * sqrt 2)) (no special-function erf exists; erff is a CUDA-core polynomial).
+ * Backward: sigma (1 - sigma), 1 - tanh^2, sigma (1 + x (1 - sigma)),
+ * Phi + x phi, all recomputed from x.  One rounding to the target format.
+ *
+ * POLY_CTRL_PACKED (the _v calls): packed two-lane arithmetic in the target
+ * format with one tanh.approx.{f16x2,bf16x2} per pair (GB300's
+ * special-function unit is twice GB200's, Approximating Softmax in
+ * Pretrained LLMs, Appendix B.5): tanh = tanh.approx(x); sigmoid =
+ * fma(t, 1/2, 1/2), t = tanh.approx(x * 1/2); SiLU = fma(h, t, h) with
+ * h = x * 1/2, t = tanh.approx(h); GELU in the tanh form h (1 + tanh(z)),
+ * z = x (k + k c x^2), k = sqrt(2/pi), c = 0.044715 (within 4.8e-4 of exact
+ * GELU).  Backward: sigma' = fma(-p, p, p), tanh' = fma(-t, t, 1),
+ * SiLU' = fma(x, fma(-p, p, p), p), GELU' = fma(1 - t^2, h z', p) with x
+ * clamped to [-16, 16] and z' = k + 3 k c x^2; dx = dy * derivative.  SwiGLU:
+ * y = SiLU(g) * u; dg = (dy * u) * SiLU'(g), du = dy * SiLU(g).  Every
+ * operation rounds once to the target format.  Infinite inputs are outside
+ * both controls' domain (the backward controls give NaN at +-inf).
+ *
+ * Results approximate the true function, not the polynomial programs. */
+enum { POLY_CTRL_FP32 = 0, POLY_CTRL_PACKED = 1 };
 int poly_ctrl_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n,
                       poly_stream_t stream);
 int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy,
@@ -356,13 +399,25 @@ int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy,
 int poly_ctrl_swiglu_fwd(int dtype, const void *g, const void *u, void *y,
                          int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
                          int64_t ldy, poly_stream_t stream);
-/* 2^x by ex2.approx.ftz.f32 on the special-function unit, same memory
- * schedule and validation as poly_exp2. */
-int poly_ctrl_exp2(const float *x, float *y, int64_t n, poly_stream_t stream);
 int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u,
                          const void *dy, void *dg, void *du, int64_t rows,
                          int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,
                          int64_t lddg, int64_t lddu, poly_stream_t stream);
+/* The controls with the variant as an argument (POLY_EINVAL for another). */
+int poly_ctrl_act_fwd_v(int variant, int fn, int dtype, const void *x, void *y, int64_t n,
+                        poly_stream_t stream);
+int poly_ctrl_act_bwd_v(int variant, int fn, int dtype, const void *x, const void *dy,
+                        void *dx, int64_t n, poly_stream_t stream);
+int poly_ctrl_swiglu_fwd_v(int variant, int dtype, const void *g, const void *u, void *y,
+                           int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
+                           poly_stream_t stream);
+int poly_ctrl_swiglu_bwd_v(int variant, int dtype, const void *g, const void *u,
+                           const void *dy, void *dg, void *du, int64_t rows, int64_t cols,
+                           int64_t ldg, int64_t ldu, int64_t lddy, int64_t lddg,
+                           int64_t lddu, poly_stream_t stream);
+/* 2^x by ex2.approx.ftz.f32 on the special-function unit, same memory
+ * schedule and validation as poly_exp2. */
+int poly_ctrl_exp2(const float *x, float *y, int64_t n, poly_stream_t stream);
 
 /* ---- arithmetic diagnostic ------------------------------------------------
  * Runs one raw packed instruction over n element triples so that the
@@ -380,6 +435,21 @@ enum { POLY_DIAG_FMA = 0, POLY_DIAG_MUL = 1, POLY_DIAG_MIN_NAN = 2, POLY_DIAG_MA
        POLY_DIAG_GT = 4 };
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c,
                      void *out, int64_t n, poly_stream_t stream);
+
+/* ---- streaming-bandwidth probe (a measurement tool; no counterpart in the
+ * paper, which states its L2 and HBM regimes (§4.2) but no peaks) ---------
+ * reps passes of out[i] = a[i] (nin = 1) or a[i] ^ b[i] (nin = 2, bitwise)
+ * over n 16-bit elements, with the loads, stores and residency of the
+ * streaming kernels (eight 256-thread blocks per SM); pass r assigns each
+ * 16-byte chunk to another thread than pass r - 1 did.  The rate
+ * reps * n * 2 * (nin + 1) bytes / time is the L2 streaming bandwidth of
+ * that access pattern when a, b and out fit in L2 and the launch spans many
+ * passes, and its HBM rate when they do not.  a, b, out: device memory,
+ * 16-byte aligned; out overlaps neither input; n a multiple of 8 below
+ * 2^34; 1 <= reps <= 2^20; b unused (may be NULL) for nin = 1.  POLY_EINVAL
+ * otherwise; n == 0 is a no-op. */
+int poly_diag_stream_peak(int nin, const void *a, const void *b, void *out, int64_t n,
+                          int reps, poly_stream_t stream);
 
 /* ---- failure injection (host only; no counterpart in the paper) ----------
  * poly_debug_fail_launches: the next `count` kernel launches, from any entry

@@ -24,7 +24,7 @@ FN = {"sigmoid": POLY_SIGMOID, "tanh": POLY_TANH, "silu": POLY_SILU, "gelu": POL
 FN_NAMES = {v: k for k, v in FN.items()}
 
 # version of include/polyact.h this binding marshals for (poly_abi_version)
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 # every function declared in include/polyact.h
 EXPORTS = [
@@ -39,10 +39,14 @@ EXPORTS = [
     "poly_derive_program", "poly_softcap_fwd", "poly_softcap_bwd", "poly_exp2",
     "poly_ctrl_exp2", "poly_rope_fwd", "poly_rope_bwd", "poly_rope_turn_increments",
     "poly_rope_programs",
+    "poly_swiglu_fwd_v", "poly_swiglu_bwd_v", "poly_swiglu_fwd_ragged_v",
+    "poly_swiglu_bwd_ragged_v", "poly_ctrl_act_fwd_v", "poly_ctrl_act_bwd_v",
+    "poly_ctrl_swiglu_fwd_v", "poly_ctrl_swiglu_bwd_v", "poly_diag_stream_peak",
 ]
 POLY_ROPE_POLY, POLY_ROPE_MUFU, POLY_ROPE_TABLE = 0, 1, 2
 POLY_EXP2_D1, POLY_EXP2_PWL2, POLY_EXP2_D2, POLY_EXP2_D3 = 0, 1, 2, 3
 POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID = 0, 1
+POLY_CTRL_FP32, POLY_CTRL_PACKED = 0, 1
 POLY_DIAG_FMA, POLY_DIAG_MUL, POLY_DIAG_MIN_NAN, POLY_DIAG_MAX, POLY_DIAG_GT = 0, 1, 2, 3, 4
 
 
@@ -130,6 +134,17 @@ def lib():
     L.poly_swiglu_bwd_ragged.argtypes = [_i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
     L.poly_ragged_zero_outside.argtypes = [_p, _p, _i, _i64, _i64, _p]
     L.poly_diag_packed.argtypes = [_i, _i, _p, _p, _p, _p, _i64, _p]
+    L.poly_diag_stream_peak.argtypes = [_i, _p, _p, _p, _i64, _i, _p]
+    L.poly_ctrl_act_fwd_v.argtypes = [_i, _i, _i, _p, _p, _i64, _p]
+    L.poly_ctrl_act_bwd_v.argtypes = [_i, _i, _i, _p, _p, _p, _i64, _p]
+    for name in ("poly_swiglu_fwd_v", "poly_ctrl_swiglu_fwd_v"):
+        getattr(L, name).argtypes = [_i, _i, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p]
+    for name in ("poly_swiglu_bwd_v", "poly_ctrl_swiglu_bwd_v"):
+        getattr(L, name).argtypes = [_i, _i, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64,
+                                     _i64, _i64, _p]
+    L.poly_swiglu_fwd_ragged_v.argtypes = [_i, _i, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
+    L.poly_swiglu_bwd_ragged_v.argtypes = [_i, _i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p,
+                                           _p]
     L.poly_debug_fail_launches.argtypes = [_i, _i]
     for name in EXPORTS:
         if name not in ("poly_status_str",):
@@ -327,6 +342,22 @@ def poly_ctrl_act_bwd(fn, dtype, x, dy, dx, n=None, stream=None):
            "poly_ctrl_act_bwd")
 
 
+def poly_ctrl_act_fwd_v(variant, fn, dtype, x, y, n=None, stream=None):
+    n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (y, "y")):
+        _room(t, 2 * n, "poly_ctrl_act_fwd_v", nm, dtype=dtype)
+    _check(lib().poly_ctrl_act_fwd_v(variant, fn, dtype, _ptr(x), _ptr(y), n, _stream(stream)),
+           "poly_ctrl_act_fwd_v")
+
+
+def poly_ctrl_act_bwd_v(variant, fn, dtype, x, dy, dx, n=None, stream=None):
+    n = x.numel() if n is None else n
+    for t, nm in ((x, "x"), (dy, "dy"), (dx, "dx")):
+        _room(t, 2 * n, "poly_ctrl_act_bwd_v", nm, dtype=dtype)
+    _check(lib().poly_ctrl_act_bwd_v(variant, fn, dtype, _ptr(x), _ptr(dy), _ptr(dx), n,
+                                     _stream(stream)), "poly_ctrl_act_bwd_v")
+
+
 def _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, name):
     cols = g.shape[-1] if cols is None else cols
     rows = _rows(g, cols) if rows is None else rows
@@ -351,6 +382,18 @@ def poly_ctrl_swiglu_fwd(dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=Non
                 "poly_ctrl_swiglu_fwd")
 
 
+def poly_swiglu_fwd_v(variant, dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=None,
+                      ldy=None, stream=None):
+    cfn = lambda *a: lib().poly_swiglu_fwd_v(variant, *a)
+    _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, "poly_swiglu_fwd_v")
+
+
+def poly_ctrl_swiglu_fwd_v(variant, dtype, g, u, y, rows=None, cols=None, ldg=None, ldu=None,
+                           ldy=None, stream=None):
+    cfn = lambda *a: lib().poly_ctrl_swiglu_fwd_v(variant, *a)
+    _swiglu_fwd(cfn, dtype, g, u, y, rows, cols, ldg, ldu, ldy, stream, "poly_ctrl_swiglu_fwd_v")
+
+
 def _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, lds, stream, name):
     cols = g.shape[-1] if cols is None else cols
     rows = _rows(g, cols) if rows is None else rows
@@ -372,6 +415,20 @@ def poly_ctrl_swiglu_bwd(dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None
                          lddy=None, lddg=None, lddu=None, stream=None):
     _swiglu_bwd(lib().poly_ctrl_swiglu_bwd, dtype, g, u, dy, dg, du, rows, cols,
                 (ldg, ldu, lddy, lddg, lddu), stream, "poly_ctrl_swiglu_bwd")
+
+
+def poly_swiglu_bwd_v(variant, dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None,
+                      ldu=None, lddy=None, lddg=None, lddu=None, stream=None):
+    cfn = lambda *a: lib().poly_swiglu_bwd_v(variant, *a)
+    _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, (ldg, ldu, lddy, lddg, lddu), stream,
+                "poly_swiglu_bwd_v")
+
+
+def poly_ctrl_swiglu_bwd_v(variant, dtype, g, u, dy, dg, du, rows=None, cols=None, ldg=None,
+                           ldu=None, lddy=None, lddg=None, lddu=None, stream=None):
+    cfn = lambda *a: lib().poly_ctrl_swiglu_bwd_v(variant, *a)
+    _swiglu_bwd(cfn, dtype, g, u, dy, dg, du, rows, cols, (ldg, ldu, lddy, lddg, lddu), stream,
+                "poly_ctrl_swiglu_bwd_v")
 
 
 def _ragged_room(where, dtype, ts, names, seg_off, num_segments, cap_rows, cols, status):
@@ -404,6 +461,42 @@ def poly_swiglu_bwd_ragged(dtype, g, u, dy, dg, du, seg_off, num_segments=None, 
                                         _ptr(seg_off), num_segments, cap_rows, cols,
                                         _ptr(status), _stream(stream)),
            "poly_swiglu_bwd_ragged")
+
+
+def poly_swiglu_fwd_ragged_v(variant, dtype, g, u, y, seg_off, num_segments=None,
+                             cap_rows=None, cols=None, status=None, stream=None):
+    num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
+    cols = g.shape[-1] if cols is None else cols
+    cap_rows = _rows(g, cols) if cap_rows is None else cap_rows
+    _ragged_room("poly_swiglu_fwd_ragged_v", dtype, (g, u, y), ("g", "u", "y"), seg_off,
+                 num_segments, cap_rows, cols, status)
+    _check(lib().poly_swiglu_fwd_ragged_v(variant, dtype, _ptr(g), _ptr(u), _ptr(y),
+                                          _ptr(seg_off), num_segments, cap_rows, cols,
+                                          _ptr(status), _stream(stream)),
+           "poly_swiglu_fwd_ragged_v")
+
+
+def poly_swiglu_bwd_ragged_v(variant, dtype, g, u, dy, dg, du, seg_off, num_segments=None,
+                             cap_rows=None, cols=None, status=None, stream=None):
+    num_segments = seg_off.numel() - 1 if num_segments is None else num_segments
+    cols = g.shape[-1] if cols is None else cols
+    cap_rows = _rows(g, cols) if cap_rows is None else cap_rows
+    _ragged_room("poly_swiglu_bwd_ragged_v", dtype, (g, u, dy, dg, du),
+                 ("g", "u", "dy", "dg", "du"), seg_off, num_segments, cap_rows, cols, status)
+    _check(lib().poly_swiglu_bwd_ragged_v(variant, dtype, _ptr(g), _ptr(u), _ptr(dy), _ptr(dg),
+                                          _ptr(du), _ptr(seg_off), num_segments, cap_rows, cols,
+                                          _ptr(status), _stream(stream)),
+           "poly_swiglu_bwd_ragged_v")
+
+
+def poly_diag_stream_peak(nin, a, b, out, n=None, reps=1, stream=None):
+    """reps streaming passes out = a (nin 1) or a ^ b (nin 2) over n 16-bit
+    elements (the bandwidth probe)."""
+    n = a.numel() if n is None else n
+    for t, nm in ((a, "a"), (b, "b"), (out, "out")):
+        _room(t, 2 * n, "poly_diag_stream_peak", nm)
+    _check(lib().poly_diag_stream_peak(nin, _ptr(a), _ptr(b), _ptr(out), n, reps,
+                                       _stream(stream)), "poly_diag_stream_peak")
 
 
 def poly_ragged_zero_outside(out, seg_off, num_segments=None, cap_rows=None, cols=None,

@@ -28,6 +28,8 @@ std::atomic<int> g_swiglu_variant{POLY_SWIGLU_DIRECT};
 bool valid_fn(int fn) { return fn >= POLY_SIGMOID && fn <= POLY_GELU; }
 bool valid_dir(int d) { return d == POLY_FWD || d == POLY_BWD; }
 bool valid_dtype(int dt) { return dt == POLY_F16 || dt == POLY_BF16; }
+bool valid_ctrl(int v) { return v == POLY_CTRL_FP32 || v == POLY_CTRL_PACKED; }
+bool valid_swiglu_variant(int v) { return v == POLY_SWIGLU_DIRECT || v == POLY_SWIGLU_SIGMOID; }
 
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return POLY_OK;
@@ -71,6 +73,11 @@ int check_program(const poly_program &p) {
   if (p.version != POLY_PROGRAM_VERSION) return POLY_ENOPROG;
   const bool even = p.form == POLY_FORM_E;
   if (!even && (p.coef[0] & 0x7FFF) != 0) return POLY_ENOPROG;   // c_0 = f(0) = 0
+  // the clamp: a finite positive target-format value, lc its exact value, and
+  // no further than one unit past the fit interval (Lc <= Li + 1, §3.2 step 6)
+  const double lc = to_double(p.lc_bits, p.dtype);
+  if (!std::isfinite(lc) || !(lc > 0.0) || lc != p.lc) return POLY_ENOPROG;
+  if (!std::isfinite(p.li) || !(p.li > 0.0) || !(lc <= p.li + 1.0)) return POLY_ENOPROG;
   return POLY_OK;
 }
 
@@ -301,7 +308,7 @@ const char *poly_status_str(int status) {
 
 int poly_last_cuda_error(void) { return t_last_cuda_error; }
 
-int poly_abi_version(void) { return 3; }
+int poly_abi_version(void) { return 4; }
 
 int poly_debug_fail_launches(int cuda_error, int count) {
   if (cuda_error <= 0 || count < 0) return POLY_EINVAL;
@@ -382,7 +389,7 @@ int poly_get_program(int fn, int dir, int dtype, poly_program *out) {
 }
 
 int poly_set_swiglu_variant(int variant) {
-  if (variant != POLY_SWIGLU_DIRECT && variant != POLY_SWIGLU_SIGMOID) return POLY_EINVAL;
+  if (!valid_swiglu_variant(variant)) return POLY_EINVAL;
   g_swiglu_variant.store(variant);
   return POLY_OK;
 }
@@ -395,9 +402,11 @@ int poly_reset_programs(void) {
   return POLY_OK;
 }
 
-static int act_call(bool ctrl, int kind, int fn, int dtype, const void *x, const void *dy,
+// ctrl < 0: the polynomial program; otherwise the MUFU control of that variant.
+static int act_call(int ctrl, int kind, int fn, int dtype, const void *x, const void *dy,
                     void *y, int64_t n, poly_stream_t stream) {
   if (!valid_fn(fn) || !valid_dtype(dtype) || n < 0) return POLY_EINVAL;
+  if (ctrl >= 0 && !valid_ctrl(ctrl)) return POLY_EINVAL;
   if (n == 0) return POLY_OK;
   const bool bwd = kind == kActBwd;
   if (x == nullptr || y == nullptr || (bwd && dy == nullptr)) return POLY_EINVAL;
@@ -410,7 +419,8 @@ static int act_call(bool ctrl, int kind, int fn, int dtype, const void *x, const
   Streams s{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dy), nullptr,
             static_cast<uint16_t *>(y), nullptr};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (ctrl) return launch_status([&] { return launch_ctrl(kind, dtype, fn, s, l, cs); });
+  if (ctrl >= 0)
+    return launch_status([&] { return launch_ctrl(kind, dtype, fn, s, l, cs, ctrl); });
   poly_program p;
   int st = registry_get(fn, bwd ? POLY_BWD : POLY_FWD, dtype, &p);
   if (st != POLY_OK) return st;
@@ -420,28 +430,42 @@ static int act_call(bool ctrl, int kind, int fn, int dtype, const void *x, const
 }
 
 int poly_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n, poly_stream_t stream) {
-  return act_call(false, kActFwd, fn, dtype, x, nullptr, y, n, stream);
+  return act_call(-1, kActFwd, fn, dtype, x, nullptr, y, n, stream);
 }
 
 int poly_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx, int64_t n,
                  poly_stream_t stream) {
-  return act_call(false, kActBwd, fn, dtype, x, dy, dx, n, stream);
+  return act_call(-1, kActBwd, fn, dtype, x, dy, dx, n, stream);
 }
 
 int poly_ctrl_act_fwd(int fn, int dtype, const void *x, void *y, int64_t n,
                       poly_stream_t stream) {
-  return act_call(true, kActFwd, fn, dtype, x, nullptr, y, n, stream);
+  return act_call(POLY_CTRL_FP32, kActFwd, fn, dtype, x, nullptr, y, n, stream);
 }
 
 int poly_ctrl_act_bwd(int fn, int dtype, const void *x, const void *dy, void *dx, int64_t n,
                       poly_stream_t stream) {
-  return act_call(true, kActBwd, fn, dtype, x, dy, dx, n, stream);
+  return act_call(POLY_CTRL_FP32, kActBwd, fn, dtype, x, dy, dx, n, stream);
 }
 
-static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void *u,
+int poly_ctrl_act_fwd_v(int variant, int fn, int dtype, const void *x, void *y, int64_t n,
+                        poly_stream_t stream) {
+  if (!valid_ctrl(variant)) return POLY_EINVAL;
+  return act_call(variant, kActFwd, fn, dtype, x, nullptr, y, n, stream);
+}
+
+int poly_ctrl_act_bwd_v(int variant, int fn, int dtype, const void *x, const void *dy, void *dx,
+                        int64_t n, poly_stream_t stream) {
+  if (!valid_ctrl(variant)) return POLY_EINVAL;
+  return act_call(variant, kActBwd, fn, dtype, x, dy, dx, n, stream);
+}
+
+// ctrl < 0: the polynomial rule `variant`; otherwise the MUFU control `ctrl`.
+static int swiglu_call(int ctrl, int variant, bool bwd, int dtype, const void *g, const void *u,
                        const void *dy, void *o0, void *o1, int64_t rows, int64_t cols,
                        const int64_t *ld_in, const int64_t *ld_out, poly_stream_t stream) {
   if (!valid_dtype(dtype)) return POLY_EINVAL;
+  if (ctrl >= 0 ? !valid_ctrl(ctrl) : !valid_swiglu_variant(variant)) return POLY_EINVAL;
   const void *in[3] = {g, u, dy};
   void *out[2] = {o0, o1};
   Layout l;
@@ -453,8 +477,8 @@ static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void
             static_cast<uint16_t *>(o1)};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int kind = bwd ? kSwigluBwd : kSwigluFwd;
-  if (ctrl) return launch_status([&] { return launch_ctrl(kind, dtype, POLY_SILU, s, l, cs); });
-  const int variant = g_swiglu_variant.load();
+  if (ctrl >= 0)
+    return launch_status([&] { return launch_ctrl(kind, dtype, POLY_SILU, s, l, cs, ctrl); });
   poly_program ps, pd;
   st = swiglu_programs(variant, dtype, bwd, &ps, &pd);
   if (st != POLY_OK) return st;
@@ -464,37 +488,71 @@ static int swiglu_call(bool ctrl, bool bwd, int dtype, const void *g, const void
   });
 }
 
+int poly_swiglu_fwd_v(int variant, int dtype, const void *g, const void *u, void *y,
+                      int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
+                      poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
+  return swiglu_call(-1, variant, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo,
+                     stream);
+}
+
+int poly_swiglu_bwd_v(int variant, int dtype, const void *g, const void *u, const void *dy,
+                      void *dg, void *du, int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
+                      int64_t lddy, int64_t lddg, int64_t lddu, poly_stream_t stream) {
+  const int64_t li[3] = {ldg, ldu, lddy}, lo[2] = {lddg, lddu};
+  return swiglu_call(-1, variant, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
+}
+
 int poly_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
                     int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy, poly_stream_t stream) {
-  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
-  return swiglu_call(false, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo, stream);
+  return poly_swiglu_fwd_v(g_swiglu_variant.load(), dtype, g, u, y, rows, cols, ldg, ldu, ldy,
+                           stream);
 }
 
 int poly_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy, void *dg, void *du,
                     int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t lddy,
                     int64_t lddg, int64_t lddu, poly_stream_t stream) {
+  return poly_swiglu_bwd_v(g_swiglu_variant.load(), dtype, g, u, dy, dg, du, rows, cols, ldg,
+                           ldu, lddy, lddg, lddu, stream);
+}
+
+int poly_ctrl_swiglu_fwd_v(int variant, int dtype, const void *g, const void *u, void *y,
+                           int64_t rows, int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
+                           poly_stream_t stream) {
+  if (!valid_ctrl(variant)) return POLY_EINVAL;
+  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
+  return swiglu_call(variant, 0, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo,
+                     stream);
+}
+
+int poly_ctrl_swiglu_bwd_v(int variant, int dtype, const void *g, const void *u, const void *dy,
+                           void *dg, void *du, int64_t rows, int64_t cols, int64_t ldg,
+                           int64_t ldu, int64_t lddy, int64_t lddg, int64_t lddu,
+                           poly_stream_t stream) {
+  if (!valid_ctrl(variant)) return POLY_EINVAL;
   const int64_t li[3] = {ldg, ldu, lddy}, lo[2] = {lddg, lddu};
-  return swiglu_call(false, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
+  return swiglu_call(variant, 0, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
 }
 
 int poly_ctrl_swiglu_fwd(int dtype, const void *g, const void *u, void *y, int64_t rows,
                          int64_t cols, int64_t ldg, int64_t ldu, int64_t ldy,
                          poly_stream_t stream) {
-  const int64_t li[3] = {ldg, ldu, cols}, lo[2] = {ldy, cols};
-  return swiglu_call(true, false, dtype, g, u, nullptr, y, nullptr, rows, cols, li, lo, stream);
+  return poly_ctrl_swiglu_fwd_v(POLY_CTRL_FP32, dtype, g, u, y, rows, cols, ldg, ldu, ldy,
+                                stream);
 }
 
 int poly_ctrl_swiglu_bwd(int dtype, const void *g, const void *u, const void *dy, void *dg,
                          void *du, int64_t rows, int64_t cols, int64_t ldg, int64_t ldu,
                          int64_t lddy, int64_t lddg, int64_t lddu, poly_stream_t stream) {
-  const int64_t li[3] = {ldg, ldu, lddy}, lo[2] = {lddg, lddu};
-  return swiglu_call(true, true, dtype, g, u, dy, dg, du, rows, cols, li, lo, stream);
+  return poly_ctrl_swiglu_bwd_v(POLY_CTRL_FP32, dtype, g, u, dy, dg, du, rows, cols, ldg, ldu,
+                                lddy, lddg, lddu, stream);
 }
 
-static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const void *dy,
-                       void *o0, void *o1, const int32_t *seg_off, int num_segments,
-                       int64_t cap_rows, int64_t cols, int32_t *status, poly_stream_t stream) {
-  if (!valid_dtype(dtype)) return POLY_EINVAL;
+static int ragged_call(int variant, bool bwd, int dtype, const void *g, const void *u,
+                       const void *dy, void *o0, void *o1, const int32_t *seg_off,
+                       int num_segments, int64_t cap_rows, int64_t cols, int32_t *status,
+                       poly_stream_t stream) {
+  if (!valid_dtype(dtype) || !valid_swiglu_variant(variant)) return POLY_EINVAL;
   const void *in[3] = {g, u, dy};
   void *out[2] = {o0, o1};
   Layout l;
@@ -502,7 +560,6 @@ static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const 
                          cols, status, &l);
   if (st == 1) return POLY_OK;
   if (st != POLY_OK) return st;
-  const int variant = g_swiglu_variant.load();
   poly_program ps, pd;
   st = swiglu_programs(variant, dtype, bwd, &ps, &pd);
   if (st != POLY_OK) return st;
@@ -516,18 +573,33 @@ static int ragged_call(bool bwd, int dtype, const void *g, const void *u, const 
   });
 }
 
+int poly_swiglu_fwd_ragged_v(int variant, int dtype, const void *g, const void *u, void *y,
+                             const int32_t *seg_off, int num_segments, int64_t cap_rows,
+                             int64_t cols, int32_t *status, poly_stream_t stream) {
+  return ragged_call(variant, false, dtype, g, u, nullptr, y, nullptr, seg_off, num_segments,
+                     cap_rows, cols, status, stream);
+}
+
+int poly_swiglu_bwd_ragged_v(int variant, int dtype, const void *g, const void *u,
+                             const void *dy, void *dg, void *du, const int32_t *seg_off,
+                             int num_segments, int64_t cap_rows, int64_t cols, int32_t *status,
+                             poly_stream_t stream) {
+  return ragged_call(variant, true, dtype, g, u, dy, dg, du, seg_off, num_segments, cap_rows,
+                     cols, status, stream);
+}
+
 int poly_swiglu_fwd_ragged(int dtype, const void *g, const void *u, void *y,
                            const int32_t *seg_off, int num_segments, int64_t cap_rows,
                            int64_t cols, int32_t *status, poly_stream_t stream) {
-  return ragged_call(false, dtype, g, u, nullptr, y, nullptr, seg_off, num_segments, cap_rows,
-                     cols, status, stream);
+  return poly_swiglu_fwd_ragged_v(g_swiglu_variant.load(), dtype, g, u, y, seg_off,
+                                  num_segments, cap_rows, cols, status, stream);
 }
 
 int poly_swiglu_bwd_ragged(int dtype, const void *g, const void *u, const void *dy, void *dg,
                            void *du, const int32_t *seg_off, int num_segments, int64_t cap_rows,
                            int64_t cols, int32_t *status, poly_stream_t stream) {
-  return ragged_call(true, dtype, g, u, dy, dg, du, seg_off, num_segments, cap_rows, cols,
-                     status, stream);
+  return poly_swiglu_bwd_ragged_v(g_swiglu_variant.load(), dtype, g, u, dy, dg, du, seg_off,
+                                  num_segments, cap_rows, cols, status, stream);
 }
 
 int poly_ragged_zero_outside(void *out, const int32_t *seg_off, int num_segments,
@@ -729,6 +801,27 @@ int poly_rope_bwd(int variant, const void *dq, const void *dk, void *dq_out, voi
                   int64_t pos_offset, poly_stream_t stream) {
   return rope_call(1, variant, dq, dk, dq_out, dk_out, delta, cos_tab, sin_tab, batch, seq, hq,
                    hkv, head_dim, pos_offset, stream);
+}
+
+int poly_diag_stream_peak(int nin, const void *a, const void *b, void *out, int64_t n,
+                          int reps, poly_stream_t stream) {
+  if ((nin != 1 && nin != 2) || n < 0 || (n & 7) || reps < 1 || reps > (1 << 20))
+    return POLY_EINVAL;
+  if ((n >> 3) >= (int64_t(1) << 31)) return POLY_EINVAL;
+  if (n == 0) return POLY_OK;
+  if (nin == 1) b = a;
+  if (a == nullptr || b == nullptr || out == nullptr) return POLY_EINVAL;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(out)) return POLY_EINVAL;
+  const Span si[2] = {span_flat(a, n), span_flat(b, n)};
+  const Span so = span_flat(out, n);
+  if (!si[0].ok || !si[1].ok || !so.ok) return POLY_EINVAL;
+  for (int i = 0; i < 2; ++i)
+    if (overlaps(so, si[i])) return POLY_EINVAL;
+  return launch_status([&] {
+    return launch_stream_peak(nin, static_cast<const uint16_t *>(a),
+                              static_cast<const uint16_t *>(b), static_cast<uint16_t *>(out),
+                              n >> 3, reps, reinterpret_cast<cudaStream_t>(stream));
+  });
 }
 
 int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void *c, void *out,

@@ -68,7 +68,70 @@ static cudaError_t diag_dt(int op, const Streams &s, const Layout &l, cudaStream
   return cudaErrorInvalidValue;
 }
 
+// Streaming-bandwidth probe (a measurement tool beside the kernels it
+// measures): `reps` passes over nvec 16-byte chunks, each writing out = a or
+// a ^ b with the kernels' own loads and stores, from a grid of eight 256-thread
+// blocks per SM (full residency).  Pass r shifts the chunk a thread takes by
+// r * rot (mod nvec), so every pass moves each chunk through another SM.
+// With a working set that fits in L2 and enough passes to hide one launch's
+// ramp and drain, the rate is the L2 streaming bandwidth of the kernels'
+// access pattern; above L2 size it is the HBM rate of that pattern.
+template <int NIN>
+__global__ void __launch_bounds__(kThreads)
+    stream_peak_kernel(const uint16_t *a, const uint16_t *b, uint16_t *out, uint32_t nvec,
+                       uint32_t rot, int reps) {
+  pdl_enter();
+  const uint32_t stride = gridDim.x * (uint32_t)kThreads;
+  const uint32_t first = blockIdx.x * (uint32_t)kThreads + threadIdx.x;
+  uint32_t shift = 0;
+#pragma unroll 1
+  for (int r = 0; r < reps; ++r) {
+#pragma unroll 1
+    for (uint32_t c = first; c < nvec; c += 2 * stride) {
+      uint32_t k[2];
+      uint4 v[2][NIN];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t j = c + u * stride;
+        k[u] = 0xFFFFFFFFu;
+        if (j < nvec) {
+          k[u] = j + shift < nvec ? j + shift : j + shift - nvec;
+          v[u][0] = ld_stream(a + (size_t)k[u] * 8);
+          if constexpr (NIN == 2) v[u][1] = ld_stream(b + (size_t)k[u] * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (k[u] != 0xFFFFFFFFu) {
+          uint4 o = v[u][0];
+          if constexpr (NIN == 2) {
+            o.x ^= v[u][1].x;
+            o.y ^= v[u][1].y;
+            o.z ^= v[u][1].z;
+            o.w ^= v[u][1].w;
+          }
+          st_stream(out + (size_t)k[u] * 8, o);
+        }
+      }
+    }
+    shift += rot;
+    if (shift >= nvec) shift -= nvec;
+  }
+}
+
 }  // namespace dev
+
+cudaError_t launch_stream_peak(int nin, const uint16_t *a, const uint16_t *b, uint16_t *out,
+                               int64_t nvec, int reps, cudaStream_t stream) {
+  const uint32_t n = (uint32_t)nvec;
+  const uint32_t rot = (n / 7u) | 1u;   // any shift co-prime-ish to the grid; < n for n >= 1
+  const int64_t blocks = (int64_t)dev::sm_count() * 8;
+  if (nin == 2)
+    return dev::launch_pdl(dev::stream_peak_kernel<2>, blocks, dev::kThreads, stream, a, b, out,
+                           n, rot % (n ? n : 1u), reps);
+  return dev::launch_pdl(dev::stream_peak_kernel<1>, blocks, dev::kThreads, stream, a, b, out,
+                         n, rot % (n ? n : 1u), reps);
+}
 
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,
                         cudaStream_t stream) {

@@ -51,9 +51,9 @@ cudaError_t launch_poly(int kind, int dtype, int form1, int deg1, int deg2, cons
                         const Layout &l, const DevProg &p1, const DevProg &p2,
                         cudaStream_t stream, int variant = 0);
 
-// MUFU controls (fn used by kActFwd / kActBwd).
+// MUFU controls (fn used by kActFwd / kActBwd; variant = POLY_CTRL_*).
 cudaError_t launch_ctrl(int kind, int dtype, int fn, const Streams &s, const Layout &l,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int variant);
 
 // Tanh softcap: forward with the odd tanh program, backward with an even
 // derivative program; alpha and 1/alpha as target-format bit patterns.
@@ -85,6 +85,11 @@ cudaError_t launch_rope(int variant, int inv, const RopeArgs &a, const RopeConst
 // (clamped to [0, cap_rows] on the device, as the ragged kernels do).
 cudaError_t launch_zero_outside(uint16_t *out, const int32_t *seg, int32_t nseg,
                                 int64_t cap_rows, int64_t cols, cudaStream_t stream);
+
+// Streaming-bandwidth probe: reps passes of out = a (nin 1) or a ^ b (nin 2)
+// over nvec 16-byte chunks (every stream 16-byte aligned, nvec < 2^31).
+cudaError_t launch_stream_peak(int nin, const uint16_t *a, const uint16_t *b, uint16_t *out,
+                               int64_t nvec, int reps, cudaStream_t stream);
 
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,

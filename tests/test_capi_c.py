@@ -48,5 +48,5 @@ def test_c_program_uses_the_abi(tmp_path):
     assert lines["fit"].split()[0] == "POLY_OK"
     li, lc, degree, form = lines["fit"].split()[1:]
     assert (float(li), float(lc), int(degree), int(form)) == (4.75, 4.75, 4, 2)   # even form
-    assert int(lines["abi"]) == 3
+    assert int(lines["abi"]) == 4
     assert int(lines["empty"]) == 0 and int(lines["bad"]) == -1

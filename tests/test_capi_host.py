@@ -117,7 +117,7 @@ def test_fit_argument_errors(L):
         o = B.poly_fit_defaults()
         setattr(o, field, value)
         assert L.poly_fit(0, 0, 0, 3, ctypes.byref(o), ctypes.byref(p)) == B.POLY_EINVAL
-    assert L.poly_abi_version() == B.ABI_VERSION == 3
+    assert L.poly_abi_version() == B.ABI_VERSION == 4
     # no admissible clamp at all: Lc starts above Li + 1
     o = B.poly_fit_defaults()
     o.li_max, o.lc_min = 2.0, 5.0
@@ -136,6 +136,44 @@ def test_set_program_rejects_inconsistent_descriptors(L):
     assert L.poly_set_program(ctypes.byref(bad)) == B.POLY_ENOPROG
     assert L.poly_set_program(None) == B.POLY_EINVAL
     B.poly_reset_programs()
+
+
+def test_set_program_rejects_bad_clamps(L):
+    """The clamp Lc must be a finite positive target-format value equal to
+    lc, no further than Li + 1 (§3.2 step 6): a descriptor breaking any of
+    these would make every later call return NaN or unclamped values."""
+    good = B.poly_fit(B.POLY_SIGMOID, B.POLY_FWD, B.POLY_BF16, 3)
+    assert L.poly_set_program(ctypes.byref(good)) == B.POLY_OK
+    cases = [
+        ("lc_bits", 0x7FC0, None, None),          # NaN
+        ("lc_bits", 0x7F80, None, None),          # +inf
+        ("lc_bits", 0xFF80, None, None),          # -inf
+        ("lc_bits", 0xBF80, None, None),          # -1
+        ("lc_bits", 0x0000, None, None),          # +0
+        ("lc_bits", 0x8000, None, None),          # -0
+        ("lc", good.lc + 0.25, None, None),       # lc disagrees with lc_bits
+        ("li", good.lc - 1.5, None, None),        # Lc > Li + 1
+        ("li", float("nan"), None, None),
+        ("li", -1.0, None, None),
+    ]
+    try:
+        for field, value, _, _ in cases:
+            bad = B.PolyProgram.from_buffer_copy(bytes(good))
+            setattr(bad, field, value)
+            if field == "lc_bits":
+                bad.lc = float("nan") if value in (0x7FC0,) else bad.lc
+            assert L.poly_set_program(ctypes.byref(bad)) == B.POLY_ENOPROG, (field, value)
+        # the boundary Lc = Li + 1 itself is accepted
+        edge = B.PolyProgram.from_buffer_copy(bytes(good))
+        edge.li = good.lc - 1.0
+        assert L.poly_set_program(ctypes.byref(edge)) == B.POLY_OK
+        # derivation checks the forward program the same way
+        bad = B.PolyProgram.from_buffer_copy(bytes(good))
+        bad.lc_bits = 0x7F80
+        out = B.PolyProgram()
+        assert L.poly_derive_program(ctypes.byref(bad), ctypes.byref(out)) == B.POLY_ENOPROG
+    finally:
+        B.poly_reset_programs()
 
 
 FAKE = 0x7F0000001000          # never dereferenced: every call below fails validation
@@ -178,6 +216,32 @@ def test_device_calls_reject_bad_arguments_on_host(L):
     # diagnostic: FMA needs c, bad op
     assert L.poly_diag_packed(0, 0, FAKE, FAKE + 4096, None, FAKE + 8192, 8, s) == B.POLY_EINVAL
     assert L.poly_diag_packed(9, 0, FAKE, FAKE + 4096, FAKE, FAKE + 8192, 8, s) == B.POLY_EINVAL
+    # per-call variants: unknown SwiGLU rule or control variant
+    assert L.poly_swiglu_fwd_v(2, 1, FAKE, FAKE + 8192, FAKE + 16384, 4, 16, 16, 16, 16,
+                               s) == B.POLY_EINVAL
+    assert L.poly_swiglu_bwd_v(-1, 1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576,
+                               FAKE + 32768, 4, 16, 16, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_fwd_ragged_v(5, 1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 30000, 4, 4,
+                                      16, None, s) == B.POLY_EINVAL
+    assert L.poly_swiglu_bwd_ragged_v(5, 1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576,
+                                      FAKE + 32768, FAKE + 40000, 4, 4, 16, None,
+                                      s) == B.POLY_EINVAL
+    assert L.poly_ctrl_act_fwd_v(2, 0, 0, FAKE, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    assert L.poly_ctrl_act_bwd_v(-1, 0, 0, FAKE, FAKE + 4096, FAKE + 8192, 8, s) == B.POLY_EINVAL
+    assert L.poly_ctrl_swiglu_fwd_v(3, 1, FAKE, FAKE + 8192, FAKE + 16384, 4, 16, 16, 16, 16,
+                                    s) == B.POLY_EINVAL
+    assert L.poly_ctrl_swiglu_bwd_v(3, 1, FAKE, FAKE + 8192, FAKE + 16384, FAKE + 24576,
+                                    FAKE + 32768, 4, 16, 16, 16, 16, 16, 16, s) == B.POLY_EINVAL
+    # the packed control shares the validation
+    assert L.poly_ctrl_act_fwd_v(1, 0, 0, FAKE + 1, FAKE + 4096, 8, s) == B.POLY_EINVAL
+    assert L.poly_ctrl_act_fwd_v(1, 0, 0, FAKE, FAKE + 2, 8, s) == B.POLY_EINVAL
+    # streaming probe: nin, n a multiple of 8, reps range, 16-byte alignment, overlap
+    for args in ((3, FAKE, FAKE, FAKE + 8192, 64, 1), (1, FAKE, None, FAKE + 8192, 60, 1),
+                 (1, FAKE, None, FAKE + 8192, 64, 0), (1, FAKE, None, FAKE + 8192, 64, 1 << 21),
+                 (1, FAKE + 8, None, FAKE + 8192, 64, 1), (2, FAKE, FAKE + 4104, FAKE + 8192, 64, 1),
+                 (2, FAKE, None, FAKE + 8192, 64, 1), (1, FAKE, None, FAKE + 64, 64, 1),
+                 (1, FAKE, None, FAKE + 8192, -8, 1), (1, FAKE, None, FAKE + 8192, 1 << 34, 1)):
+        assert L.poly_diag_stream_peak(*args, s) == B.POLY_EINVAL, args
 
 
 def test_oversized_and_wrapping_arguments_are_rejected(L):
@@ -252,6 +316,13 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_ragged_zero_outside(None, FAKE, 4, 0, 16, s) == B.POLY_OK
     assert L.poly_ragged_zero_outside(None, FAKE, 4, 8, 0, s) == B.POLY_OK
     assert L.poly_diag_packed(0, 0, None, None, None, None, 0, s) == B.POLY_OK
+    assert L.poly_ctrl_act_fwd_v(1, 2, 0, None, None, 0, s) == B.POLY_OK
+    assert L.poly_ctrl_swiglu_bwd_v(1, 1, None, None, None, None, None, 0, 8, 8, 8, 8, 8, 8,
+                                    s) == B.POLY_OK
+    assert L.poly_swiglu_fwd_v(1, 1, None, None, None, 0, 16, 16, 16, 16, s) == B.POLY_OK
+    assert L.poly_swiglu_bwd_ragged_v(0, 1, None, None, None, None, None, FAKE, 4, 0, 16, None,
+                                      s) == B.POLY_OK
+    assert L.poly_diag_stream_peak(2, None, None, None, 0, 1, s) == B.POLY_OK
     assert L.poly_last_cuda_error() == before
 
 
@@ -269,6 +340,34 @@ def test_failure_injection_is_consumed_only_by_launches(L):
         assert L.poly_last_cuda_error() == before
     finally:
         assert L.poly_debug_fail_launches(701, 0) == 2       # both still pending; cleared
+
+
+def test_per_call_swiglu_rule_ignores_the_process_default(L):
+    """The _v SwiGLU calls take their rule from the argument: with the
+    process-wide default set to either rule, both rules validate and reach
+    their launch (shown by consuming an injected launch failure), and an
+    unknown rule is refused before any launch."""
+    T, H = 4, 16
+    g, u, dy, dg, du = (FAKE + (k << 16) for k in range(5))
+    seg = FAKE + (6 << 16)
+    try:
+        for default in (B.POLY_SWIGLU_DIRECT, B.POLY_SWIGLU_SIGMOID):
+            B.poly_set_swiglu_variant(default)
+            for v in (B.POLY_SWIGLU_DIRECT, B.POLY_SWIGLU_SIGMOID):
+                calls = (
+                    lambda: L.poly_swiglu_fwd_v(v, 1, g, u, dg, T, H, H, H, H, None),
+                    lambda: L.poly_swiglu_bwd_v(v, 0, g, u, dy, dg, du, T, H, H, H, H, H, H, None),
+                    lambda: L.poly_swiglu_fwd_ragged_v(v, 1, g, u, dg, seg, 2, T, H, None, None),
+                    lambda: L.poly_swiglu_bwd_ragged_v(v, 0, g, u, dy, dg, du, seg, 2, T, H, None,
+                                                       None),
+                )
+                for call in calls:
+                    assert L.poly_debug_fail_launches(812, 1) == 0
+                    assert call() == B.POLY_ECUDA and L.poly_last_cuda_error() == 812
+            assert B.poly_get_swiglu_variant() == default
+    finally:
+        L.poly_debug_fail_launches(812, 0)
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)
 
 
 def test_swiglu_variant_switch(L):
