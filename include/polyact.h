@@ -439,17 +439,19 @@ int poly_diag_packed(int op, int dtype, const void *a, const void *b, const void
 /* ---- streaming-bandwidth probe (a measurement tool; no counterpart in the
  * paper, which states its L2 and HBM regimes (§4.2) but no peaks) ---------
  * reps passes of out[i] = a[i] (nin = 1) or a[i] ^ b[i] (nin = 2, bitwise)
- * over n 16-bit elements, with the loads, stores and residency of the
- * streaming kernels (eight 256-thread blocks per SM); pass r assigns each
- * 16-byte chunk to another thread than pass r - 1 did.  The rate
- * reps * n * 2 * (nin + 1) bytes / time is the L2 streaming bandwidth of
- * that access pattern when a, b and out fit in L2 and the launch spans many
- * passes, and its HBM rate when they do not.  a, b, out: device memory,
- * 16-byte aligned; out overlaps neither input; n a multiple of 8 below
- * 2^34; 1 <= reps <= 2^20; b unused (may be NULL) for nin = 1.  POLY_EINVAL
- * otherwise; n == 0 is a no-op. */
-int poly_diag_stream_peak(int nin, const void *a, const void *b, void *out, int64_t n,
-                          int reps, poly_stream_t stream);
+ * over n 16-bit elements, with the 16-byte loads and stores of the
+ * streaming kernels; every thread keeps `inflight` (1, 2, 4 or 8) 16-byte
+ * chunks per input in flight, from as many 256-thread blocks as the SMs hold
+ * at once for that register budget, and pass r assigns each chunk to another
+ * thread than pass r - 1 did.
+ * The rate reps * n * 2 * (nin + 1) bytes / time is the L2 streaming
+ * bandwidth of that access pattern when a, b and out fit in L2 and the
+ * launch spans many passes, and its HBM rate when they do not.  a, b, out:
+ * device memory, 16-byte aligned; out overlaps neither input; n a multiple of
+ * 8 below 2^34; 1 <= reps <= 2^20; b unused (may be NULL) for nin = 1.
+ * POLY_EINVAL otherwise; n == 0 is a no-op. */
+int poly_diag_stream_peak(int nin, int inflight, const void *a, const void *b, void *out,
+                          int64_t n, int reps, poly_stream_t stream);
 
 /* ---- failure injection (host only; no counterpart in the paper) ----------
  * poly_debug_fail_launches: the next `count` kernel launches, from any entry

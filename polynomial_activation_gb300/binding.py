@@ -134,7 +134,7 @@ def lib():
     L.poly_swiglu_bwd_ragged.argtypes = [_i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p]
     L.poly_ragged_zero_outside.argtypes = [_p, _p, _i, _i64, _i64, _p]
     L.poly_diag_packed.argtypes = [_i, _i, _p, _p, _p, _p, _i64, _p]
-    L.poly_diag_stream_peak.argtypes = [_i, _p, _p, _p, _i64, _i, _p]
+    L.poly_diag_stream_peak.argtypes = [_i, _i, _p, _p, _p, _i64, _i, _p]
     L.poly_ctrl_act_fwd_v.argtypes = [_i, _i, _i, _p, _p, _i64, _p]
     L.poly_ctrl_act_bwd_v.argtypes = [_i, _i, _i, _p, _p, _p, _i64, _p]
     for name in ("poly_swiglu_fwd_v", "poly_ctrl_swiglu_fwd_v"):
@@ -489,13 +489,14 @@ def poly_swiglu_bwd_ragged_v(variant, dtype, g, u, dy, dg, du, seg_off, num_segm
            "poly_swiglu_bwd_ragged_v")
 
 
-def poly_diag_stream_peak(nin, a, b, out, n=None, reps=1, stream=None):
+def poly_diag_stream_peak(nin, a, b, out, n=None, reps=1, inflight=2, stream=None):
     """reps streaming passes out = a (nin 1) or a ^ b (nin 2) over n 16-bit
-    elements (the bandwidth probe)."""
+    elements with `inflight` 16-byte chunks per input in flight per thread
+    (the bandwidth probe)."""
     n = a.numel() if n is None else n
     for t, nm in ((a, "a"), (b, "b"), (out, "out")):
         _room(t, 2 * n, "poly_diag_stream_peak", nm)
-    _check(lib().poly_diag_stream_peak(nin, _ptr(a), _ptr(b), _ptr(out), n, reps,
+    _check(lib().poly_diag_stream_peak(nin, inflight, _ptr(a), _ptr(b), _ptr(out), n, reps,
                                        _stream(stream)), "poly_diag_stream_peak")
 
 

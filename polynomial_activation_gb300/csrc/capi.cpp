@@ -803,10 +803,11 @@ int poly_rope_bwd(int variant, const void *dq, const void *dk, void *dq_out, voi
                    hkv, head_dim, pos_offset, stream);
 }
 
-int poly_diag_stream_peak(int nin, const void *a, const void *b, void *out, int64_t n,
-                          int reps, poly_stream_t stream) {
+int poly_diag_stream_peak(int nin, int inflight, const void *a, const void *b, void *out,
+                          int64_t n, int reps, poly_stream_t stream) {
   if ((nin != 1 && nin != 2) || n < 0 || (n & 7) || reps < 1 || reps > (1 << 20))
     return POLY_EINVAL;
+  if (inflight != 1 && inflight != 2 && inflight != 4 && inflight != 8) return POLY_EINVAL;
   if ((n >> 3) >= (int64_t(1) << 31)) return POLY_EINVAL;
   if (n == 0) return POLY_OK;
   if (nin == 1) b = a;
@@ -818,7 +819,7 @@ int poly_diag_stream_peak(int nin, const void *a, const void *b, void *out, int6
   for (int i = 0; i < 2; ++i)
     if (overlaps(so, si[i])) return POLY_EINVAL;
   return launch_status([&] {
-    return launch_stream_peak(nin, static_cast<const uint16_t *>(a),
+    return launch_stream_peak(nin, inflight, static_cast<const uint16_t *>(a),
                               static_cast<const uint16_t *>(b), static_cast<uint16_t *>(out),
                               n >> 3, reps, reinterpret_cast<cudaStream_t>(stream));
   });

@@ -70,67 +70,106 @@ static cudaError_t diag_dt(int op, const Streams &s, const Layout &l, cudaStream
 
 // Streaming-bandwidth probe (a measurement tool beside the kernels it
 // measures): `reps` passes over nvec 16-byte chunks, each writing out = a or
-// a ^ b with the kernels' own loads and stores, from a grid of eight 256-thread
-// blocks per SM (full residency).  Pass r shifts the chunk a thread takes by
-// r * rot (mod nvec), so every pass moves each chunk through another SM.
-// With a working set that fits in L2 and enough passes to hide one launch's
-// ramp and drain, the rate is the L2 streaming bandwidth of the kernels'
-// access pattern; above L2 size it is the HBM rate of that pattern.
-template <int NIN>
+// a ^ b with the kernels' own loads and stores.  Every thread keeps INF
+// chunks per input in flight: U of its chunk slots (grid-strided) times ILP
+// consecutive passes loaded before any is stored.  Pass r shifts the chunk a
+// slot takes by r * rot (mod nvec), so every pass moves each chunk through
+// another SM.  With a working set that fits in L2 and enough passes to hide
+// one launch's ramp and drain, the rate is the L2 streaming bandwidth of
+// 16-byte register-staged accesses with that much in flight; above L2 size
+// it is the HBM rate of the same pattern.
+template <int NIN, int U, int ILP>
 __global__ void __launch_bounds__(kThreads)
     stream_peak_kernel(const uint16_t *a, const uint16_t *b, uint16_t *out, uint32_t nvec,
                        uint32_t rot, int reps) {
-  pdl_enter();
+  pdl_wait();
   const uint32_t stride = gridDim.x * (uint32_t)kThreads;
   const uint32_t first = blockIdx.x * (uint32_t)kThreads + threadIdx.x;
   uint32_t shift = 0;
 #pragma unroll 1
-  for (int r = 0; r < reps; ++r) {
+  for (int r = 0; r < reps; r += ILP) {
 #pragma unroll 1
-    for (uint32_t c = first; c < nvec; c += 2 * stride) {
-      uint32_t k[2];
-      uint4 v[2][NIN];
+    for (uint32_t c = first; c < nvec; c += U * stride) {
+      uint32_t k[U][ILP];
+      uint4 v[U][ILP][NIN];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         const uint32_t j = c + u * stride;
-        k[u] = 0xFFFFFFFFu;
-        if (j < nvec) {
-          k[u] = j + shift < nvec ? j + shift : j + shift - nvec;
-          v[u][0] = ld_stream(a + (size_t)k[u] * 8);
-          if constexpr (NIN == 2) v[u][1] = ld_stream(b + (size_t)k[u] * 8);
+        uint32_t sh = shift;
+#pragma unroll
+        for (int q = 0; q < ILP; ++q) {
+          k[u][q] = 0xFFFFFFFFu;
+          if (j < nvec && r + q < reps) {
+            k[u][q] = j + sh < nvec ? j + sh : j + sh - nvec;
+            v[u][q][0] = ld_stream(a + (size_t)k[u][q] * 8);
+            if constexpr (NIN == 2) v[u][q][1] = ld_stream(b + (size_t)k[u][q] * 8);
+          }
+          sh += rot;
+          if (sh >= nvec) sh -= nvec;
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (k[u] != 0xFFFFFFFFu) {
-          uint4 o = v[u][0];
-          if constexpr (NIN == 2) {
-            o.x ^= v[u][1].x;
-            o.y ^= v[u][1].y;
-            o.z ^= v[u][1].z;
-            o.w ^= v[u][1].w;
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int q = 0; q < ILP; ++q) {
+          if (k[u][q] != 0xFFFFFFFFu) {
+            uint4 o = v[u][q][0];
+            if constexpr (NIN == 2) {
+              o.x ^= v[u][q][1].x;
+              o.y ^= v[u][q][1].y;
+              o.z ^= v[u][q][1].z;
+              o.w ^= v[u][q][1].w;
+            }
+            st_stream(out + (size_t)k[u][q] * 8, o);
           }
-          st_stream(out + (size_t)k[u] * 8, o);
         }
       }
     }
-    shift += rot;
-    if (shift >= nvec) shift -= nvec;
+#pragma unroll
+    for (int q = 0; q < ILP; ++q) {
+      shift += rot;
+      if (shift >= nvec) shift -= nvec;
+    }
   }
+  pdl_release();
+}
+
+// One launch of a probe instance with as many blocks as the SMs hold at
+// once (its register budget decides: more chunks in flight per thread means
+// fewer resident threads).
+template <int NIN, int U, int ILP>
+static cudaError_t stream_peak_launch(const uint16_t *a, const uint16_t *b, uint16_t *out,
+                                      uint32_t n, uint32_t rot, int reps, cudaStream_t stream) {
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, stream_peak_kernel<NIN, U, ILP>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  return launch_pdl(stream_peak_kernel<NIN, U, ILP>, (int64_t)sm_count() * per_sm, kThreads,
+                    stream, a, b, out, n, rot, reps);
+}
+
+template <int NIN>
+static cudaError_t stream_peak_nin(int inflight, const uint16_t *a, const uint16_t *b,
+                                   uint16_t *out, uint32_t n, uint32_t rot, int reps,
+                                   cudaStream_t stream) {
+  switch (inflight) {
+    case 1: return stream_peak_launch<NIN, 1, 1>(a, b, out, n, rot, reps, stream);
+    case 2: return stream_peak_launch<NIN, 2, 1>(a, b, out, n, rot, reps, stream);
+    case 4: return stream_peak_launch<NIN, 2, 2>(a, b, out, n, rot, reps, stream);
+    case 8: return stream_peak_launch<NIN, 2, 4>(a, b, out, n, rot, reps, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dev
 
-cudaError_t launch_stream_peak(int nin, const uint16_t *a, const uint16_t *b, uint16_t *out,
-                               int64_t nvec, int reps, cudaStream_t stream) {
+cudaError_t launch_stream_peak(int nin, int inflight, const uint16_t *a, const uint16_t *b,
+                               uint16_t *out, int64_t nvec, int reps, cudaStream_t stream) {
   const uint32_t n = (uint32_t)nvec;
-  const uint32_t rot = (n / 7u) | 1u;   // any shift co-prime-ish to the grid; < n for n >= 1
-  const int64_t blocks = (int64_t)dev::sm_count() * 8;
-  if (nin == 2)
-    return dev::launch_pdl(dev::stream_peak_kernel<2>, blocks, dev::kThreads, stream, a, b, out,
-                           n, rot % (n ? n : 1u), reps);
-  return dev::launch_pdl(dev::stream_peak_kernel<1>, blocks, dev::kThreads, stream, a, b, out,
-                         n, rot % (n ? n : 1u), reps);
+  const uint32_t rot = ((n / 7u) | 1u) % n;   // n >= 1; shift stays below n
+  return nin == 2 ? dev::stream_peak_nin<2>(inflight, a, b, out, n, rot, reps, stream)
+                  : dev::stream_peak_nin<1>(inflight, a, b, out, n, rot, reps, stream);
 }
 
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,

@@ -75,7 +75,7 @@ template <int CORE>
 __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restrict__ x,
                                                            float *__restrict__ y, int64_t n,
                                                            int vec, Exp2Params p) {
-  pdl_enter();
+  pdl_wait();
   int64_t head = n;
   if (vec) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(x);
@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kExp2Threads) exp2_kernel(const float *__restr
     const float xv = x[e];
     y[e] = exp2_pair<CORE>(xv, xv, p).x;
   }
+  pdl_release();
 }
 
 template <int CORE>

@@ -38,7 +38,7 @@ __device__ __forceinline__ void zero_range(uint16_t *p, int64_t s, int64_t e, in
 __global__ void __launch_bounds__(kFillThreads)
     zero_outside_kernel(uint16_t *out, const int32_t *seg, int32_t nseg, int64_t cap_rows,
                         int64_t cols) {
-  pdl_enter();
+  pdl_wait();
   int64_t lo, hi;
   ragged_rows(seg, nseg, cap_rows, nullptr, lo, hi);
   if (lo > cap_rows) lo = cap_rows;   // offsets past the buffer: an empty range
@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kFillThreads)
   const int64_t nt = (int64_t)gridDim.x * kFillThreads;
   zero_range(out, 0, lo * cols, t, nt);
   zero_range(out, hi * cols, cap_rows * cols, t, nt);
+  pdl_release();
 }
 
 }  // namespace dev

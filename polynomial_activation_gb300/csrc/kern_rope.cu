@@ -110,7 +110,7 @@ __device__ __forceinline__ void st16(uint16_t *p, const uint4 &v) {
 
 template <int VARIANT, int INV>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeConsts k) {
-  pdl_enter();
+  pdl_wait();
   const int64_t groups = a.head_dim >> 3;                // chunks of 4 frequencies
   const int64_t H = a.hq + a.hkv;
   const int64_t hchunks = (H + kHeadsPerThread - 1) / kHeadsPerThread;
@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(RopeArgs a, RopeCons
       }
     }
   }
+  pdl_release();
 }
 
 template <int VARIANT>

@@ -87,9 +87,10 @@ cudaError_t launch_zero_outside(uint16_t *out, const int32_t *seg, int32_t nseg,
                                 int64_t cap_rows, int64_t cols, cudaStream_t stream);
 
 // Streaming-bandwidth probe: reps passes of out = a (nin 1) or a ^ b (nin 2)
-// over nvec 16-byte chunks (every stream 16-byte aligned, nvec < 2^31).
-cudaError_t launch_stream_peak(int nin, const uint16_t *a, const uint16_t *b, uint16_t *out,
-                               int64_t nvec, int reps, cudaStream_t stream);
+// over nvec 16-byte chunks (every stream 16-byte aligned, 1 <= nvec < 2^31),
+// `inflight` (1, 2, 4 or 8) chunks per input in flight per thread.
+cudaError_t launch_stream_peak(int nin, int inflight, const uint16_t *a, const uint16_t *b,
+                               uint16_t *out, int64_t nvec, int reps, cudaStream_t stream);
 
 // Raw packed instruction over element triples (arithmetic diagnostic).
 cudaError_t launch_diag(int op, int dtype, const Streams &s, const Layout &l,

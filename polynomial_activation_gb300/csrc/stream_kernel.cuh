@@ -48,14 +48,25 @@ __device__ __forceinline__ void st_stream(uint16_t *p, const uint4 &v) {
                : "memory");
 }
 
-// Programmatic dependent launch: let the next kernel on the stream be
-// scheduled as soon as every block of this one is, and wait here until the
-// previous kernel has completed and its writes are visible.  Ordering
-// between kernels is unchanged; only launch latency is hidden.  (Both are
-// no-ops for a launch without the programmatic-serialisation attribute.)
-__device__ __forceinline__ void pdl_enter() {
+// Programmatic dependent launch.  pdl_wait() (first thing in every kernel):
+// wait until the previous kernel on the stream has completed and its writes
+// are visible -- nothing is read before.  pdl_release() (last thing, after the
+// stores): this block is done, so the next kernel on the stream may be
+// launched once every block of this one has released or exited; its blocks
+// are then scheduled while this grid's last stores drain and its completion
+// is signalled, instead of after.  Releasing at the end rather than at entry
+// keeps the next kernel's blocks from occupying SMs, parked in their own
+// wait, while this grid still streams: measured on GB300, 6-25 % off
+// launches of 0.5-8 M elements (L2-resident), no change at HBM sizes.  The
+// dense kernel releases earlier, right after its loads are issued, where
+// that measured faster still: one-input launches of one chunk per thread
+// (below ~1.2 M elements) and multi-input launches whose grid is resident at
+// once (at most 8 blocks per SM) -- 5-12 % off 0.25-4 M elements.
+// Ordering between kernels is unchanged.  (Both are no-ops for a launch
+// without the programmatic-serialisation attribute.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
@@ -66,15 +77,18 @@ __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
 
 // Chunks of 8 elements per stream per thread: two for single-input
 // operations, one for multi-input ones (measured on GB300 with a one-pass
-// grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes).  A
-// single-input call too small to give every SM four blocks of two-chunk
-// threads takes one chunk per thread instead (dense kernel only): at 0.5-2 M
-// elements that keeps twice as many warps issuing loads.
+// grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes at HBM
+// sizes).  Smaller flat calls of the dense kernel (measured over 256 K-268 M
+// elements, 256-thread blocks, release after the stores):
+//  * single input: one chunk per thread while two would give fewer than two
+//    blocks per SM (below ~1.2 M elements);
+//  * two inputs, one output: two chunks per thread while that grid holds 1 to
+//    16 blocks per SM (~0.6-10 M elements: 5-25 % faster there), one above.
 template <class Op>
 __host__ __device__ constexpr int chunks_per_thread() {
   return Op::NIN == 1 ? 2 : 1;
 }
-constexpr int kMinBlocksPerSm = 4;
+constexpr int kTwoChunkMaxBlocksPerSm = 16;
 constexpr int64_t kRowsTwoOutMax = int64_t(1) << 19;
 
 template <class Op>
@@ -133,7 +147,7 @@ __device__ __forceinline__ void ragged_rows(const int32_t *seg, int32_t nseg, in
 template <class Op>
 __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
                                                           typename Op::Params p) {
-  pdl_enter();
+  pdl_wait();
   constexpr int U = chunks_per_thread<Op>();
   int64_t n = l.n, off = 0;
   if (l.mode == kRagged) {
@@ -189,6 +203,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
     const int64_t e = i < head ? i : body_end + (i - head);
     apply_one<Op>(in, out, e, p);
   }
+  pdl_release();
 }
 
 // Dense: the common layouts with 32-bit indices, no layout branches and no
@@ -205,9 +220,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
 //                 buffer); the row of a chunk comes from a multiply and a
 //                 shift instead of a division.
 enum DenseMode { kDenseFlat = 0, kDenseRagged = 1, kDenseRows = 2 };
+enum ReleaseAt { kReleaseAfterLoads = 1, kReleaseAtEnd = 2 };
 
 struct DenseArgs {
   uint32_t nvec, ntail;            // chunks of 8 elements; flat tail elements
+  uint32_t release_at;              // where dependents are released: kRelease*
   const int32_t *seg;              // ragged: device offsets, their count,
   int32_t nseg, cap_rows;          //   the row capacity and the status word
   int32_t *status;
@@ -241,7 +258,7 @@ __device__ __forceinline__ size_t chunk_offset(uint32_t i, const DenseArgs &a, u
 template <class Op, int MODE, int U>
 __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, DenseArgs a,
                                                          typename Op::Params p) {
-  pdl_enter();
+  pdl_wait();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
   uint32_t nvec = a.nvec;
@@ -266,6 +283,7 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, DenseArgs a,
         r[u][k] = ld_stream(src[k] + chunk_offset<MODE>(i, a, a.ld_in[k]));
     }
   }
+  if (a.release_at == kReleaseAfterLoads) pdl_release();
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const uint32_t i = base + u * kThreads;
@@ -287,6 +305,7 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, DenseArgs a,
     for (int k = 0; k < Op::NOUT; ++k) out[k] = dst[k];
     apply_one<Op>(in, out, (int64_t)nvec * 8 + threadIdx.x, p);
   }
+  if (a.release_at == kReleaseAtEnd) pdl_release();
 }
 
 // Strided: rows x cols with a leading dimension per stream (a separate
@@ -294,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(Streams s, DenseArgs a,
 template <class Op>
 __global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
                                                            typename Op::Params p) {
-  pdl_enter();
+  pdl_wait();
   const uint16_t *src[3] = {s.in0, s.in1, s.in2};
   uint16_t *dst[2] = {s.out0, s.out1};
   const int64_t gid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -328,6 +347,7 @@ __global__ void __launch_bounds__(kThreads) strided_kernel(Streams s, Layout l,
       apply_one<Op>(in, out, col, p);
     }
   }
+  pdl_release();
 }
 
 // Blocks for a launch: `per_thread` elements per thread, covering the work
@@ -337,7 +357,7 @@ int64_t grid_for(const Layout &l, int per_thread);
 // Streaming multiprocessors of the calling thread's current device (cached).
 int sm_count();
 
-// Launch with the programmatic-stream-serialisation attribute (see pdl_enter).
+// Launch with the programmatic-stream-serialisation attribute (see pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cudaStream_t stream,
                        Args... args) {
@@ -352,6 +372,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cu
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// A dense-kernel launch, releasing its dependents where pdl_release says.
+template <class Op, int MODE, int U>
+cudaError_t launch_dense(int64_t blocks, cudaStream_t stream, const Streams &s, DenseArgs a,
+                         const typename Op::Params &p) {
+  if (Op::NIN == 1)
+    a.release_at = U == 1 ? kReleaseAfterLoads : kReleaseAtEnd;
+  else
+    a.release_at = blocks <= 8 * (int64_t)sm_count() ? kReleaseAfterLoads : kReleaseAtEnd;
+  return launch_pdl(dense_kernel<Op, MODE, U>, blocks, kThreads, stream, s, a, p);
 }
 
 // Every stream of s starts on a 16-byte boundary (unused streams are null).
@@ -387,7 +418,7 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
         for (int k = 0; k < 2; ++k) a.ld_out[k] = (uint32_t)l.ld_out[k];
         int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
         if (blocks < 1) blocks = 1;
-        return launch_pdl(dense_kernel<Op, kDenseRows, U>, blocks, kThreads, stream, s, a, p);
+        return launch_dense<Op, kDenseRows, U>(blocks, stream, s, a, p);
       }
       const int64_t blocks = grid_for(l, l.vec ? 8 : 1);
       return launch_pdl(strided_kernel<Op>, blocks, kThreads, stream, s, l, p);
@@ -400,14 +431,18 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     a.ntail = (uint32_t)(l.n & 7);
     int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
+    const int64_t two = ((int64_t)a.nvec + 2 * kThreads - 1) / (2 * kThreads);   // U = 2 grid
     if constexpr (U > 1) {
-      if (blocks < (int64_t)kMinBlocksPerSm * sm_count()) {
+      if (two < 2 * (int64_t)sm_count()) {
         blocks = ((int64_t)a.nvec + kThreads - 1) / kThreads;
         if (blocks < 1) blocks = 1;
-        return launch_pdl(dense_kernel<Op, kDenseFlat, 1>, blocks, kThreads, stream, s, a, p);
+        return launch_dense<Op, kDenseFlat, 1>(blocks, stream, s, a, p);
       }
+    } else if constexpr (Op::NIN == 2 && Op::NOUT == 1) {
+      if (two >= sm_count() && two <= (int64_t)kTwoChunkMaxBlocksPerSm * sm_count())
+        return launch_dense<Op, kDenseFlat, 2>(two, stream, s, a, p);
     }
-    return launch_pdl(dense_kernel<Op, kDenseFlat, U>, blocks, kThreads, stream, s, a, p);
+    return launch_dense<Op, kDenseFlat, U>(blocks, stream, s, a, p);
   }
   if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < lim && aligned16(s)) {
     DenseArgs a{};
@@ -418,7 +453,7 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     a.cols = (uint32_t)l.cols;
     int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(dense_kernel<Op, kDenseRagged, U>, blocks, kThreads, stream, s, a, p);
+    return launch_dense<Op, kDenseRagged, U>(blocks, stream, s, a, p);
   }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);

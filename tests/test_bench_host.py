@@ -5,11 +5,13 @@ import stat
 import sys
 import time
 
+import numpy as np
+
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 import bench  # noqa: E402
 
 FAKE = """#!/bin/sh
-# stand-in for nvidia-smi --query-gpu ... -lms 200: one line per 20 ms
+# stand-in for nvidia-smi --query-gpu ... -lms N: one line per 20 ms
 i=0
 while [ $i -lt 500 ]; do
   if [ $i -eq 3 ]; then
@@ -23,19 +25,37 @@ done
 """
 
 
-def test_clock_sampler_parses_samples_and_reasons(tmp_path, monkeypatch):
+def _fake_smi(tmp_path, monkeypatch):
     exe = tmp_path / "nvidia-smi"
     exe.write_text(FAKE)
     exe.chmod(exe.stat().st_mode | stat.S_IEXEC)
     monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+
+
+def test_clock_sampler_parses_samples_and_reasons(tmp_path, monkeypatch):
+    _fake_smi(tmp_path, monkeypatch)
     c = bench.ClockSampler(0)
     c.start()
-    assert c.skip >= 1                      # start() waited for the first sample
+    assert len(c.lines) >= 1                # start() waited for the first sample
     time.sleep(0.3)
     r = c.stop()
-    assert r["samples"] >= 3
+    assert r["samples"] >= 10
     assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0 and r["mem_mhz"] == 3996.0
-    assert r["reasons"] == (["sw_power_cap"] if c.skip <= 3 else [])
+    assert r["reasons"] == ["sw_power_cap"]   # the fourth line, inside the window
+    assert 290 <= r["window_ms"] < 1000
+
+
+def test_clock_sampler_brackets_a_short_region(tmp_path, monkeypatch):
+    """A timed region shorter than the sampling period still gets the last
+    sample before it and the first one after it."""
+    _fake_smi(tmp_path, monkeypatch)
+    c = bench.ClockSampler(0)
+    c.start()
+    time.sleep(0.1)                          # past the throttled fourth line
+    c.t0 = time.monotonic()                  # the region starts now ...
+    r = c.stop()                             # ... and ends at once
+    assert r["samples"] >= 2 and r["window_ms"] < 20
+    assert r["reasons"] == []
 
 
 def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
@@ -69,8 +89,11 @@ def test_oracle_pool_covers_the_sample():
     x, dy = workloads.isolated_hbm("f16", n=10_007)
     pool = bench.OraclePool(3)
     try:
-        wall, per, sizes = pool.run(x, dy)
+        wall, per, sizes = pool.run("six", x, dy)
+        assert sum(sizes) == x.size and len(per) == len(sizes) == 3
+        assert wall > 0 and all(t > 0 for t in per)
+        g, u, d = (np.zeros((7, 24), np.uint16) for _ in range(3))
+        wall, per, sizes = pool.run("swiglu", g, u, d)
+        assert sum(sizes) == 7 and len(per) == 3
     finally:
         pool.close()
-    assert sum(sizes) == x.size and len(per) == len(sizes) == 3
-    assert wall > 0 and all(t > 0 for t in per)

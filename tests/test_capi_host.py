@@ -236,11 +236,14 @@ def test_device_calls_reject_bad_arguments_on_host(L):
     assert L.poly_ctrl_act_fwd_v(1, 0, 0, FAKE + 1, FAKE + 4096, 8, s) == B.POLY_EINVAL
     assert L.poly_ctrl_act_fwd_v(1, 0, 0, FAKE, FAKE + 2, 8, s) == B.POLY_EINVAL
     # streaming probe: nin, n a multiple of 8, reps range, 16-byte alignment, overlap
-    for args in ((3, FAKE, FAKE, FAKE + 8192, 64, 1), (1, FAKE, None, FAKE + 8192, 60, 1),
-                 (1, FAKE, None, FAKE + 8192, 64, 0), (1, FAKE, None, FAKE + 8192, 64, 1 << 21),
-                 (1, FAKE + 8, None, FAKE + 8192, 64, 1), (2, FAKE, FAKE + 4104, FAKE + 8192, 64, 1),
-                 (2, FAKE, None, FAKE + 8192, 64, 1), (1, FAKE, None, FAKE + 64, 64, 1),
-                 (1, FAKE, None, FAKE + 8192, -8, 1), (1, FAKE, None, FAKE + 8192, 1 << 34, 1)):
+    for args in ((3, 2, FAKE, FAKE, FAKE + 8192, 64, 1), (1, 2, FAKE, None, FAKE + 8192, 60, 1),
+                 (1, 2, FAKE, None, FAKE + 8192, 64, 0), (1, 2, FAKE, None, FAKE + 8192, 64, 1 << 21),
+                 (1, 2, FAKE + 8, None, FAKE + 8192, 64, 1),
+                 (2, 2, FAKE, FAKE + 4104, FAKE + 8192, 64, 1),
+                 (2, 2, FAKE, None, FAKE + 8192, 64, 1), (1, 2, FAKE, None, FAKE + 64, 64, 1),
+                 (1, 2, FAKE, None, FAKE + 8192, -8, 1), (1, 2, FAKE, None, FAKE + 8192, 1 << 34, 1),
+                 (1, 3, FAKE, None, FAKE + 8192, 64, 1), (1, 16, FAKE, None, FAKE + 8192, 64, 1),
+                 (1, 0, FAKE, None, FAKE + 8192, 64, 1)):
         assert L.poly_diag_stream_peak(*args, s) == B.POLY_EINVAL, args
 
 
@@ -322,7 +325,7 @@ def test_empty_calls_are_no_ops(L):
     assert L.poly_swiglu_fwd_v(1, 1, None, None, None, 0, 16, 16, 16, 16, s) == B.POLY_OK
     assert L.poly_swiglu_bwd_ragged_v(0, 1, None, None, None, None, None, FAKE, 4, 0, 16, None,
                                       s) == B.POLY_OK
-    assert L.poly_diag_stream_peak(2, None, None, None, 0, 1, s) == B.POLY_OK
+    assert L.poly_diag_stream_peak(2, 2, None, None, None, 0, 1, s) == B.POLY_OK
     assert L.poly_last_cuda_error() == before
 
 
