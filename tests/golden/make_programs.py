@@ -2,7 +2,7 @@
 
 Calls only ``oracle/``.  The GPU parity tests replay these programs on the
 CPU; the product's own fitter must reproduce them bit for bit
-(tests/test_fit_capi.py).  Re-run after any change to the oracle fitter:
+(tests/test_capi_host.py).  Re-run after any change to the oracle fitter:
 
     python tests/golden/make_programs.py
 """

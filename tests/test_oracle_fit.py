@@ -99,12 +99,17 @@ def _table2_rows():
 
 
 # How close the accepted program's Table 2 metric must come to the printed
-# value.  sigma' D4 and the D3 centred sigmoid land within 1% of the paper's
-# values; the others are order-of-magnitude checks, because the paper's exact
-# (Li, Lc) choice is not reproducible from its text (its Lc values are off
-# the stated 0.25 grid).
-T2_FACTOR = {("bwd", "sigmoid"): 1.02, ("fwd", "sigmoid"): 1.02, ("fwd", "tanh"): 1.5,
-             ("fwd", "silu"): 2.0, ("fwd", "gelu"): 3.0}
+# value.  sigma' D4 and the D3 centred sigmoid land within 1 % of the paper's
+# values.  For the other three the accepted program is not the paper's: the
+# Sollya column bounds the paper's clamps (test_sollya_column_bounds_the_clamp)
+# and shows SiLU's and GELU's below the ones accepted here, which the score of
+# §3.2 step 6 with the exact relu tail cannot select
+# (test_accepted_clamps_against_the_sollya_bound); tanh keeps the paper's clamp
+# but a different fit interval.  Their factors are the measured gaps (1.173,
+# 1.465, 2.826) with 0.5 % of margin, so that any change to the fitter or the
+# metric that moves them fails.
+T2_FACTOR = {("bwd", "sigmoid"): 1.01, ("fwd", "sigmoid"): 1.01, ("fwd", "tanh"): 1.18,
+             ("fwd", "silu"): 1.472, ("fwd", "gelu"): 2.84}
 
 
 @pytest.mark.parametrize("row", _table2_rows())
@@ -117,6 +122,115 @@ def test_table2_magnitudes(row):
     m = fit.table2_metric(p)
     k = T2_FACTOR[(d, name)]
     assert printed / k <= m <= printed * k, (name, m, printed)
+
+
+def _sollya_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "table2_sollya_bf16.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                d, name, D, form, v, lc = line.split()
+                rows.append((d, name, int(D), form, float(v) * 1e-3, float(lc)))
+    return rows
+
+
+def _monomials(form, D):
+    """Powers of t the row's polynomial carries (§3.1: no constant term
+    except for the even form)."""
+    return list(range(0, D + 1)) if form == "E" else list(range(1, D + 1))
+
+
+def _fp64_minimax(fn, direction, form, D, lc, m=3000):
+    """Smallest max |P(t) - r(t)| over m points of [0, Lc] for P in the
+    row's monomial span, r the half-domain residual: a linear program
+    (scipy's HiGHS), independent of the oracle's least-squares code."""
+    from scipy.optimize import linprog
+    t = np.linspace(0.0, lc, m)
+    V = np.stack([t ** p for p in _monomials(form, D)], axis=1)
+    y = ref.residual(fn, direction)(t)
+    k = V.shape[1]
+    A = np.vstack([np.hstack([V, -np.ones((m, 1))]), np.hstack([-V, -np.ones((m, 1))])])
+    res = linprog(np.r_[np.zeros(k), 1.0], A_ub=A, b_ub=np.r_[y, -y],
+                  bounds=[(None, None)] * k + [(0, None)], method="highs")
+    assert res.status == 0
+    return float(res.x[-1])
+
+
+@pytest.mark.parametrize("row", _sollya_rows())
+def test_sollya_column_bounds_the_clamp(row):
+    """The printed Sollya minimax errors (Table 2) bound each row's clamp:
+    an fpminimax fit with BF16 coefficients errs at least as much as the
+    unconstrained FP64 minimax on the same interval, which grows with Lc.
+    The FP64 minimax at the golden clamp stays below the printed value and,
+    except for the centred sigmoid (whose D3 minimax plateaus near 5.3e-3
+    for Lc in [5.75, 7]), exceeds it 0.25 further out -- so the paper's Lc
+    lies below that point.  A wrong residual, form or monomial set moves the
+    crossing and fails here."""
+    d, name, D, form, printed, lc = row
+    fn = gp.NAMES[name]
+    direction = ref.FWD if d == "fwd" else ref.BWD
+    assert ref.form_of(fn, direction) == form
+    assert _fp64_minimax(fn, direction, form, D, lc) <= printed
+    assert _fp64_minimax(fn, direction, form, D, lc + 0.25) > printed
+
+
+def _ls_error(fn, direction, D, li, lc, rounded):
+    """Table 2 metric of the eq. 8 fit on [0, Li] clamped at Lc, with FP64 or
+    BF16-rounded coefficients."""
+    c = fit.fit_coefficients(fn, direction, D, li)
+    if rounded:
+        return fit.table2_metric(fit.make_program(fn, direction, "bf16", D, li, lc,
+                                                  tf.from_f64(c, "bf16")))
+    from oracle.replay import evaluate_real
+    x = np.linspace(-lc, lc, 20001)
+    y = evaluate_real(ref.form_of(fn, direction), c, lc, x)
+    return float(np.max(np.abs(y - ref.function(fn, direction)(x))))
+
+
+@pytest.mark.parametrize("row", _table2_rows())
+def test_table2_least_squares_value_is_bracketed(row):
+    """At the clamp the Sollya column allows (fit interval = clamp), the
+    printed least-squares value lies between this fitter's FP64 error and its
+    BF16-rounded error: the eq. 8 fit agrees with the paper's, and the gap to
+    the printed value is coefficient rounding (tanh D4, GELU D5, sigma' D4).
+    SiLU D3's printed value falls between the FP64 errors of the grid clamps
+    4.25 and 4.5 (an off-grid clamp, like Figure 2's 5.28125); the centred
+    sigmoid's accepted program matches it to 1 %."""
+    d, name, D, form, printed = row
+    fn = gp.NAMES[name]
+    direction = ref.FWD if d == "fwd" else ref.BWD
+    lc = {r[1]: r[5] for r in _sollya_rows() if r[0] == d}[name]
+    if (d, name) == ("fwd", "sigmoid"):
+        p = gp.get(fn, direction, "bf16", D)
+        assert abs(fit.table2_metric(p) / printed - 1) <= 0.01
+    elif (d, name) == ("fwd", "silu"):
+        assert (_ls_error(fn, direction, D, 4.25, 4.25, False) < printed
+                < _ls_error(fn, direction, D, 4.5, 4.5, False))
+    else:
+        assert (_ls_error(fn, direction, D, lc, lc, False) <= printed
+                <= _ls_error(fn, direction, D, lc, lc, True))
+
+
+def test_accepted_clamps_against_the_sollya_bound():
+    """tanh D4 and sigma' D4 are accepted at the largest clamp the Sollya
+    column allows.  SiLU D3 and GELU D5 are accepted above it: every clamp
+    below the bound leaves an exact-relu tail error just above the clamp
+    (x sigma(-x), x (1 - Phi(x)), evaluated at the bound, where they are
+    smallest) larger than the accepted program's whole deployed error, so
+    the maximum-error score over [0, 12] (§3.2 step 6) with the exact tail
+    cannot select the paper's clamp -- the paper's selection weighed that
+    tail differently, which its text does not state."""
+    bound = {(r[0], r[1]): r[5] + 0.25 for r in _sollya_rows()}
+    for d, name, D in (("fwd", "tanh", 4), ("bwd", "sigmoid", 4)):
+        fn = gp.NAMES[name]
+        p = gp.get(fn, ref.FWD if d == "fwd" else ref.BWD, "bf16", D)
+        assert p.lc == bound[(d, name)] - 0.25
+    for name, D, tail in (("silu", 3, lambda x: x * ref.sigmoid(-x)),
+                          ("gelu", 5, lambda x: x * ref.Phi(-x))):
+        p = gp.get(gp.NAMES[name], ref.FWD, "bf16", D)
+        b = bound[("fwd", name)]
+        assert p.lc >= b
+        assert float(tail(np.array([b]))[0]) > p.info["deployed_score"]
 
 
 def test_figure2_configuration_is_reproduced():
