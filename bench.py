@@ -1114,9 +1114,11 @@ def l2_extras(dev, stream):
     """4,194,304-element FP16 sweep, deliberately L2-resident (no flush): the
     regime where arithmetic, not HBM, can show (Table 3, first column).
 
-    * The L2 roof: the streaming probe's rate over the same buffer sizes in
-      one long launch (l2_peak), per shape (one input: forward; two:
-      backward); l2_frac = a program's algorithmic GB/s over it.
+    * The L2 roof (l2_roof), per shape (one input: forward; two: backward):
+      the highest L2 streaming rate measured for the kernels' access
+      pattern -- the streaming probe over the same buffer sizes in one long
+      launch (l2_peak), or the one-pass probe's marginal rate from the size
+      curve below; l2_frac = a program's algorithmic GB/s over it.
     * Per program: polynomial, FP32 control, packed control, torch and the
       probe making one pass over the same bytes (same_size_copy) under the
       paper's alternating protocol, every arm a CUDA graph of 200 launches
@@ -1172,7 +1174,7 @@ def l2_extras(dev, stream):
     res["config"] = ("4,194,304 FP16 elements, x ~ N(0, 3^2), dy ~ N(0, 1); L2-resident by "
                      "design; 9 alternating rounds per program, each arm one replay of a CUDA "
                      "graph of 200 launches; median of per-round means; l2_frac against "
-                     "l2_peak (the streaming probe, 200 passes in one launch, same sizes)")
+                     "l2_roof")
     # launch time against size: intercept = fixed cost of a launch, slope = L2 streaming rate
     big = torch.empty(1 << 24, dtype=torch.float16, device=dev)
     big[:n].copy_(x)
@@ -1215,6 +1217,25 @@ def l2_extras(dev, stream):
         fit_b[arm] = {"intercept_us": a, "rate_gbs": 6 / (b * 1e-6) / 1e9 if b > 0 else None}
     res["size_curve_sigmoid_bwd"] = curve_b
     res["size_curve_fit_bwd"] = fit_b
+    # the L2 roof per shape: the highest L2 streaming rate measured for the
+    # kernels' access pattern -- the long probe launch, or (one input) the
+    # one-pass probe's marginal rate over 1-16 M elements, whichever is higher
+    # (the backward size curve leaves L2 at its largest size, so its slope is
+    # not an L2 rate)
+    roof = {"in1": max(peak["in1"]["gbs"], fit["copy"]["rate_gbs"] or 0.0),
+            "in2": peak["in2"]["gbs"]}
+    res["l2_roof"] = {
+        "fwd_gbs": roof["in1"], "bwd_gbs": roof["in2"],
+        "fwd_source": "size-curve slope of the one-pass probe"
+                      if roof["in1"] > peak["in1"]["gbs"] else "long probe launch",
+        "bwd_source": "long probe launch",
+        "note": "l2_frac = a program's algorithmic GB/s over this roof; ncu's hardware "
+                "figure (lts__t_bytes.sum.peak_sustained x L2 clock) is 36 TB/s of L2 "
+                "request bytes, of which the long probe reaches 48 %"}
+    for name, d, D in SIX:
+        e = res[f"{name}.{'bwd' if d else 'fwd'}.D{D}"]
+        e["l2_peak_gbs"] = roof["in2" if d else "in1"]
+        e["l2_frac"] = e["poly_gbs"] / e["l2_peak_gbs"]
     res["size_curve_note"] = ("least squares over 2^20..2^24 elements (4 bytes per element): "
                               "intercept = fixed cost of one launch in a graph, rate = marginal "
                               "L2 streaming rate; the arms are sigmoid D3 forward, its two MUFU "

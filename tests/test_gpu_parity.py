@@ -378,10 +378,12 @@ def _equal_bits(got, want):
 
 def test_chunk_shape_switch_sizes():
     """Sizes on both sides of the point where a one-input call changes from
-    one to two 16-byte chunks per thread (four two-chunk blocks per SM), with
-    and without an n mod 8 tail: every element against the oracle's table."""
+    one 16-byte chunk per thread (releasing the next launch after its loads)
+    to two (releasing after its stores) -- two two-chunk blocks per SM --
+    with and without an n mod 8 tail: every element against the oracle's
+    table."""
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
-    edge = 4 * sms * 256 * 2 * 8
+    edge = 2 * sms * 256 * 2 * 8
     dt = B.POLY_BF16
     op = oracle_program(B.POLY_GELU, B.POLY_FWD, dt)
     rng = np.random.default_rng(81)
@@ -392,6 +394,38 @@ def test_chunk_shape_switch_sizes():
         B.poly_act_fwd(B.POLY_GELU, dt, xd[:n], y[:n], n)
         assert _equal_bits(y[:n], _apply_lut(op, xd[:n])), n
         assert bool((y[n:].view(torch.int16) == 0x5A5A).all()), n
+
+
+def test_two_input_launch_shape_switch_sizes():
+    """Two-input calls change shape with size: one chunk per thread below one
+    two-chunk block per SM, two chunks up to 16 such blocks per SM, one above;
+    the next launch is released after the loads while the grid is resident at
+    once (at most 8 blocks per SM), after the stores beyond.  Sizes on both
+    sides of every switch, with and without a tail, for the backward program
+    and the SwiGLU forward: every element against the oracle's tables."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    per_two_chunk_block = 256 * 2 * 8
+    edges = [sms * per_two_chunk_block, 8 * sms * per_two_chunk_block,
+             16 * sms * per_two_chunk_block]
+    dt = B.POLY_F16
+    op = oracle_program(B.POLY_SIGMOID, B.POLY_BWD, dt)
+    s_op = oracle_program(B.POLY_SILU, B.POLY_FWD, dt)
+    top = edges[-1] + 8192
+    rng = np.random.default_rng(83)
+    xd = to_dev(_rand_bits(rng, top, "f16"), dt)
+    dyd = to_dev(_rand_bits(rng, top, "f16"), dt)
+    for edge in edges:
+        for n in (edge - 4096 - 3, edge - 8, edge, edge + 5, edge + 8, edge + 4096):
+            y = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+            B.poly_act_bwd(B.POLY_SIGMOID, dt, xd[:n], dyd[:n], y[:n], n)
+            assert _equal_bits(y[:n], _rn_mul(dyd[:n], _apply_lut(op, xd[:n]))), (edge, n)
+            assert bool((y[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
+            if n % 8 == 0:
+                z = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+                B.poly_swiglu_fwd(dt, xd[:n].view(n // 8, 8), dyd[:n].view(n // 8, 8),
+                                  z[:n].view(n // 8, 8))
+                assert _equal_bits(z[:n], _rn_mul(_apply_lut(s_op, xd[:n]), dyd[:n])), (edge, n)
+                assert bool((z[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
 
 
 @pytest.mark.parametrize("n", [(1 << 31) - 3, (1 << 31) + 13])
