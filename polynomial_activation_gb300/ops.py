@@ -46,29 +46,47 @@ def _rows(t):
     return t if t.dim() == 2 and t.stride(1) == 1 else t.contiguous()
 
 
-def swiglu_fwd(g, u, out=None, control: bool = False):
+def _rule(rule):
+    """The SwiGLU rule of a call: POLY_SWIGLU_DIRECT or POLY_SWIGLU_SIGMOID,
+    or None for the library's process-wide default, read now."""
+    if rule is None:
+        return B.poly_get_swiglu_variant()
+    if rule not in (B.POLY_SWIGLU_DIRECT, B.POLY_SWIGLU_SIGMOID):
+        raise ValueError(f"unknown SwiGLU rule {rule!r}")
+    return rule
+
+
+def swiglu_fwd(g, u, out=None, control: bool = False, rule=None):
+    """y = SiLU(g) * u under `rule` (None: the process default), or with the
+    FP32 MUFU control."""
     y = torch.empty(g.shape, dtype=g.dtype, device=g.device) if out is None else out
-    (B.poly_ctrl_swiglu_fwd if control else B.poly_swiglu_fwd)(_dt(g), g, u, y)
+    if control:
+        B.poly_ctrl_swiglu_fwd(_dt(g), g, u, y)
+    else:
+        B.poly_swiglu_fwd_v(_rule(rule), _dt(g), g, u, y)
     return y
 
 
-def swiglu_bwd(g, u, dy, control: bool = False):
+def swiglu_bwd(g, u, dy, control: bool = False, rule=None):
     dg = torch.empty(g.shape, dtype=g.dtype, device=g.device)
     du = torch.empty(g.shape, dtype=g.dtype, device=g.device)
-    (B.poly_ctrl_swiglu_bwd if control else B.poly_swiglu_bwd)(_dt(g), g, u, dy, dg, du)
+    if control:
+        B.poly_ctrl_swiglu_bwd(_dt(g), g, u, dy, dg, du)
+    else:
+        B.poly_swiglu_bwd_v(_rule(rule), _dt(g), g, u, dy, dg, du)
     return dg, du
 
 
-def swiglu_fwd_ragged(g, u, seg_off, out=None, status=None):
+def swiglu_fwd_ragged(g, u, seg_off, out=None, status=None, rule=None):
     y = torch.empty_like(g) if out is None else out
-    B.poly_swiglu_fwd_ragged(_dt(g), g, u, y, seg_off, status=status)
+    B.poly_swiglu_fwd_ragged_v(_rule(rule), _dt(g), g, u, y, seg_off, status=status)
     return y
 
 
-def swiglu_bwd_ragged(g, u, dy, seg_off, dg=None, du=None, status=None):
+def swiglu_bwd_ragged(g, u, dy, seg_off, dg=None, du=None, status=None, rule=None):
     dg = torch.empty_like(g) if dg is None else dg
     du = torch.empty_like(g) if du is None else du
-    B.poly_swiglu_bwd_ragged(_dt(g), g, u, dy, dg, du, seg_off, status=status)
+    B.poly_swiglu_bwd_ragged_v(_rule(rule), _dt(g), g, u, dy, dg, du, seg_off, status=status)
     return dg, du
 
 
@@ -120,18 +138,20 @@ def gelu(x):
 
 
 class PolySwiGLU(torch.autograd.Function):
-    """y = SiLU(g) * u with the library's current SwiGLU rule."""
+    """y = SiLU(g) * u under a SwiGLU rule fixed at forward time (the
+    backward uses the same rule whatever the process default is by then)."""
 
     @staticmethod
-    def forward(ctx, g, u):
+    def forward(ctx, g, u, rule=None):
         g, u = _rows(g), _rows(u)
         ctx.save_for_backward(g, u)
-        return swiglu_fwd(g, u)
+        ctx.rule = _rule(rule)
+        return swiglu_fwd(g, u, rule=ctx.rule)
 
     @staticmethod
     def backward(ctx, dy):
         g, u = ctx.saved_tensors
-        return swiglu_bwd(g, u, _rows(dy))
+        return swiglu_bwd(g, u, _rows(dy), rule=ctx.rule) + (None,)
 
 
 def _fused_base(g, u):
@@ -160,16 +180,19 @@ def _fused_base(g, u):
     return b
 
 
-def swiglu(g, u):
-    """SiLU(g) * u.  When g and u are the two halves of one fused gate-up
+def swiglu(g, u, rule=None):
+    """SiLU(g) * u under `rule` (POLY_SWIGLU_DIRECT, POLY_SWIGLU_SIGMOID, or
+    None for the process default at the time of the call; the backward
+    keeps that rule).  When g and u are the two halves of one fused gate-up
     buffer (gu.chunk(2, dim=-1)), the recorded path runs on that buffer so
     that the backward writes one [..., 2H] gradient (see swiglu_packed)."""
+    rule = _rule(rule)
     if not _grad(g, u):
-        return swiglu_fwd(_rows(g), _rows(u))
+        return swiglu_fwd(_rows(g), _rows(u), rule=rule)
     b = _fused_base(g, u)
     if b is not None:
-        return PolySwiGLUPacked.apply(b).view(g.shape)
-    return PolySwiGLU.apply(g, u)
+        return PolySwiGLUPacked.apply(b, rule).view(g.shape)
+    return PolySwiGLU.apply(g, u, rule)
 
 
 def _halves(gu):
@@ -182,10 +205,10 @@ def _halves(gu):
     return gu2, gu2[:, :h], gu2[:, h:]
 
 
-def _packed_fwd(gu):
+def _packed_fwd(gu, rule):
     gu2, g, u = _halves(gu)
     y = torch.empty((gu2.shape[0], g.shape[1]), dtype=gu.dtype, device=gu.device)
-    B.poly_swiglu_fwd(_dt(gu), g, u, y)
+    B.poly_swiglu_fwd_v(rule, _dt(gu), g, u, y)
     return y.view(*gu.shape[:-1], g.shape[1])
 
 
@@ -196,9 +219,10 @@ class PolySwiGLUPacked(torch.autograd.Function):
     no slice gradients are assembled afterwards."""
 
     @staticmethod
-    def forward(ctx, gu):
+    def forward(ctx, gu, rule=None):
         ctx.save_for_backward(gu)
-        return _packed_fwd(gu)
+        ctx.rule = _rule(rule)
+        return _packed_fwd(gu, ctx.rule)
 
     @staticmethod
     def backward(ctx, dy):
@@ -206,13 +230,16 @@ class PolySwiGLUPacked(torch.autograd.Function):
         gu2, g, u = _halves(gu)
         h = g.shape[1]
         dgu = torch.empty((gu2.shape[0], 2 * h), dtype=gu.dtype, device=gu.device)
-        B.poly_swiglu_bwd(_dt(gu), g, u, _dense(dy).view(-1, h), dgu[:, :h], dgu[:, h:])
-        return dgu.view(gu.shape)
+        B.poly_swiglu_bwd_v(ctx.rule, _dt(gu), g, u, _dense(dy).view(-1, h), dgu[:, :h],
+                            dgu[:, h:])
+        return dgu.view(gu.shape), None
 
 
-def swiglu_packed(gu):
-    """SwiGLU of a fused gate-up buffer [..., 2H] -> [..., H]."""
-    return PolySwiGLUPacked.apply(gu) if _grad(gu) else _packed_fwd(gu)
+def swiglu_packed(gu, rule=None):
+    """SwiGLU of a fused gate-up buffer [..., 2H] -> [..., H] under `rule`
+    (None: the process default at the time of the call)."""
+    rule = _rule(rule)
+    return PolySwiGLUPacked.apply(gu, rule) if _grad(gu) else _packed_fwd(gu, rule)
 
 
 class PolySwiGLURagged(torch.autograd.Function):
@@ -224,30 +251,31 @@ class PolySwiGLURagged(torch.autograd.Function):
     and the zeroing launch is skipped."""
 
     @staticmethod
-    def forward(ctx, g, u, seg_off, padding_free):
+    def forward(ctx, g, u, seg_off, padding_free, rule=None):
         g, u = _dense(g), _dense(u)
         ctx.save_for_backward(g, u, seg_off)
         ctx.padding_free = padding_free
-        return _ragged_fwd(g, u, seg_off, padding_free)
+        ctx.rule = _rule(rule)
+        return _ragged_fwd(g, u, seg_off, padding_free, ctx.rule)
 
     @staticmethod
     def backward(ctx, dy):
         g, u, seg_off = ctx.saved_tensors
-        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off)
+        dg, du = swiglu_bwd_ragged(g, u, _dense(dy), seg_off, rule=ctx.rule)
         if not ctx.padding_free:
             B.poly_ragged_zero_outside(dg, seg_off)
             B.poly_ragged_zero_outside(du, seg_off)
-        return dg, du, None, None
+        return dg, du, None, None, None
 
 
-def _ragged_fwd(g, u, seg_off, padding_free=False):
-    y = swiglu_fwd_ragged(g, u, seg_off)
+def _ragged_fwd(g, u, seg_off, padding_free=False, rule=None):
+    y = swiglu_fwd_ragged(g, u, seg_off, rule=rule)
     if not padding_free:
         B.poly_ragged_zero_outside(y, seg_off)
     return y
 
 
-def swiglu_ragged(g, u, seg_off, padding_free: bool = False):
+def swiglu_ragged(g, u, seg_off, padding_free: bool = False, rule=None):
     """Rows outside [seg_off[0], seg_off[E]) of the output (and of the
     gradients) are zero: one extra launch zeroes them on the device, writing
     nothing when the segments cover every row.  padding_free=True (seg_off[0]
@@ -256,9 +284,10 @@ def swiglu_ragged(g, u, seg_off, padding_free: bool = False):
     padding-free call covers every row, so it computes exactly what swiglu
     does; for gate and up halves of one fused [rows, 2H] buffer, which the
     ragged calls do not take, use swiglu or swiglu_packed.)"""
+    rule = _rule(rule)
     if _grad(g, u):
-        return PolySwiGLURagged.apply(g, u, seg_off, padding_free)
-    return _ragged_fwd(_dense(g), _dense(u), seg_off, padding_free)
+        return PolySwiGLURagged.apply(g, u, seg_off, padding_free, rule)
+    return _ragged_fwd(_dense(g), _dense(u), seg_off, padding_free, rule)
 
 
 class PolySoftcap(torch.autograd.Function):

@@ -344,3 +344,48 @@ def test_stream_peak_probe_l2_passes(inflight):
     for _ in range(3):
         B.poly_diag_stream_peak(2, a, b, out, n, reps=200, inflight=inflight)
     assert torch.equal(out, a ^ b)
+
+
+@pytest.mark.parametrize("rule", [B.POLY_SWIGLU_DIRECT, B.POLY_SWIGLU_SIGMOID])
+def test_autograd_swiglu_keeps_its_rule(rule):
+    """ops.swiglu / swiglu_packed / swiglu_ragged fix the SwiGLU rule when the
+    forward runs: with the process default switched to the other rule before
+    backward(), the gradients are still the chosen rule's, bit for bit."""
+    from polynomial_activation_gb300 import ops
+    dt, fmt = B.POLY_BF16, "bf16"
+    rng = np.random.default_rng(90 + rule)
+    rows, h = 64, 264
+    g = _rand_bits(rng, rows * h, fmt).reshape(rows, h)
+    u = _rand_bits(rng, rows * h, fmt).reshape(rows, h)
+    dy = _rand_bits(rng, rows * h, fmt).reshape(rows, h)
+    wy, wdg, wdu = _want(rule, dt, g, u, dy)
+    dyd = to_dev(dy, dt).view(rows, h)
+    try:
+        for mode in ("pair", "packed", "chunked", "ragged"):
+            B.poly_set_swiglu_variant(_other(rule))
+            if mode == "pair":
+                gd = to_dev(g, dt).view(rows, h).requires_grad_(True)
+                ud = to_dev(u, dt).view(rows, h).requires_grad_(True)
+                y = ops.swiglu(gd, ud, rule=rule)
+            elif mode == "ragged":
+                gd = to_dev(g, dt).view(rows, h).requires_grad_(True)
+                ud = to_dev(u, dt).view(rows, h).requires_grad_(True)
+                seg = torch.tensor([0, 20, rows], dtype=torch.int32, device=DEV)
+                y = ops.swiglu_ragged(gd, ud, seg, rule=rule)
+            else:
+                gu = torch.cat([to_dev(g, dt).view(rows, h), to_dev(u, dt).view(rows, h)],
+                               dim=1).requires_grad_(True)
+                y = (ops.swiglu_packed(gu, rule=rule) if mode == "packed"
+                     else ops.swiglu(*gu.chunk(2, dim=-1), rule=rule))
+            B.poly_set_swiglu_variant(rule)       # flip the default between fwd and bwd
+            B.poly_set_swiglu_variant(_other(rule))
+            y.backward(dyd)
+            assert np.array_equal(from_dev(y.detach()).reshape(rows, h), wy), mode
+            if mode in ("pair", "ragged"):
+                dg, du = gd.grad, ud.grad
+            else:
+                dg, du = gu.grad[:, :h], gu.grad[:, h:]
+            assert np.array_equal(from_dev(dg).reshape(rows, h), wdg), mode
+            assert np.array_equal(from_dev(du).reshape(rows, h), wdu), mode
+    finally:
+        B.poly_set_swiglu_variant(B.POLY_SWIGLU_DIRECT)

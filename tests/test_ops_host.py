@@ -62,3 +62,11 @@ def test_fused_base_detection():
     assert ops._fused_base(g, u) is None                        # views made without grad
     t = torch.zeros(10, 6, dtype=torch.float16, requires_grad=True).t()
     assert ops._fused_base(*t.chunk(2, dim=-1)) is None         # buffer not row-major
+
+
+def test_unknown_swiglu_rule_is_refused():
+    g = torch.zeros(8, 8, dtype=torch.bfloat16)
+    for f in (lambda: ops.swiglu(g, g, rule=7), lambda: ops.swiglu_packed(g, rule=-1),
+              lambda: ops.swiglu_ragged(g, g, torch.zeros(2, dtype=torch.int32), rule=2)):
+        with pytest.raises(ValueError, match="rule"):
+            f()
