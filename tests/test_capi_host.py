@@ -464,3 +464,23 @@ def test_rope_rejects_bad_arguments(L):
     assert L.poly_rope_bwd(*args(b=-1)) == B.POLY_EINVAL
     assert L.poly_rope_fwd(*args(b=0)) == B.POLY_OK
     assert L.poly_rope_fwd(*args(hq=0, hkv=0)) == B.POLY_OK
+
+
+def test_packed_control_constants_are_the_nearest_values():
+    """The packed MUFU control's constants (csrc/kern_ctrl.cu, PkConst) are the
+    FP16 / BF16 values nearest to 1, sqrt(2/pi), 0.044715 sqrt(2/pi),
+    3 x 0.044715 sqrt(2/pi) and 16, duplicated in both lanes."""
+    import math
+    import torch
+    src = open(os.path.join(ROOT, "polynomial_activation_gb300", "csrc", "kern_ctrl.cu")).read()
+    body = src[src.index("struct PkConst"):src.index("};", src.index("struct PkConst"))]
+    k = math.sqrt(2.0 / math.pi)
+    want = {"one": 1.0, "k": k, "kc": k * 0.044715, "k3c": 3.0 * k * 0.044715, "sixteen": 16.0}
+    for name, value in want.items():
+        m = re.search(r"\b%s = DT == kF16 \? 0x([0-9A-F]{8})u : 0x([0-9A-F]{8})u;" % name, body)
+        assert m, name
+        f16 = int(np.array([value], np.float16).view(np.uint16)[0])
+        bf16 = int(torch.tensor([value], dtype=torch.float64).to(torch.bfloat16)
+                   .view(torch.int16).item()) & 0xFFFF
+        assert int(m.group(1), 16) == f16 * 0x00010001, name
+        assert int(m.group(2), 16) == bf16 * 0x00010001, name
