@@ -484,3 +484,23 @@ def test_packed_control_constants_are_the_nearest_values():
                    .view(torch.int16).item()) & 0xFFFF
         assert int(m.group(1), 16) == f16 * 0x00010001, name
         assert int(m.group(2), 16) == bf16 * 0x00010001, name
+
+
+def test_fitted_programs_pass_the_clamp_check(L):
+    """Whatever the search options (a clamp step the target format cannot
+    represent, clamps refined by ulps, a narrow fit-interval range), the
+    fitter's programs carry lc equal to their clamp's exact value and
+    Lc <= Li + 1, so poly_set_program accepts them."""
+    try:
+        for dt in (B.POLY_F16, B.POLY_BF16):
+            o = B.poly_fit_defaults()
+            o.li_min, o.li_max, o.li_step = 2.0, 6.0, 0.5
+            o.lc_min, o.lc_step = 1.05, 0.1
+            o.lc_refine_ulps = 2
+            p = B.poly_fit(B.POLY_SIGMOID, B.POLY_FWD, dt, 3, o)
+            assert p.lc <= p.li + 1.0
+            assert L.poly_set_program(ctypes.byref(p)) == B.POLY_OK
+            d = B.poly_derive_program(p)
+            assert L.poly_set_program(ctypes.byref(d)) == B.POLY_OK
+    finally:
+        B.poly_reset_programs()
