@@ -428,6 +428,78 @@ def test_two_input_launch_shape_switch_sizes():
                 assert bool((z[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
 
 
+def test_random_sizes_offsets_and_families():
+    """Sixty random calls: sizes log-uniform over 1..2^24 elements (across
+    every launch-shape and release switch), inputs and output at independent
+    element offsets 0..7 (same or different alignment, so dense, head / tail
+    and scalar paths all run), both formats, every program, the activation
+    forward and backward and the flat SwiGLU forward and backward under both
+    rules: every element against the oracle's exhaustive tables, guard
+    bands around every output intact."""
+    rng = np.random.default_rng(2024)
+    G = 64
+    top = (1 << 24) + 16
+    pools = {}
+    for dt in DTS:
+        fmt = FMT[dt]
+        pools[dt] = [to_dev(_rand_bits(rng, top, fmt), dt) for _ in range(3)]
+    for case in range(60):
+        dt = DTS[case % 2]
+        n = int(np.exp(rng.uniform(0.0, np.log(1 << 24))))
+        offs = [int(o) for o in rng.integers(0, 8, 4)]
+        kind = ("fwd", "bwd", "swiglu_fwd", "swiglu_bwd")[int(rng.integers(0, 4))]
+        a, b, c = (pools[dt][k][offs[k]:offs[k] + n] for k in range(3))
+        outs = []
+
+        def out_buf():
+            buf = torch.full((n + 2 * G + 8,), 0x5A5A, dtype=torch.int16, device=DEV)
+            buf = buf.view(TDT[dt])
+            outs.append(buf)
+            return buf[G + offs[3]:G + offs[3] + n]
+
+        if kind in ("fwd", "bwd"):
+            fn = int(rng.integers(0, 4))
+            d = B.POLY_FWD if kind == "fwd" else B.POLY_BWD
+            op = oracle_program(fn, d, dt)
+            y = out_buf()
+            if d == B.POLY_FWD:
+                B.poly_act_fwd(fn, dt, a, y, n)
+                want = _apply_lut(op, a)
+            else:
+                B.poly_act_bwd(fn, dt, a, b, y, n)
+                want = _rn_mul(b, _apply_lut(op, a))
+            assert _equal_bits(y, want), (case, kind, fn, dt, n, offs)
+        else:
+            rule = int(rng.integers(0, 2))
+            if rule == B.POLY_SWIGLU_DIRECT:
+                s_lut = lambda t: _apply_lut(oracle_program(B.POLY_SILU, B.POLY_FWD, dt), t)
+                d_lut = lambda t: _apply_lut(oracle_program(B.POLY_SILU, B.POLY_BWD, dt), t)
+            else:
+                sig = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+                s_lut = lambda t: _rn_mul(t, _apply_lut(sig, t))
+                d_lut = None
+            if kind == "swiglu_fwd":
+                y = out_buf()
+                B.poly_swiglu_fwd_v(rule, dt, a, b, y, 1, n, n, n, n)
+                assert _equal_bits(y, _rn_mul(s_lut(a), b)), (case, kind, rule, dt, n, offs)
+            else:
+                dg, du = out_buf(), out_buf()
+                B.poly_swiglu_bwd_v(rule, dt, a, b, c, dg, du, 1, n, n, n, n, n, n)
+                if d_lut is not None:
+                    assert _equal_bits(dg, _rn_mul(_rn_mul(c, b), d_lut(a))), (case, rule, n, offs)
+                else:   # fused s' = fma(g, fma(-p, p, p), p): the oracle on a sample
+                    from oracle.replay import swiglu_sigmoid_backward
+                    k = torch.from_numpy(np.unique(rng.integers(0, n, min(n, 4096)))).to(DEV)
+                    host = [from_dev(t[k]) for t in (a, b, c)]
+                    wdg, _ = swiglu_sigmoid_backward(sig, *host)
+                    assert np.array_equal(from_dev(dg[k]), wdg), (case, rule, n, offs)
+                assert _equal_bits(du, _rn_mul(c, s_lut(a))), (case, rule, n, offs)
+        for buf in outs:
+            g = buf.view(torch.int16)
+            assert bool((g[:G + offs[3]] == 0x5A5A).all()), (case, kind, n, offs)
+            assert bool((g[G + offs[3] + n:] == 0x5A5A).all()), (case, kind, n, offs)
+
+
 @pytest.mark.parametrize("n", [(1 << 31) - 3, (1 << 31) + 13])
 def test_index_width_limits(n):
     """Just below 2^31 elements (the dense kernel's 32-bit indices at their
