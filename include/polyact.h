@@ -377,9 +377,10 @@ int poly_rope_programs(uint16_t *sin_coef, uint16_t *cos_coef);
  * Phi + x phi, all recomputed from x.  One rounding to the target format.
  *
  * POLY_CTRL_PACKED (the _v calls): packed two-lane arithmetic in the target
- * format with one tanh.approx.{f16x2,bf16x2} per pair (GB300's
- * special-function unit is twice GB200's, Approximating Softmax in
- * Pretrained LLMs, Appendix B.5): tanh = tanh.approx(x); sigmoid =
+ * format with one tanh.approx.{f16x2,bf16x2} instruction per pair -- one
+ * special-function operation per element, against two for the FP32 control's
+ * sigmoid and SiLU (GB300's special-function unit is twice GB200's,
+ * Approximating Softmax in Pretrained LLMs, Appendix B.5): tanh = tanh.approx(x); sigmoid =
  * fma(t, 1/2, 1/2), t = tanh.approx(x * 1/2); SiLU = fma(h, t, h) with
  * h = x * 1/2, t = tanh.approx(h); GELU in the tanh form h (1 + tanh(z)),
  * z = x (k + k c x^2), k = sqrt(2/pi), c = 0.044715 (within 4.8e-4 of exact

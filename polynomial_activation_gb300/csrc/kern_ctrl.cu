@@ -16,8 +16,10 @@
 // Phi + x phi.  One rounding to the target format at the end.
 //
 // Packed (POLY_CTRL_PACKED): every operation on a packed pair in the target
-// format, one special-function issue (tanh.approx.{f16x2,bf16x2}) per pair,
-// through the identities sigma(x) = 1/2 + tanh(x/2)/2 and
+// format, one tanh.approx.{f16x2,bf16x2} instruction per pair (which the
+// special-function unit executes as one operation per element: ncu counts one
+// special-function instruction per element, half the FP32 control's two for
+// sigmoid and SiLU), through the identities sigma(x) = 1/2 + tanh(x/2)/2 and
 // SiLU(x) = h + h tanh(h), h = x/2:
 //   tanh     t = tanh(x)
 //   sigmoid  t = tanh(x * 1/2);  y = fma(t, 1/2, 1/2)
