@@ -33,7 +33,9 @@
  * - Tensors hold 16-bit elements (FP16 or BF16 bit patterns), contiguous
  *   unless leading dimensions are given.  Any 2-byte alignment is accepted:
  *   16-byte-aligned data takes the 128-bit vector path, a scalar head and
- *   tail cover the rest.  Odd addresses -> POLY_EINVAL.  Exceptions, stated
+ *   tail cover the rest, and inputs that sit at other addresses modulo 16
+ *   than the output are realigned in registers (still 16-byte accesses).
+ *   Odd addresses -> POLY_EINVAL.  Exceptions, stated
  *   at each call: poly_exp2 works on FP32 (4-byte aligned), the RoPE calls
  *   on FP16 with 16-byte-aligned tensors.
  * - n == 0 (or rows == 0 / cols == 0) is a valid no-op: POLY_OK, no launch.

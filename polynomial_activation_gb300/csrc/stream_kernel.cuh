@@ -17,8 +17,10 @@
 //    while the previous kernel on the stream drains;
 //  * a scalar head (up to the first 16-byte boundary) and tail, evaluated
 //    with the same packed instructions on one lane so that every element
-//    gets bit-identical arithmetic; streams whose addresses disagree modulo
-//    16 bytes take the scalar path throughout.
+//    gets bit-identical arithmetic; inputs whose addresses disagree with the
+//    output's modulo 16 bytes are realigned in registers (two aligned
+//    16-byte loads and funnel shifts per chunk), and only layouts whose
+//    outputs disagree with each other take the scalar path throughout.
 // An operation ("Op") supplies NIN input streams, NOUT output streams and a
 // function from NIN packed pairs to NOUT packed pairs.
 #pragma once
@@ -191,6 +193,103 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(Streams s, Layout l,
       if (i < nvec) {
         uint4 o[Op::NOUT];
         apply_chunk<Op>(r[u], o, p);
+#pragma unroll
+        for (int k = 0; k < Op::NOUT; ++k) st_stream(out[k] + head + (i << 3), o[k]);
+      }
+    }
+  }
+  const int64_t ntail = n - body_end;
+#pragma unroll 1
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < head + ntail;
+       i += (int64_t)gridDim.x * kThreads) {
+    const int64_t e = i < head ? i : body_end + (i - head);
+    apply_one<Op>(in, out, e, p);
+  }
+  pdl_release();
+}
+
+// Bytes m .. m + 15 (m even, 0..14) of the 32-byte window lo:hi, little
+// endian: the 16-byte chunk that starts m bytes into an aligned window.
+__device__ __forceinline__ uint4 realign16(const uint4 &lo, const uint4 &hi, uint32_t m) {
+  const uint32_t sh = (m & 3u) * 8u;
+  uint32_t w0, w1, w2, w3, w4;
+  switch (m >> 2) {
+    case 0: w0 = lo.x; w1 = lo.y; w2 = lo.z; w3 = lo.w; w4 = hi.x; break;
+    case 1: w0 = lo.y; w1 = lo.z; w2 = lo.w; w3 = hi.x; w4 = hi.y; break;
+    case 2: w0 = lo.z; w1 = lo.w; w2 = hi.x; w3 = hi.y; w4 = hi.z; break;
+    default: w0 = lo.w; w1 = hi.x; w2 = hi.y; w3 = hi.z; w4 = hi.w; break;
+  }
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
+// Flat / ragged calls whose inputs sit at other addresses modulo 16 than
+// the output (a view that starts at an odd element, say), all outputs alike:
+// the output moves in aligned 16-byte chunks, and each input chunk is
+// assembled from the two aligned 16-byte chunks that straddle it, shifted by
+// that input's constant byte offset -- every access stays a 16-byte access
+// instead of falling back to one element per load.  The first and the last
+// output chunks take the scalar path with the head and tail, so that no
+// window reaches outside an input: chunk i reads input bytes from
+// floor16(start + 2 (head + 8 i)) >= start + 2 (head - 7) > start (head >= 8)
+// to at most start + 2 (head + 8 (i + 2)) <= start + 2 n (i <= nvec - 2 of
+// the whole chunks).
+template <class Op>
+__global__ void __launch_bounds__(kThreads) realign_kernel(Streams s, Layout l,
+                                                           typename Op::Params p) {
+  pdl_wait();
+  constexpr int U = chunks_per_thread<Op>();
+  int64_t n = l.n, off = 0;
+  if (l.mode == kRagged) {
+    int64_t lo, hi;
+    ragged_rows(l.seg, l.nseg, l.cap_rows, l.status, lo, hi);
+    off = lo * l.cols;
+    n = (hi - lo) * l.cols;
+  }
+  const uint16_t *in[Op::NIN];
+  const uint16_t *src[3] = {s.in0, s.in1, s.in2};
+#pragma unroll
+  for (int k = 0; k < Op::NIN; ++k) in[k] = src[k] + off;
+  uint16_t *out[Op::NOUT];
+  uint16_t *dst[2] = {s.out0, s.out1};
+#pragma unroll
+  for (int k = 0; k < Op::NOUT; ++k) out[k] = dst[k] + off;
+
+  const uintptr_t ao = reinterpret_cast<uintptr_t>(out[0]);
+  int64_t head = (int64_t)(((16u - (ao & 15u)) & 15u) >> 1) + 8;
+  if (head > n) head = n;
+  int64_t nvec = ((n - head) >> 3) - 1;
+  if (nvec < 0) nvec = 0;
+  const int64_t body_end = head + (nvec << 3);
+  uint32_t m[Op::NIN];
+#pragma unroll
+  for (int k = 0; k < Op::NIN; ++k)
+    m[k] = (uint32_t)(reinterpret_cast<uintptr_t>(in[k] + head) & 15u);
+#pragma unroll 1
+  for (int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x; base < nvec;
+       base += (int64_t)gridDim.x * (kThreads * U)) {
+    uint4 lo[U][Op::NIN], hi[U][Op::NIN];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + u * kThreads;
+      if (i < nvec) {
+#pragma unroll
+        for (int k = 0; k < Op::NIN; ++k) {
+          const uintptr_t a =
+              reinterpret_cast<uintptr_t>(in[k] + head + (i << 3)) & ~uintptr_t(15);
+          lo[u][k] = ld_stream(reinterpret_cast<const uint16_t *>(a));
+          hi[u][k] = m[k] ? ld_stream(reinterpret_cast<const uint16_t *>(a + 16)) : lo[u][k];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + u * kThreads;
+      if (i < nvec) {
+        uint4 x[Op::NIN], o[Op::NOUT];
+#pragma unroll
+        for (int k = 0; k < Op::NIN; ++k) x[k] = realign16(lo[u][k], hi[u][k], m[k]);
+        apply_chunk<Op>(x, o, p);
 #pragma unroll
         for (int k = 0; k < Op::NOUT; ++k) st_stream(out[k] + head + (i << 3), o[k]);
       }
@@ -454,6 +553,13 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
     return launch_dense<Op, kDenseRagged, U>(blocks, stream, s, a, p);
+  }
+  // streams that disagree modulo 16 while the outputs agree: realigned
+  // 16-byte accesses instead of one element per load
+  if (!l.vec && (Op::NOUT == 1 || ((reinterpret_cast<uintptr_t>(s.out0) ^
+                                    reinterpret_cast<uintptr_t>(s.out1)) & 15u) == 0)) {
+    const int64_t blocks = grid_for(l, 8 * chunks_per_thread<Op>());
+    return launch_pdl(realign_kernel<Op>, blocks, kThreads, stream, s, l, p);
   }
   const int64_t blocks = grid_for(l, l.vec ? 8 * chunks_per_thread<Op>() : 1);
   return launch_pdl(stream_kernel<Op>, blocks, kThreads, stream, s, l, p);

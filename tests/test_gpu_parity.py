@@ -428,6 +428,47 @@ def test_two_input_launch_shape_switch_sizes():
                 assert bool((z[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
 
 
+@pytest.mark.parametrize("dt", DTS)
+def test_realigned_inputs_every_offset_pair(dt):
+    """Inputs at other addresses modulo 16 bytes than the output take the
+    realigning kernel (two aligned 16-byte loads and a funnel shift per
+    chunk; its first and last chunks and the head and tail scalar): every
+    pair of input / output element offsets 0..7, the second input at yet
+    another offset, sizes around the head, body and tail boundaries -- every
+    element against the oracle's tables, guard bands intact."""
+    fmt = FMT[dt]
+    rng = np.random.default_rng(71)
+    op_f = oracle_program(B.POLY_GELU, B.POLY_FWD, dt)
+    op_b = oracle_program(B.POLY_TANH, B.POLY_BWD, dt)
+    s_op = oracle_program(B.POLY_SILU, B.POLY_FWD, dt)
+    top = 8192
+    xs = to_dev(_rand_bits(rng, top, fmt), dt)
+    ds = to_dev(_rand_bits(rng, top, fmt), dt)
+    G = 32
+    for n in (1, 7, 8, 9, 15, 16, 17, 23, 24, 25, 31, 32, 33, 40, 41, 1000, 4099):
+        for ox in range(8):
+            for oy in range(8):
+                od = (ox + 3 + oy) % 8
+                x, dy = xs[ox:ox + n], ds[od:od + n]
+                for kind in ("fwd", "bwd", "swiglu"):
+                    buf = torch.full((n + 2 * G + 8,), 0x5A5A, dtype=torch.int16, device=DEV)
+                    buf = buf.view(TDT[dt])
+                    y = buf[G + oy:G + oy + n]
+                    if kind == "fwd":
+                        B.poly_act_fwd(B.POLY_GELU, dt, x, y, n)
+                        want = _apply_lut(op_f, x)
+                    elif kind == "bwd":
+                        B.poly_act_bwd(B.POLY_TANH, dt, x, dy, y, n)
+                        want = _rn_mul(dy, _apply_lut(op_b, x))
+                    else:
+                        B.poly_swiglu_fwd_v(B.POLY_SWIGLU_DIRECT, dt, x, dy, y, 1, n, n, n, n)
+                        want = _rn_mul(_apply_lut(s_op, x), dy)
+                    assert _equal_bits(y, want), (kind, n, ox, oy, od)
+                    g = buf.view(torch.int16)
+                    assert bool((g[:G + oy] == 0x5A5A).all() and
+                                (g[G + oy + n:] == 0x5A5A).all()), (kind, n, ox, oy, od)
+
+
 def test_random_sizes_offsets_and_families():
     """Sixty random calls: sizes log-uniform over 1..2^24 elements (across
     every launch-shape and release switch), inputs and output at independent
