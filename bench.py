@@ -561,6 +561,31 @@ def main():
                                    "per-round means, min/max kept; speedup_vs_ctrl against the "
                                    "faster control")
 
+    # ---- the two backward rows Table 3 lost in extraction (SiLU' and GELU'
+    # D4, the centred derivative fits), same protocol, against PyTorch's fused
+    # backward kernels from x (the paper quotes GELU backward at 1.615x native
+    # on HBM)
+    if not args.no_extras:
+        extra = {}
+        for name in ("silu", "gelu"):
+            fn = FN[name]
+            arms = {"poly": lambda fn=fn: B.poly_act_bwd(fn, B.POLY_F16, x, dy, outs[0], n),
+                    "ctrl_fp32": lambda fn=fn: B.poly_ctrl_act_bwd_v(B.POLY_CTRL_FP32, fn,
+                                                                      B.POLY_F16, x, dy, outs[0], n),
+                    "ctrl_packed": lambda fn=fn: B.poly_ctrl_act_bwd_v(B.POLY_CTRL_PACKED, fn,
+                                                                        B.POLY_F16, x, dy, outs[0], n),
+                    "torch": (lambda: torch.ops.aten.silu_backward(dy, x)) if name == "silu"
+                             else (lambda: torch.ops.aten.gelu_backward(dy, x))}
+            t = alternating(arms, stream, rounds=9, reps=20, warm=10)
+            pm = t["poly"]["ms"]
+            best = min(("ctrl_fp32", "ctrl_packed"), key=lambda k: t[k]["ms"])
+            extra[f"{name}.bwd.D4"] = {
+                "poly_ms": pm, "poly_gbs": 6 * n / pm / 1e6, "poly_frac": 6 * n / pm / 1e6 / peak,
+                "ctrl_fp32_ms": t["ctrl_fp32"]["ms"], "ctrl_packed_ms": t["ctrl_packed"]["ms"],
+                "torch_native_ms": t["torch"]["ms"], "best_ctrl": best,
+                "speedup_vs_ctrl": t[best]["ms"] / pm, "speedup_vs_torch": t["torch"]["ms"] / pm}
+        result["programs_lost_rows"] = extra
+
     # ---- roofline of the dominant kernel
     name, d, D = SIX[dom]
     kkey = f"{name}.{'bwd' if d else 'fwd'}.D{D}"
