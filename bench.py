@@ -1196,6 +1196,27 @@ def l2_extras(dev, stream):
                     "l2_frac": gbs / peak[f"in{nin}"]["gbs"],
                     "rounds": {k: {"median_us": v["ms"] * 1e3, "min_us": v["min_ms"] * 1e3,
                                    "max_us": v["max_ms"] * 1e3} for k, v in t.items()}}
+    # the backward rows Table 3 lost (SiLU', GELU' D4; the paper's L2 maximum,
+    # 2.193x against PyTorch, belongs to one of them)
+    lost = {}
+    for name in ("silu", "gelu"):
+        fn = FN[name]
+        t = alternating({
+            "poly": lambda fn=fn: B.poly_act_bwd(fn, f16, x, dy, y, n),
+            "ctrl_fp32": lambda fn=fn: B.poly_ctrl_act_bwd_v(0, fn, f16, x, dy, y, n),
+            "ctrl_packed": lambda fn=fn: B.poly_ctrl_act_bwd_v(1, fn, f16, x, dy, y, n),
+            "torch": (lambda: torch.ops.aten.silu_backward(dy, x)) if name == "silu"
+                     else (lambda: torch.ops.aten.gelu_backward(dy, x))},
+            stream, rounds=9, reps=200, warm=20, graph=True)
+        tp = t["poly"]["ms"]
+        best = min(("ctrl_fp32", "ctrl_packed"), key=lambda k: t[k]["ms"])
+        lost[f"{name}.bwd.D4"] = {
+            "poly_us": tp * 1e3, "ctrl_fp32_us": t["ctrl_fp32"]["ms"] * 1e3,
+            "ctrl_packed_us": t["ctrl_packed"]["ms"] * 1e3,
+            "torch_native_us": t["torch"]["ms"] * 1e3, "best_ctrl": best,
+            "speedup_vs_ctrl": t[best]["ms"] / tp, "speedup_vs_torch": t["torch"]["ms"] / tp,
+            "poly_gbs": 6 * n / tp / 1e6}
+    res["lost_rows"] = lost
     res["config"] = ("4,194,304 FP16 elements, x ~ N(0, 3^2), dy ~ N(0, 1); L2-resident by "
                      "design; 9 alternating rounds per program, each arm one replay of a CUDA "
                      "graph of 200 launches; median of per-round means; l2_frac against "
@@ -1261,6 +1282,8 @@ def l2_extras(dev, stream):
         e = res[f"{name}.{'bwd' if d else 'fwd'}.D{D}"]
         e["l2_peak_gbs"] = roof["in2" if d else "in1"]
         e["l2_frac"] = e["poly_gbs"] / e["l2_peak_gbs"]
+    for e in res["lost_rows"].values():
+        e["l2_frac"] = e["poly_gbs"] / roof["in2"]
     res["size_curve_note"] = ("least squares over 2^20..2^24 elements (4 bytes per element): "
                               "intercept = fixed cost of one launch in a graph, rate = marginal "
                               "L2 streaming rate; the arms are sigmoid D3 forward, its two MUFU "
