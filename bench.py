@@ -97,6 +97,19 @@ def recorded_traffic(kernel_key):
     return None
 
 
+def recorded_dram_peak():
+    """ncu's DRAM peak for this GPU (GB/s) from the committed summary, or None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 2 and parts[0] == "dram_peak_gbs":
+                return float(parts[1])
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every `period_ms`, each
     stamped on arrival.  start() returns once sampling is running; stop()
@@ -601,6 +614,9 @@ def main():
                           "share_of_step": per_ms[dom] / sum(per_ms),
                           "above_peak": ach > peak,
                           "achieved_back_to_back": b2b, "frac_back_to_back": b2b / peak,
+                          "dram_peak_gbs": recorded_dram_peak(),
+                          "frac_vs_dram_peak": (ach / recorded_dram_peak()
+                                                if recorded_dram_peak() else None),
                           "same_shape_stream_gbs": stream_gbs,
                           "same_shape_stream_by_inflight": stream_rates,
                           "frac_vs_same_shape_stream": ach / stream_gbs,
@@ -611,7 +627,8 @@ def main():
                                   "the timed calls; peak: a torch copy_, which a streaming kernel "
                                   "can exceed; same_shape_stream: the library's own streaming "
                                   "probe moving the same bytes (reads and writes) with the "
-                                  "kernels' loads and stores"}
+                                  "kernels' loads and stores; dram_peak: ncu's DRAM peak for "
+                                  "this GPU (profiles/dram_traffic.txt)"}
 
     # ---- extras: SwiGLU and the L2-resident sweep
     if not args.no_extras:
