@@ -61,9 +61,12 @@ __device__ __forceinline__ void st_stream(uint16_t *p, const uint4 &v) {
 // wait, while this grid still streams: measured on GB300, 6-25 % off
 // launches of 0.5-8 M elements (L2-resident), no change at HBM sizes.  The
 // dense kernel releases earlier, right after its loads are issued, where
-// that measured faster still: one-input launches of one chunk per thread
-// (below ~1.2 M elements) and multi-input launches whose grid is resident at
-// once (at most 8 blocks per SM) -- 5-12 % off 0.25-4 M elements.
+// that measured faster still: one-input and two-input one-output launches of
+// one chunk per thread (below ~1.2 M and ~2.4 M elements) -- 5-22 % off
+// 0.25-2.4 M elements.  Everywhere else, and for the three-input SwiGLU
+// backward at every size, the release after the stores measured faster
+// (8-23 % off 0.25-2 M-element SwiGLU backward launches, 8-18 % off two-input
+// launches of two chunks per thread at 2.5-4 M elements).
 // Ordering between kernels is unchanged.  (Both are no-ops for a launch
 // without the programmatic-serialisation attribute.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -80,12 +83,15 @@ __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
 // Chunks of 8 elements per stream per thread: two for single-input
 // operations, one for multi-input ones (measured on GB300 with a one-pass
 // grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes at HBM
-// sizes).  Smaller flat calls of the dense kernel (measured over 256 K-268 M
-// elements, 256-thread blocks, release after the stores):
+// sizes).  Smaller flat and rows-mode calls of the dense kernel (measured
+// over 256 K-268 M elements, 256-thread blocks; dense_shape below):
 //  * single input: one chunk per thread while two would give fewer than two
 //    blocks per SM (below ~1.2 M elements);
-//  * two inputs, one output: two chunks per thread while that grid holds 1 to
-//    16 blocks per SM (~0.6-10 M elements: 5-25 % faster there), one above.
+//  * two inputs, one output: one chunk per thread while that grid holds at
+//    most 8 blocks per SM (below ~2.4 M elements), then two while the
+//    two-chunk grid holds at most 16 blocks per SM (~2.4-10 M elements:
+//    8-18 % faster at 2.5-4 M for the polynomial programs of 3-5 FMAs, within
+//    2 % for the lighter even-form derivatives), one above.
 template <class Op>
 __host__ __device__ constexpr int chunks_per_thread() {
   return Op::NIN == 1 ? 2 : 1;
@@ -473,15 +479,42 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// A dense-kernel launch, releasing its dependents where pdl_release says.
-template <class Op, int MODE, int U>
-cudaError_t launch_dense(int64_t blocks, cudaStream_t stream, const Streams &s, DenseArgs a,
+// Chunks per thread and release point of a flat or rows-mode dense-kernel
+// launch over nvec chunks (the rules above chunks_per_thread and pdl_wait).
+struct DenseShape {
+  int u;
+  uint32_t release_at;
+};
+template <class Op>
+DenseShape dense_shape(int64_t nvec) {
+  const int64_t sms = sm_count();
+  const int64_t one = (nvec + kThreads - 1) / kThreads;             // U = 1 grid
+  const int64_t two = (nvec + 2 * kThreads - 1) / (2 * kThreads);   // U = 2 grid
+  if constexpr (Op::NIN == 1) {
+    if (two < 2 * sms) return {1, kReleaseAfterLoads};
+    return {2, kReleaseAtEnd};
+  } else if constexpr (Op::NIN == 2 && Op::NOUT == 1) {
+    if (one <= 8 * sms) return {1, kReleaseAfterLoads};
+    if (two <= kTwoChunkMaxBlocksPerSm * sms) return {2, kReleaseAtEnd};
+    return {1, kReleaseAtEnd};
+  } else {
+    return {1, kReleaseAtEnd};
+  }
+}
+
+// A flat or rows-mode dense-kernel launch in the shape dense_shape gives.
+template <class Op, int MODE>
+cudaError_t launch_dense(cudaStream_t stream, const Streams &s, DenseArgs a,
                          const typename Op::Params &p) {
-  if (Op::NIN == 1)
-    a.release_at = U == 1 ? kReleaseAfterLoads : kReleaseAtEnd;
-  else
-    a.release_at = blocks <= 8 * (int64_t)sm_count() ? kReleaseAfterLoads : kReleaseAtEnd;
-  return launch_pdl(dense_kernel<Op, MODE, U>, blocks, kThreads, stream, s, a, p);
+  const DenseShape sh = dense_shape<Op>(a.nvec);
+  a.release_at = sh.release_at;
+  const int64_t per = (int64_t)kThreads * sh.u;
+  int64_t blocks = ((int64_t)a.nvec + per - 1) / per;
+  if (blocks < 1) blocks = 1;
+  if constexpr (Op::NIN == 1 || (Op::NIN == 2 && Op::NOUT == 1)) {
+    if (sh.u == 2) return launch_pdl(dense_kernel<Op, MODE, 2>, blocks, kThreads, stream, s, a, p);
+  }
+  return launch_pdl(dense_kernel<Op, MODE, 1>, blocks, kThreads, stream, s, a, p);
 }
 
 // Every stream of s starts on a 16-byte boundary (unused streams are null).
@@ -515,9 +548,7 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
         row_divisor(a.cpr, a.mul, a.shift);
         for (int k = 0; k < 3; ++k) a.ld_in[k] = (uint32_t)l.ld_in[k];
         for (int k = 0; k < 2; ++k) a.ld_out[k] = (uint32_t)l.ld_out[k];
-        int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
-        if (blocks < 1) blocks = 1;
-        return launch_dense<Op, kDenseRows, U>(blocks, stream, s, a, p);
+        return launch_dense<Op, kDenseRows>(stream, s, a, p);
       }
       const int64_t blocks = grid_for(l, l.vec ? 8 : 1);
       return launch_pdl(strided_kernel<Op>, blocks, kThreads, stream, s, l, p);
@@ -528,20 +559,7 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     DenseArgs a{};
     a.nvec = (uint32_t)(l.n >> 3);
     a.ntail = (uint32_t)(l.n & 7);
-    int64_t blocks = ((int64_t)a.nvec * 8 + per_block - 1) / per_block;
-    if (blocks < 1) blocks = 1;
-    const int64_t two = ((int64_t)a.nvec + 2 * kThreads - 1) / (2 * kThreads);   // U = 2 grid
-    if constexpr (U > 1) {
-      if (two < 2 * (int64_t)sm_count()) {
-        blocks = ((int64_t)a.nvec + kThreads - 1) / kThreads;
-        if (blocks < 1) blocks = 1;
-        return launch_dense<Op, kDenseFlat, 1>(blocks, stream, s, a, p);
-      }
-    } else if constexpr (Op::NIN == 2 && Op::NOUT == 1) {
-      if (two >= sm_count() && two <= (int64_t)kTwoChunkMaxBlocksPerSm * sm_count())
-        return launch_dense<Op, kDenseFlat, 2>(two, stream, s, a, p);
-    }
-    return launch_dense<Op, kDenseFlat, U>(blocks, stream, s, a, p);
+    return launch_dense<Op, kDenseFlat>(stream, s, a, p);
   }
   if (l.mode == kRagged && l.cols % 8 == 0 && l.cap_rows * l.cols < lim && aligned16(s)) {
     DenseArgs a{};
@@ -552,7 +570,11 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     a.cols = (uint32_t)l.cols;
     int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
     if (blocks < 1) blocks = 1;
-    return launch_dense<Op, kDenseRagged, U>(blocks, stream, s, a, p);
+    // the row range is known on the device only: the shape of the capacity
+    a.release_at = Op::NIN == 2 && Op::NOUT == 1 && blocks <= 8 * (int64_t)sm_count()
+                       ? kReleaseAfterLoads
+                       : kReleaseAtEnd;
+    return launch_pdl(dense_kernel<Op, kDenseRagged, U>, blocks, kThreads, stream, s, a, p);
   }
   // streams that disagree modulo 16 while the outputs agree: realigned
   // 16-byte accesses instead of one element per load

@@ -397,16 +397,15 @@ def test_chunk_shape_switch_sizes():
 
 
 def test_two_input_launch_shape_switch_sizes():
-    """Two-input calls change shape with size: one chunk per thread below one
-    two-chunk block per SM, two chunks up to 16 such blocks per SM, one above;
-    the next launch is released after the loads while the grid is resident at
-    once (at most 8 blocks per SM), after the stores beyond.  Sizes on both
+    """Two-input one-output calls change shape with size: one chunk per thread
+    while that grid holds at most 8 blocks per SM (the next launch released
+    after the loads), two chunks while the two-chunk grid holds at most 16
+    blocks per SM, one above (both released after the stores).  Sizes on both
     sides of every switch, with and without a tail, for the backward program
-    and the SwiGLU forward: every element against the oracle's tables."""
+    and the SwiGLU forward, flat and on the halves of a fused gate-up buffer
+    (rows mode): every element against the oracle's tables."""
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
-    per_two_chunk_block = 256 * 2 * 8
-    edges = [sms * per_two_chunk_block, 8 * sms * per_two_chunk_block,
-             16 * sms * per_two_chunk_block]
+    edges = [8 * sms * 256 * 8, 16 * sms * 256 * 2 * 8]
     dt = B.POLY_F16
     op = oracle_program(B.POLY_SIGMOID, B.POLY_BWD, dt)
     s_op = oracle_program(B.POLY_SILU, B.POLY_FWD, dt)
@@ -426,6 +425,16 @@ def test_two_input_launch_shape_switch_sizes():
                                   z[:n].view(n // 8, 8))
                 assert _equal_bits(z[:n], _rn_mul(_apply_lut(s_op, xd[:n]), dyd[:n])), (edge, n)
                 assert bool((z[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
+        cols = 1024
+        for rows in (edge // cols - 3, edge // cols, edge // cols + 1, edge // cols + 4):
+            n = rows * cols
+            g, u = xd[:n].view(rows, cols), dyd[:n].view(rows, cols)
+            gu = torch.cat([g, u], dim=1)
+            zb = torch.full((rows, cols + 8), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
+            B.poly_swiglu_fwd(dt, gu[:, :cols], gu[:, cols:], zb[:, :cols])
+            want = _rn_mul(_apply_lut(s_op, xd[:n]), dyd[:n])
+            assert _equal_bits(zb[:, :cols].reshape(-1), want), (edge, rows)
+            assert bool((zb[:, cols:].view(torch.int16) == 0x5A5A).all()), (edge, rows)
 
 
 @pytest.mark.parametrize("dt", DTS)
