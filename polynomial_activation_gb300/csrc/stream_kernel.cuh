@@ -97,7 +97,7 @@ __host__ __device__ constexpr int chunks_per_thread() {
   return Op::NIN == 1 ? 2 : 1;
 }
 constexpr int kTwoChunkMaxBlocksPerSm = 16;
-constexpr int64_t kRowsTwoOutMax = int64_t(1) << 19;
+constexpr int64_t kRowsTwoOutMax = int64_t(1) << 23;
 
 template <class Op>
 __device__ __forceinline__ void apply_chunk(const uint4 (&in)[Op::NIN], uint4 (&out)[Op::NOUT],
@@ -536,8 +536,9 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
   if constexpr (Op::TWO_D) {
     if (l.mode == kStrided) {
       // two-output operations (the SwiGLU backward) keep the strided kernel
-      // above 2^19 chunks: measured 3-8 % faster there on GB300, while the
-      // rows mode wins below and for every single-output operation
+      // above 2^23 chunks (67 M elements): within +-2 % of the rows mode at
+      // 117 M on GB300, while the rows mode wins below (3-22 % at 4-56 M on
+      // fused gate-up halves) and for every single-output operation
       bool fast = l.vec && l.rows * (l.cols >> 3) < (Op::NOUT == 1 ? lim : kRowsTwoOutMax);
       for (int k = 0; k < 3; ++k) fast &= (l.rows - 1) * l.ld_in[k] + l.cols < lim;
       for (int k = 0; k < 2; ++k) fast &= (l.rows - 1) * l.ld_out[k] + l.cols < lim;

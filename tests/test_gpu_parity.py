@@ -973,14 +973,15 @@ def test_swiglu_fused_gate_up_halves(dt, H):
     assert np.array_equal(got[:, :H], wdg) and np.array_equal(got[:, H:], wdu)
 
 
-def test_swiglu_fused_halves_large_every_element():
-    """Gate / up and dg / du as halves of [T, 2H] buffers above the size at
-    which the backward changes kernel (T = 2100, H = 2048: 537,600 chunks of
-    8), every element through the oracle's exhaustive tables, products
-    rounded once."""
+@pytest.mark.parametrize("T,H", [(2100, 2048), (8200, 8192)])
+def test_swiglu_fused_halves_large_every_element(T, H):
+    """Gate / up and dg / du as halves of [T, 2H] buffers on both sides of the
+    size at which the backward leaves the dense rows mode for the strided
+    kernel (2^23 chunks of 8: T = 2100, H = 2048 gives 537,600 chunks, below;
+    T = 8200, H = 8192 gives 8,396,800, above), every element through the
+    oracle's exhaustive tables, products rounded once."""
     dt = B.POLY_BF16
     s_op, d_op = _swiglu_ops(dt)
-    T, H = 2100, 2048
     rng = np.random.default_rng(97)
     gu = to_dev(_rand_bits(rng, T * 2 * H, "bf16"), dt).view(T, 2 * H)
     dyd = to_dev(_rand_bits(rng, T * H, "bf16"), dt).view(T, H)
