@@ -191,25 +191,31 @@ def swiglu(g, u, rule=None):
         return swiglu_fwd(_rows(g), _rows(u), rule=rule)
     b = _fused_base(g, u)
     if b is not None:
-        return PolySwiGLUPacked.apply(b, rule).view(g.shape)
+        y = PolySwiGLUPacked.apply(b, rule)
+        return y if y.shape == g.shape else y.view(g.shape)
     return PolySwiGLU.apply(g, u, rule)
 
 
 def _halves(gu):
-    """[rows, 2H] row-major view of a fused gate-up buffer and its two halves."""
+    """[rows, 2H] row-major view of a fused gate-up buffer, H, the leading
+    dimension, and the addresses of the two halves (raw addresses rather
+    than slice tensors: two slices cost more host time than the call)."""
     two_h = gu.shape[-1]
     if two_h % 2:
         raise ValueError("the last dimension of a fused gate-up buffer must be even")
     gu2 = gu if gu.dim() == 2 and gu.stride(1) == 1 else _dense(gu).view(-1, two_h)
     h = two_h // 2
-    return gu2, gu2[:, :h], gu2[:, h:]
+    p = gu2.data_ptr()
+    return gu2, h, gu2.stride(0), p, p + h * gu2.element_size()
 
 
 def _packed_fwd(gu, rule):
-    gu2, g, u = _halves(gu)
-    y = torch.empty((gu2.shape[0], g.shape[1]), dtype=gu.dtype, device=gu.device)
-    B.poly_swiglu_fwd_v(rule, _dt(gu), g, u, y)
-    return y.view(*gu.shape[:-1], g.shape[1])
+    gu2, h, ld, gp, up = _halves(gu)
+    rows = gu2.shape[0]
+    y = torch.empty((rows, h), dtype=gu.dtype, device=gu.device)
+    # the halves lie inside gu2 by construction; y carries the device check
+    B.poly_swiglu_fwd_v(rule, _dt(gu), gp, up, y, rows=rows, cols=h, ldg=ld, ldu=ld, ldy=h)
+    return y.view(*gu.shape[:-1], h)
 
 
 class PolySwiGLUPacked(torch.autograd.Function):
@@ -227,11 +233,13 @@ class PolySwiGLUPacked(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         (gu,) = ctx.saved_tensors
-        gu2, g, u = _halves(gu)
-        h = g.shape[1]
-        dgu = torch.empty((gu2.shape[0], 2 * h), dtype=gu.dtype, device=gu.device)
-        B.poly_swiglu_bwd_v(ctx.rule, _dt(gu), g, u, _dense(dy).view(-1, h), dgu[:, :h],
-                            dgu[:, h:])
+        gu2, h, ld, gp, up = _halves(gu)
+        rows = gu2.shape[0]
+        dgu = torch.empty((rows, 2 * h), dtype=gu.dtype, device=gu.device)
+        dyv = _dense(dy).view(-1, h)
+        dp = dgu.data_ptr()
+        B.poly_swiglu_bwd_v(ctx.rule, _dt(gu), gp, up, dyv, dp, dp + h * dgu.element_size(),
+                            rows=rows, cols=h, ldg=ld, ldu=ld, lddy=h, lddg=2 * h, lddu=2 * h)
         return dgu.view(gu.shape), None
 
 
