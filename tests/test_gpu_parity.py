@@ -1682,8 +1682,9 @@ def test_wrappers_without_autograd_match_recorded_calls():
 def test_swiglu_packed_gate_up_buffer(variant):
     """ops.swiglu_packed on a fused [.., 2H] gate-up buffer: the same bits as
     the separate-tensor SwiGLU, forward and backward, with the gradient
-    written as one [.., 2H] tensor; 2-D and 3-D, recorded and not; under
-    both SwiGLU rules."""
+    written as one [.., 2H] tensor; 2-D and 3-D, recorded and not, and
+    2-D views of wider buffers (a leading dimension above 2H, at an aligned
+    and at an odd element offset); under both SwiGLU rules."""
     from polynomial_activation_gb300 import ops
     rng = np.random.default_rng(79)
     B.poly_set_swiglu_variant(variant)
@@ -1695,9 +1696,15 @@ def test_swiglu_packed_gate_up_buffer(variant):
 
 def _packed_cases(ops, rng):
     for dt in DTS:
-        for shape in ((64, 2 * 200), (3, 7, 2 * 48)):
+        for shape, pad, off in (((64, 2 * 200), 0, 0), ((3, 7, 2 * 48), 0, 0),
+                                ((40, 2 * 64), 24, 8), ((40, 2 * 64), 24, 3)):
             m = int(np.prod(shape))
-            gu = to_dev(_rand_bits(rng, m, FMT[dt]), dt).view(*shape)
+            if pad:
+                rows, w = shape
+                big = to_dev(_rand_bits(rng, rows * (w + pad), FMT[dt]), dt).view(rows, w + pad)
+                gu = big[:, off:off + w]
+            else:
+                gu = to_dev(_rand_bits(rng, m, FMT[dt]), dt).view(*shape)
             dy = to_dev(_rand_bits(rng, m // 2, FMT[dt]), dt).view(*shape[:-1], shape[-1] // 2)
             h = shape[-1] // 2
             g, u = gu[..., :h].contiguous(), gu[..., h:].contiguous()
@@ -1705,14 +1712,21 @@ def _packed_cases(ops, rng):
             got = ops.swiglu_packed(gu)
             assert got.shape == want.shape and got.grad_fn is None
             assert torch.equal(got.view(torch.int16), want.view(torch.int16))
-            gur = gu.clone().requires_grad_(True)
+            if pad:   # the recorded input is itself a view of the wider buffer
+                bigr = big.clone().requires_grad_(True)
+                gur = bigr[:, off:off + shape[1]]
+            else:
+                gur = gu.clone().requires_grad_(True)
             y = ops.swiglu_packed(gur)
             assert torch.equal(y.detach().view(torch.int16), want.view(torch.int16))
             y.backward(dy)
+            grad = bigr.grad[:, off:off + shape[1]] if pad else gur.grad
             dg, du = ops.swiglu_bwd(g.reshape(-1, h), u.reshape(-1, h), dy.reshape(-1, h))
-            assert gur.grad.shape == gu.shape
-            assert torch.equal(gur.grad[..., :h].reshape(-1, h).view(torch.int16), dg.view(torch.int16))
-            assert torch.equal(gur.grad[..., h:].reshape(-1, h).view(torch.int16), du.view(torch.int16))
+            assert grad.shape == gu.shape
+            assert torch.equal(grad[..., :h].reshape(-1, h).view(torch.int16), dg.view(torch.int16))
+            assert torch.equal(grad[..., h:].reshape(-1, h).view(torch.int16), du.view(torch.int16))
+            if pad:
+                assert not bool(bigr.grad[:, :off].any()) and not bool(bigr.grad[:, off + shape[1]:].any())
 
 
 def test_swiglu_on_chunked_halves_takes_the_fused_path():
