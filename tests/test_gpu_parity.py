@@ -401,24 +401,39 @@ def test_two_input_launch_shape_switch_sizes():
     while that grid holds at most 8 blocks per SM (the next launch released
     after the loads), two chunks while the two-chunk grid holds at most 16
     blocks per SM, one above (both released after the stores).  Sizes on both
-    sides of every switch, with and without a tail, for the backward program
-    and the SwiGLU forward, flat and on the halves of a fused gate-up buffer
-    (rows mode): every element against the oracle's tables."""
+    sides of every switch, with and without a tail, for the σ′ and GELU′
+    backward programs (FP16), the SwiGLU forward (FP16) and its sigmoid rule
+    (BF16), flat and on the halves of a fused gate-up buffer (rows mode):
+    every element against the oracle's tables."""
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
     edges = [8 * sms * 256 * 8, 16 * sms * 256 * 2 * 8]
-    dt = B.POLY_F16
+    dt, bf = B.POLY_F16, B.POLY_BF16
     op = oracle_program(B.POLY_SIGMOID, B.POLY_BWD, dt)
+    gelu_op = oracle_program(B.POLY_GELU, B.POLY_BWD, dt)
     s_op = oracle_program(B.POLY_SILU, B.POLY_FWD, dt)
+    sig_bf = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, bf)
     top = edges[-1] + 8192
     rng = np.random.default_rng(83)
     xd = to_dev(_rand_bits(rng, top, "f16"), dt)
     dyd = to_dev(_rand_bits(rng, top, "f16"), dt)
+    xb = to_dev(_rand_bits(rng, top, "bf16"), bf)
+    ub = to_dev(_rand_bits(rng, top, "bf16"), bf)
     for edge in edges:
         for n in (edge - 4096 - 3, edge - 8, edge, edge + 5, edge + 8, edge + 4096):
             y = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
             B.poly_act_bwd(B.POLY_SIGMOID, dt, xd[:n], dyd[:n], y[:n], n)
             assert _equal_bits(y[:n], _rn_mul(dyd[:n], _apply_lut(op, xd[:n]))), (edge, n)
             assert bool((y[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
+            B.poly_act_bwd(B.POLY_GELU, dt, xd[:n], dyd[:n], y[:n], n)
+            assert _equal_bits(y[:n], _rn_mul(dyd[:n], _apply_lut(gelu_op, xd[:n]))), (edge, n)
+            assert bool((y[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
+            if n % 8 == 0:
+                zb = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[bf])
+                B.poly_swiglu_fwd_v(B.POLY_SWIGLU_SIGMOID, bf, xb[:n].view(n // 8, 8),
+                                    ub[:n].view(n // 8, 8), zb[:n].view(n // 8, 8))
+                want = _rn_mul(_rn_mul(xb[:n], _apply_lut(sig_bf, xb[:n])), ub[:n])
+                assert _equal_bits(zb[:n], want), (edge, n)
+                assert bool((zb[n:].view(torch.int16) == 0x5A5A).all()), (edge, n)
             if n % 8 == 0:
                 z = torch.full((n + 16,), 0x5A5A, dtype=torch.int16, device=DEV).view(TDT[dt])
                 B.poly_swiglu_fwd(dt, xd[:n].view(n // 8, 8), dyd[:n].view(n // 8, 8),
