@@ -83,8 +83,9 @@ __device__ __forceinline__ uint16_t ld_one(const uint16_t *p) {
 // Chunks of 8 elements per stream per thread: two for single-input
 // operations, one for multi-input ones (measured on GB300 with a one-pass
 // grid: the fastest of 1, 2, 4 and 8 chunks of 16 or 32 bytes at HBM
-// sizes).  Smaller flat and rows-mode calls of the dense kernel (measured
-// over 256 K-268 M elements, 256-thread blocks; dense_shape below):
+// sizes).  Smaller calls of the dense kernel, flat, rows or ragged (the
+// latter by row capacity), measured over 256 K-268 M elements with
+// 256-thread blocks (dense_shape below):
 //  * single input: one chunk per thread while two would give fewer than two
 //    blocks per SM (below ~1.2 M elements);
 //  * two inputs, one output: one chunk per thread while that grid holds at
@@ -479,8 +480,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t blocks, int threads, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Chunks per thread and release point of a flat or rows-mode dense-kernel
-// launch over nvec chunks (the rules above chunks_per_thread and pdl_wait).
+// Chunks per thread and release point of a dense-kernel launch over nvec
+// chunks (the rules above chunks_per_thread and pdl_wait).
 struct DenseShape {
   int u;
   uint32_t release_at;
@@ -502,7 +503,7 @@ DenseShape dense_shape(int64_t nvec) {
   }
 }
 
-// A flat or rows-mode dense-kernel launch in the shape dense_shape gives.
+// A dense-kernel launch in the shape dense_shape gives.
 template <class Op, int MODE>
 cudaError_t launch_dense(cudaStream_t stream, const Streams &s, DenseArgs a,
                          const typename Op::Params &p) {
@@ -530,8 +531,6 @@ inline bool aligned16(const Streams &s) {
 template <class Op>
 cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Params &p,
                       cudaStream_t stream) {
-  constexpr int U = chunks_per_thread<Op>();
-  const int64_t per_block = (int64_t)kThreads * 8 * U;
   const int64_t lim = int64_t(1) << 31;
   if constexpr (Op::TWO_D) {
     if (l.mode == kStrided) {
@@ -569,13 +568,10 @@ cudaError_t launch_op(const Streams &s, const Layout &l, const typename Op::Para
     a.cap_rows = (int32_t)l.cap_rows;
     a.status = l.status;
     a.cols = (uint32_t)l.cols;
-    int64_t blocks = (l.cap_rows * l.cols + per_block - 1) / per_block;
-    if (blocks < 1) blocks = 1;
-    // the row range is known on the device only: the shape of the capacity
-    a.release_at = Op::NIN == 2 && Op::NOUT == 1 && blocks <= 8 * (int64_t)sm_count()
-                       ? kReleaseAfterLoads
-                       : kReleaseAtEnd;
-    return launch_pdl(dense_kernel<Op, kDenseRagged, U>, blocks, kThreads, stream, s, a, p);
+    // the row range is known on the device only: the grid and shape are the
+    // capacity's (the kernel takes its own chunk count from the offsets)
+    a.nvec = (uint32_t)((l.cap_rows * l.cols) >> 3);
+    return launch_dense<Op, kDenseRagged>(stream, s, a, p);
   }
   // streams that disagree modulo 16 while the outputs agree: realigned
   // 16-byte accesses instead of one element per load

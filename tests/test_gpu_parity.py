@@ -855,6 +855,43 @@ def test_ragged_swiglu_full_size_sampled():
     assert _equal_bits(du[:rows], _rn_mul(dys, sg))
 
 
+def test_ragged_launch_shape_switch_sizes():
+    """Ragged calls take the dense kernel's launch shapes by row capacity
+    (one chunk per thread up to 8 blocks per SM, two up to 16, one above, for
+    the two-input forward): capacities on both sides of each edge, segments
+    covering all but the last rows; every row inside against the oracle's
+    tables and the rows past the last offset untouched, forward under both
+    SwiGLU rules and backward (BF16, 2048 columns)."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    cols = 2048
+    dt = B.POLY_BF16
+    s_op, d_op = _swiglu_ops(dt)
+    sig = oracle_program(B.POLY_SIGMOID, B.POLY_FWD, dt)
+    rng = np.random.default_rng(89)
+    for edge in (8 * sms * 256 * 8, 16 * sms * 256 * 2 * 8):
+        for cap in (edge // cols - 1, edge // cols, edge // cols + 1):
+            rows = cap - 5
+            segd = torch.from_numpy(np.linspace(0, rows, 9).astype(np.int32)).to(DEV)
+            gd, ud, dyd = (to_dev(_rand_bits(rng, cap * cols, "bf16"), dt).view(cap, cols)
+                           for _ in range(3))
+            fill = lambda: torch.full((cap, cols), 0x5A5A, dtype=torch.int16,
+                                      device=DEV).view(TDT[dt])
+            gs, us, dys = gd[:rows], ud[:rows], dyd[:rows]
+            sg = _apply_lut(s_op, gs)
+            y = fill()
+            B.poly_swiglu_fwd_ragged(dt, gd, ud, y, segd)
+            assert _equal_bits(y[:rows], _rn_mul(sg, us)), (edge, cap)
+            y2 = fill()
+            B.poly_swiglu_fwd_ragged_v(B.POLY_SWIGLU_SIGMOID, dt, gd, ud, y2, segd)
+            assert _equal_bits(y2[:rows], _rn_mul(_rn_mul(gs, _apply_lut(sig, gs)), us)), (edge, cap)
+            dg, du = fill(), fill()
+            B.poly_swiglu_bwd_ragged(dt, gd, ud, dyd, dg, du, segd)
+            assert _equal_bits(dg[:rows], _rn_mul(_rn_mul(dys, us), _apply_lut(d_op, gs))), (edge, cap)
+            assert _equal_bits(du[:rows], _rn_mul(dys, sg)), (edge, cap)
+            for t in (y, y2, dg, du):
+                assert bool((t.view(torch.int16)[rows:] == 0x5A5A).all()), (edge, cap)
+
+
 @pytest.mark.parametrize("cols", [24, 21])
 @pytest.mark.parametrize("dt", DTS)
 def test_ragged_small_every_element_and_status(dt, cols):
